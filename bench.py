@@ -1,0 +1,548 @@
+#!/usr/bin/env python
+"""Throughput of the batched power-of-two C2C FFT on one GB300 (or N, one
+process per GPU, each with its own full batch: weak scaling).
+
+Default workload (``--config c2``): 16384 transforms of 4096 fp32 complex
+points (512 MiB), a step = forward then inverse (1/N).  Inputs are larger
+than L2 (129 MB), so no flush between steps is needed.
+
+Metric: effective GB/s = algorithmic HBM bytes of the step / step time,
+where the algorithmic bytes of one transform call are (HBM passes of the
+chosen plan) x 2 x (bytes of the complex array); the on-chip path makes one
+pass.  Also reported: 5 N log2 N GFLOP/s, transforms/s, the roofline of
+the dominant kernel against the measured HBM copy bandwidth, the fp64 CPU
+oracle on a bounded sample, an end-to-end figure with host buffers, and
+the SM clocks sampled during the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c1..c5]
+    python bench.py --impl reference ...   # the fp64 CPU oracle, timed alone
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+GIB = float(1 << 30)
+
+
+def log2i(n: int) -> int:
+    return int(n).bit_length() - 1
+
+
+# ---------------------------------------------------------------------------
+# Workload descriptions (bytes / flops / units per step)
+# ---------------------------------------------------------------------------
+
+def workload_info(name: str, pass_log: int = 9):
+    c = workloads.CONFIGS[name]
+    n, batch = c["n"], c["batch"]
+    if c["kind"] == "fft1d":
+        elem = 8
+        arr = n * batch * elem
+        passes = 1 if log2i(n) <= 14 else max(2, math.ceil(log2i(n) / pass_log))
+        directions = 1 if name in ("c1", "c3") else 2
+        return dict(
+            kind="fft1d", n=n, batch=batch, passes=passes, directions=directions,
+            array_bytes=arr,
+            bytes_per_step=directions * passes * 2 * arr,
+            ideal_bytes_per_step=directions * 2 * arr,
+            flops_per_step=directions * 5.0 * n * log2i(n) * batch,
+            transforms_per_step=directions * batch,
+            h2d=arr, d2h=arr)
+    if c["kind"] == "fft2d":
+        arr = n * n * batch * 8
+        return dict(
+            kind="fft2d", n=n, batch=batch, passes=2, directions=2, array_bytes=arr,
+            bytes_per_step=2 * 2 * 2 * arr, ideal_bytes_per_step=2 * 2 * arr,
+            flops_per_step=2 * 5.0 * n * n * log2i(n * n) * batch,
+            transforms_per_step=2 * batch, h2d=arr, d2h=arr)
+    # polymul: fused ideal = int64 inputs read once + int64 output written once
+    nc = 2 * n - 1
+    L = 1 << (nc - 1).bit_length()
+    return dict(
+        kind="polymul", n=n, batch=batch, L=L, passes=None, directions=3,
+        array_bytes=batch * L * 16,
+        bytes_per_step=batch * (2 * n * 8 + nc * 8),
+        ideal_bytes_per_step=batch * (2 * n * 8 + nc * 8),
+        flops_per_step=3 * 5.0 * L * log2i(L) * batch,
+        transforms_per_step=3 * batch, h2d=batch * 2 * n * 8, d2h=batch * nc * 8)
+
+
+# ---------------------------------------------------------------------------
+# Clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Committed ncu traffic summary (null once the kernels have changed)
+# ---------------------------------------------------------------------------
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fft_convolution_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(config: str):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = data.get(config)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample of the same workload)
+# ---------------------------------------------------------------------------
+
+def cpu_oracle_sample(name: str, budget_s: float = 12.0):
+    """Times the fp64 oracle (recursive Cooley-Tukey; schoolbook-free fp64
+    pipeline for polymul) on a bounded sample of the workload and scales to
+    the metric's unit.  Single-threaded."""
+    import oracle
+    info = workload_info(name)
+    c = workloads.CONFIGS[name]
+    t0 = time.perf_counter()
+    done_units = 0.0  # fraction of one step's work
+    sample = ""
+    if info["kind"] == "fft1d":
+        n = c["n"]
+        if n <= 1 << 16:
+            x = workloads.config_input(name, scale_batch=min(c["batch"], 64)).astype(np.complex128)
+            k = 0
+            while time.perf_counter() - t0 < budget_s and k < x.shape[0] * 64:
+                r = x[k % x.shape[0]]
+                y = oracle.fft(r)
+                if info["directions"] == 2:
+                    oracle.ifft(y)
+                k += 1
+            done_units = k / c["batch"]
+            sample = f"{k} of {c['batch']} transforms of N={n}" + \
+                (" (forward+inverse)" if info["directions"] == 2 else "")
+        else:
+            # one long transform: time a 2^20 transform and scale by N log N
+            m = 1 << 20
+            x = workloads.normal_complex(m, 99, np.complex128)
+            k = 0
+            while time.perf_counter() - t0 < budget_s and k < 64:
+                oracle.fft(x)
+                k += 1
+            done_units = k * (m * log2i(m)) / (n * log2i(n))
+            sample = f"{k} transforms of N=2^20 scaled by N log2 N to N={n}"
+    elif info["kind"] == "fft2d":
+        n = c["n"]
+        img = workloads.normal_complex((1, n, n), 4, np.complex128)[0]
+        k = 0
+        while time.perf_counter() - t0 < budget_s and k < 8:
+            X = oracle.fft2d(img)
+            oracle.fft2d(X, +1)
+            k += 1
+        done_units = k / c["batch"]
+        sample = f"{k} of {c['batch']} images {n}x{n} (forward+inverse)"
+    else:
+        n = c["n"]
+        m = 1 << 16
+        a, b = workloads.poly_coeffs(m, 5)
+        k = 0
+        while time.perf_counter() - t0 < budget_s and k < 64:
+            oracle.polymul_fft(a, b)
+            k += 1
+        L, Lm = info["L"], 1 << (2 * m - 1 - 1).bit_length()
+        done_units = k * (Lm * log2i(Lm)) / (L * log2i(L)) / c["batch"]
+        sample = f"{k} fp64 products of 2^16-coefficient pairs, scaled by L log2 L"
+    el = time.perf_counter() - t0
+    gbs = info["bytes_per_step"] * done_units / el / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+            "seconds": round(el, 3)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import fft_convolution_gb300 as fg
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    name = args.config
+    c = workloads.CONFIGS[name]
+    info = workload_info(name)
+    stream = torch.cuda.Stream(device=dev)
+    sh = int(stream.cuda_stream)
+
+    # Inputs: seeded on the host, resident in HBM before timing.
+    if info["kind"] == "polymul":
+        a_h, b_h = workloads.config_input(name)
+        a_d, b_d = torch.from_numpy(a_h).to(dev), torch.from_numpy(b_h).to(dev)
+        c_d = torch.empty(c["batch"], 2 * c["n"] - 1, dtype=torch.int64, device=dev)
+        plans = []
+
+        def step(events=None):
+            with torch.cuda.stream(stream):
+                if events is not None:
+                    events[0].record(stream)
+                rc = fg.polymul_batched(a_d.data_ptr(), c["n"], b_d.data_ptr(), c["n"],
+                                        c_d.data_ptr(), c["batch"], sh)
+                if events is not None:
+                    events[1].record(stream)
+            assert rc == 0, fg.fft_status_string(rc)
+        kernels_per_step = 3 * max(1, math.ceil(log2i(info["L"]) / 9))
+    else:
+        x_h = workloads.config_input(name)
+        x_d = torch.from_numpy(x_h).to(dev)
+        y_d = torch.empty_like(x_d)
+        z_d = torch.empty_like(x_d)
+        dims = 2 if info["kind"] == "fft2d" else 1
+        n, batch = c["n"], c["batch"]
+        pf = fg.Plan(n, batch, dims, fg.FFT_FORWARD, fg.FFT_C2C_F32)
+        plans = [pf]
+        if info["directions"] == 2:
+            pi = fg.Plan(n, batch, dims, fg.FFT_INVERSE, fg.FFT_C2C_F32)
+            plans.append(pi)
+
+        def step(events=None):
+            rcs = []
+            if events is not None:
+                events[0].record(stream)
+            rcs.append(fg.fft_exec(pf.handle, x_d.data_ptr(), y_d.data_ptr(), sh))
+            if events is not None:
+                events[1].record(stream)
+            if len(plans) == 2:
+                rcs.append(fg.fft_exec(plans[1].handle, y_d.data_ptr(), z_d.data_ptr(), sh))
+                if events is not None:
+                    events[2].record(stream)
+            assert all(r == 0 for r in rcs), [fg.fft_status_string(r) for r in rcs]
+        kernels_per_step = sum(p.num_kernels for p in plans)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # Timed region.
+    nev = 3
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the work
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for k in range(args.steps):
+        step(ev[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    ms_step = ms_total / args.steps
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+        ms_step = ms_total / args.steps
+
+    # Per-launch durations of the dominant kernel (the forward transform;
+    # for 1-kernel plans that is one launch per exec).
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    inv_ms = [e[1].elapsed_time(e[2]) for e in ev] if info["kind"] != "polymul" and \
+        info["directions"] == 2 else []
+
+    # End-to-end through the host-buffer entry point: pinned host input ->
+    # device, transforms, device -> pinned host output, every step.
+    e2e = None
+    if info["kind"] != "polymul" and not args.no_e2e:
+        h_in = torch.from_numpy(x_h).pin_memory()
+        h_out = torch.empty_like(h_in).pin_memory()
+        e2e_steps = max(1, min(args.steps, 5))
+
+        def e2e_step():
+            if len(plans) == 2:
+                plans[0].exec_host(h_in, None, x_d, y_d, stream)
+                plans[1].exec_host(None, h_out, y_d, z_d, stream)
+            else:
+                plans[0].exec_host(h_in, h_out, x_d, y_d, stream)
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = s0.elapsed_time(s1) / e2e_steps
+        e2e = {"value": info["bytes_per_step"] * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": info["h2d"], "d2h_bytes_per_step": info["d2h"],
+               "ms_per_step": round(e2e_ms, 4)}
+    elif info["kind"] == "polymul" and not args.no_e2e:
+        ha, hb = torch.from_numpy(a_h).pin_memory(), torch.from_numpy(b_h).pin_memory()
+        hc = torch.empty(c_d.shape, dtype=torch.int64).pin_memory()
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                a_d.copy_(ha, non_blocking=True)
+                b_d.copy_(hb, non_blocking=True)
+                rc = fg.polymul_batched(a_d.data_ptr(), c["n"], b_d.data_ptr(), c["n"],
+                                        c_d.data_ptr(), c["batch"], sh)
+                hc.copy_(c_d, non_blocking=True)
+            assert rc == 0
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(max(1, min(args.steps, 3))):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = s0.elapsed_time(s1) / max(1, min(args.steps, 3))
+        e2e = {"value": info["bytes_per_step"] * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": info["h2d"], "d2h_bytes_per_step": info["d2h"],
+               "ms_per_step": round(e2e_ms, 4)}
+
+    peak, peak_kind = measured_peaks()
+    value = info["bytes_per_step"] * world / (ms_step * 1e-3) / 1e9
+
+    if info["kind"] == "polymul":
+        dom_ms = statistics.mean(fwd_ms)
+        per_launch_bytes = info["bytes_per_step"]
+        dom_name = "polymul (whole fused pipeline, %d kernels)" % kernels_per_step
+    else:
+        dom_ms = statistics.mean(fwd_ms)
+        per_launch_bytes = info["bytes_per_step"] / info["directions"]
+        dom_name = ("fft_rows_kernel<float,%d,-1>" % log2i(c["n"])) if info["passes"] == 1 and \
+            info["kind"] == "fft1d" else "forward plan (%d kernels)" % plans[0].num_kernels
+    achieved = per_launch_bytes / (dom_ms * 1e-3) / 1e9
+    tr = committed_traffic(name)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": tr["traffic_bytes_per_launch"] if tr else None,
+                "kernel": dom_name, "peak_source": peak_kind,
+                "launch_ms": round(dom_ms, 4),
+                "inverse_launch_ms": round(statistics.mean(inv_ms), 4) if inv_ms else None}
+
+    line = {
+        "metric": "batched C2C FFT effective GB/s",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64" if info["kind"] == "polymul" else "f32",
+        "data": "synthetic (seeded)",
+        "config": {"workload": workload_label(name), "l2": "inputs larger than L2, no flush",
+                   "hbm_passes": info["passes"], "parallelism": f"replicas x{world}"},
+        "hbm_frac": round(value / world / peak, 4),
+        "ideal_1pass_frac": round(info["ideal_bytes_per_step"] / (ms_step * 1e-3) / 1e9 / peak, 4),
+        "gflops": round(info["flops_per_step"] * world / (ms_step * 1e-3) / 1e9, 1),
+        "transforms_per_s": round(info["transforms_per_step"] * world / (ms_step * 1e-3), 1),
+        "gpu_launches": kernels_per_step * args.steps,
+        "roofline": roofline,
+        "e2e": e2e,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(name)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for p in plans:
+        p.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def workload_label(name: str) -> str:
+    c = workloads.CONFIGS[name]
+    if name == "c1":
+        return "1D C2C forward, N=1024, batch 1, fp32"
+    if name == "c2":
+        return "1D C2C forward+inverse, N=4096, batch 16384, fp32 (512 MiB)"
+    if name == "c3":
+        return "1D C2C forward, N=2^26, batch 1, fp32 (512 MiB), multi-pass"
+    if name == "c4":
+        return "2D C2C forward+inverse, 2048x2048, batch 8, fp32"
+    return f"polymul, {c['batch']} pairs of 2^20 int64 coefficients, fp64 transforms of 2^21"
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the fp64 CPU oracle as it stands
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    name = args.config
+    info = workload_info(name)
+
+    def one_step():
+        return cpu_oracle_sample(name, budget_s=args.ref_step_seconds)
+    for _ in range(args.warmup):
+        one_step()
+    vals, secs, last = [], 0.0, None
+    for _ in range(args.steps):
+        last = one_step()
+        vals.append(last["value"])
+        secs += last["seconds"]
+    value = statistics.mean(vals)
+    ms_step = 1e3 * info["bytes_per_step"] / (value * 1e9)
+    line = {
+        "impl": "reference",
+        "metric": "batched C2C FFT effective GB/s",
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": workload_label(name), "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": last["sample"] + " per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(workloads.CONFIGS), default="c2")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,260 @@
+"""Python binding of the GB300 power-of-two FFT library (``libfftgb300.so``).
+
+A thin ctypes layer over the C ABI of ``include/fft_gb300.h``: the functions
+below carry the same names and arguments and only marshal them; every step
+of every transform runs in the library's CUDA kernels.  PyTorch is used only
+for device memory and streams (the tensor helpers at the end).
+
+Importing this package loads the in-tree shared library and raises
+``ImportError`` if it has not been built (``python -m
+fft_convolution_gb300.build``); there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfftgb300.so")
+
+FFT_OK = 0
+FFT_ERR_INVALID_ARG = 1
+FFT_ERR_NOT_POW2 = 2
+FFT_ERR_UNSUPPORTED = 3
+FFT_ERR_CUDA = 4
+FFT_ERR_ALLOC = 5
+FFT_ERR_MISALIGNED = 6
+
+FFT_FORWARD = -1
+FFT_INVERSE = +1
+
+FFT_C2C_F32 = 0
+FFT_C2C_F64 = 1
+
+# Every symbol the header declares, with its ctypes signature.
+_VP, _I64, _INT, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "fft_plan_create": (_VP, [_I64, _I64, _INT, _INT, _INT]),
+    "fft_plan_destroy": (None, [_VP]),
+    "fft_plan_workspace_bytes": (_SZ, [_VP]),
+    "fft_plan_num_kernels": (_INT, [_VP]),
+    "fft_exec": (_INT, [_VP, _VP, _VP, _VP]),
+    "fft_exec_host": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP]),
+    "polymul": (_INT, [_VP, _I64, _VP, _I64, _VP, _VP]),
+    "polymul_batched": (_INT, [_VP, _I64, _VP, _I64, _VP, _I64, _VP]),
+    "fft_debug_radix2_pass": (_INT, [_VP, _VP, _I64, _I64, _INT, _VP]),
+    "fft_last_status": (_INT, []),
+    "fft_status_string": (ctypes.c_char_p, [_INT]),
+    "fft_last_cuda_error": (ctypes.c_char_p, []),
+}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build the CUDA library first "
+            "(python -m fft_convolution_gb300.build); there is no CPU fallback")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+class FFTError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        msg = fft_status_string(status)
+        if status == FFT_ERR_CUDA or status == FFT_ERR_ALLOC:
+            msg += f" ({fft_last_cuda_error()})"
+        super().__init__(f"{what}: {msg} [status {status}]")
+        self.status = status
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != FFT_OK:
+        raise FFTError(rc, what)
+
+
+# ---- the C ABI, name for name -------------------------------------------------
+
+def fft_plan_create(n: int, batch: int, dims: int, direction: int, dtype: int) -> int:
+    """Returns the plan handle; raises FFTError with fft_last_status()."""
+    h = _lib.fft_plan_create(n, batch, dims, direction, dtype)
+    if not h:
+        raise FFTError(_lib.fft_last_status(), "fft_plan_create")
+    return h
+
+
+def fft_plan_destroy(plan: int) -> None:
+    _lib.fft_plan_destroy(plan)
+
+
+def fft_plan_workspace_bytes(plan: int) -> int:
+    return int(_lib.fft_plan_workspace_bytes(plan))
+
+
+def fft_plan_num_kernels(plan: int) -> int:
+    return int(_lib.fft_plan_num_kernels(plan))
+
+
+def fft_exec(plan: int, in_ptr: int, out_ptr: int, stream: int) -> int:
+    return _lib.fft_exec(plan, in_ptr, out_ptr, stream)
+
+
+def fft_exec_host(plan: int, host_in: int, host_out: int, dev_in: int, dev_out: int,
+                  stream: int) -> int:
+    return _lib.fft_exec_host(plan, host_in, host_out, dev_in, dev_out, stream)
+
+
+def polymul(a_ptr: int, na: int, b_ptr: int, nb: int, c_ptr: int, stream: int) -> int:
+    return _lib.polymul(a_ptr, na, b_ptr, nb, c_ptr, stream)
+
+
+def polymul_batched(a_ptr: int, na: int, b_ptr: int, nb: int, c_ptr: int, batch: int,
+                    stream: int) -> int:
+    return _lib.polymul_batched(a_ptr, na, b_ptr, nb, c_ptr, batch, stream)
+
+
+def fft_debug_radix2_pass(in_ptr: int, out_ptr: int, n: int, half: int, dtype: int,
+                          stream: int) -> int:
+    return _lib.fft_debug_radix2_pass(in_ptr, out_ptr, n, half, dtype, stream)
+
+
+def fft_last_status() -> int:
+    return int(_lib.fft_last_status())
+
+
+def fft_status_string(status: int) -> str:
+    return _lib.fft_status_string(status).decode()
+
+
+def fft_last_cuda_error() -> str:
+    return _lib.fft_last_cuda_error().decode()
+
+
+# ---- torch tensor helpers (allocation and streams only) ------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.complex64:
+        return FFT_C2C_F32
+    if t.dtype == torch.complex128:
+        return FFT_C2C_F64
+    raise TypeError(f"expected complex64 or complex128, got {t.dtype}")
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+class Plan:
+    """Owns one fft_plan handle: `batch` transforms of length n (dims=1)
+    or of n x n images (dims=2)."""
+
+    def __init__(self, n: int, batch: int = 1, dims: int = 1, direction: int = FFT_FORWARD,
+                 dtype: int = FFT_C2C_F32):
+        self.n, self.batch, self.dims = n, batch, dims
+        self.direction, self.dtype = direction, dtype
+        self.handle = fft_plan_create(n, batch, dims, direction, dtype)
+
+    @property
+    def workspace_bytes(self) -> int:
+        return fft_plan_workspace_bytes(self.handle)
+
+    @property
+    def num_kernels(self) -> int:
+        return fft_plan_num_kernels(self.handle)
+
+    def numel(self) -> int:
+        return self.batch * self.n * (self.n if self.dims == 2 else 1)
+
+    def exec(self, inp, out=None, stream=None):
+        """Run on device tensors (complex64 / complex128, contiguous)."""
+        torch = _torch()
+        if out is None:
+            out = torch.empty_like(inp)
+        if not (inp.is_cuda and out.is_cuda and inp.is_contiguous() and out.is_contiguous()):
+            raise ValueError("exec needs contiguous CUDA tensors")
+        if inp.numel() != self.numel() or out.numel() != self.numel():
+            raise ValueError(f"tensors must hold {self.numel()} elements")
+        if _dtype_code(inp) != self.dtype or _dtype_code(out) != self.dtype:
+            raise TypeError("tensor dtype does not match the plan")
+        _check(fft_exec(self.handle, inp.data_ptr(), out.data_ptr(), _stream_handle(stream)),
+               "fft_exec")
+        return out
+
+    def exec_host(self, host_in, host_out, dev_in, dev_out, stream=None):
+        """Host-staged run (see fft_exec_host); host tensors should be pinned."""
+        hin = host_in.data_ptr() if host_in is not None else None
+        hout = host_out.data_ptr() if host_out is not None else None
+        _check(fft_exec_host(self.handle, hin, hout, dev_in.data_ptr(), dev_out.data_ptr(),
+                             _stream_handle(stream)), "fft_exec_host")
+
+    def close(self):
+        if getattr(self, "handle", None):
+            fft_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def fft(x, direction: int = FFT_FORWARD, out=None, stream=None):
+    """Transforms along the last axis of a contiguous CUDA tensor."""
+    n = x.shape[-1]
+    p = Plan(n, x.numel() // n, 1, direction, _dtype_code(x))
+    try:
+        return p.exec(x, out, stream)
+    finally:
+        if stream is None:
+            _torch().cuda.current_stream().synchronize()
+        p.close()
+
+
+def fft2(x, direction: int = FFT_FORWARD, out=None, stream=None):
+    """2D transform of the last two (equal, power-of-two) axes."""
+    n = x.shape[-1]
+    if x.shape[-2] != n:
+        raise ValueError("2D transforms are N x N")
+    p = Plan(n, x.numel() // (n * n), 2, direction, _dtype_code(x))
+    try:
+        return p.exec(x, out, stream)
+    finally:
+        if stream is None:
+            _torch().cuda.current_stream().synchronize()
+        p.close()
+
+
+def polymul_tensors(a, b, out=None, stream=None):
+    """c = a * b for int64 CUDA tensors [batch, na] and [batch, nb]
+    (or 1D); returns [batch, na+nb-1]."""
+    torch = _torch()
+    squeeze = a.dim() == 1
+    a2 = a.reshape(1, -1) if squeeze else a
+    b2 = b.reshape(1, -1) if squeeze else b
+    if a2.dtype != torch.int64 or b2.dtype != torch.int64:
+        raise TypeError("polymul takes int64 coefficients")
+    batch, na = a2.shape
+    nb = b2.shape[1]
+    if b2.shape[0] != batch:
+        raise ValueError("a and b need the same batch")
+    if out is None:
+        out = torch.empty(batch, na + nb - 1, dtype=torch.int64, device=a.device)
+    a2, b2 = a2.contiguous(), b2.contiguous()
+    _check(polymul_batched(a2.data_ptr(), na, b2.data_ptr(), nb, out.data_ptr(), batch,
+                           _stream_handle(stream)), "polymul_batched")
+    return out.reshape(-1) if squeeze else out

@@ -1,0 +1,176 @@
+// fft_pass.cuh -- one HBM pass of a multi-pass transform, and the column
+// pass of the 2D transform.
+//
+// A transform of N = 2^log_n points that does not fit on chip is split into
+// passes N = L_0 L_1 ... ; pass k is one radix-L_k Stockham stage (the stage
+// of "Stockham FFT Butterfly Algorithm in Parallel GLSL", items 2-3, with
+// radix L_k instead of 2 -- see fft_device.cuh) whose L_k-point butterflies
+// are themselves whole on-chip transforms.  With previous block length m:
+//   butterfly i = q*m + p reads      in[i + u*N/L],            u < L
+//   multiplies input u by           W_{L m}^{p u}               (m > 1)
+//   and writes                       out[q*L*m + p + v*m],     v < L.
+// The first pass (m = 1) writes out[i*L + v]: a tile's results form one
+// contiguous block, which is staged through shared memory so that the HBM
+// writes stay coalesced.  The last pass (L*m = N) reads and writes the same
+// positions, so it may run in place.
+//
+// The 2D column pass is the same kernel with N = H*W, L = H, m = W and no
+// twiddle: it transforms every column of an H x W image in place.
+//
+// One block takes a tile of C consecutive butterflies (columns) i, so every
+// HBM access moves C contiguous complex values (C * 8 or C * 16 bytes, 64 KB
+// tiles: C = 16 fp32 columns for L = 512).  Within the tile column c lives in
+// shared memory at pad16(idx) * C + c: the C lanes that share a row touch C
+// consecutive slots, free of bank conflicts.
+#pragma once
+
+#include "fft_device.cuh"
+#include "internal.h"
+
+namespace fftgb {
+// Kernels and their launchers have internal linkage: every translation unit
+// that instantiates one owns its own copy, so no kernel is registered twice.
+namespace {
+
+template <typename T, int LOGL> struct PassConfig {
+  using P = StagePlan<LOGL>;
+  static constexpr long long TILE_BYTES_TARGET = 65536;
+  static constexpr long long C_RAW =
+      TILE_BYTES_TARGET / ((long long)P::L * (long long)sizeof(vec2_t<T>));
+  static constexpr int C = C_RAW < 1 ? 1 : (C_RAW > 64 ? 64 : (int)C_RAW);
+  static constexpr int THREADS = C * P::TP;
+  static constexpr int ROW_ELEMS =
+      P::SMEM_ELEMS > P::L + 1 ? P::SMEM_ELEMS : P::L + 1;  // exchange or transpose
+  static constexpr size_t SMEM = (size_t)C * ROW_ELEMS * sizeof(vec2_t<T>);
+};
+
+// Plain complex load / store (element `pos` of transform `b`).
+template <typename V> struct LoadComplex {
+  const V *p;
+  long long bstride;
+  __device__ __forceinline__ V operator()(long long b, long long pos) const {
+    return p[b * bstride + pos];
+  }
+};
+template <typename V> struct StoreComplex {
+  V *p;
+  long long bstride;
+  __device__ __forceinline__ void operator()(long long b, long long pos, V v) const {
+    p[b * bstride + pos] = v;
+  }
+};
+
+struct PassGeom {
+  int log_n;
+  int log_m;
+  int twiddle;
+  long long tiles;  // tiles per transform
+};
+
+template <typename T, int LOGL, int DIR, class Load, class Store>
+__global__ void __launch_bounds__(PassConfig<T, LOGL>::THREADS)
+    fft_pass_kernel(Load load, Store store, PassGeom g) {
+  using V = vec2_t<T>;
+  using P = StagePlan<LOGL>;
+  constexpr int C = PassConfig<T, LOGL>::C;
+  constexpr int L = P::L;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  V *smem = reinterpret_cast<V *>(smem_raw);
+
+  const int c = threadIdx.x % C;   // column within the tile
+  const int t = threadIdx.x / C;   // thread within the column
+  const long long tile = blockIdx.x % g.tiles;
+  const long long b = blockIdx.x / g.tiles;
+  const long long cols = 1LL << (g.log_n - LOGL);  // N / L butterflies
+  const long long i = tile * C + c;
+  const bool active = i < cols;
+
+  V x[P::E];
+  if (active) {
+#pragma unroll
+    for (int w = 0; w < P::E; ++w) x[w] = load(b, i + (long long)(t + w * P::TP) * cols);
+    if (g.twiddle && g.log_m > 0) {
+      // W_{L m}^{p u} for u = t + w*TP:  W^{p t} * (W^{p TP})^w.
+      const long long p = i & ((1LL << g.log_m) - 1);
+      const int log_lm = g.log_m + LOGL;
+      const V a = twiddle<DIR>(p * t, log_lm, T());
+      const V step = twiddle<DIR>(p * P::TP, log_lm, T());
+      V pw[P::E];
+      powers<P::E>(step, pw);
+#pragma unroll
+      for (int w = 0; w < P::E; ++w) x[w] = c_mul(x[w], c_mul(a, pw[w]));
+    }
+  } else {
+#pragma unroll
+    for (int w = 0; w < P::E; ++w) x[w] = make_c<V>((T)0, (T)0);
+  }
+
+  const SmemView<V> sm{smem + c, C};
+  fft_on_chip<LOGL, DIR>(x, t, sm);
+
+  if constexpr (DIR > 0) {
+#pragma unroll
+    for (int w = 0; w < P::E; ++w) x[w] = c_scale(x[w], (T)(1.0 / L));  // 1/L per pass
+  }
+
+  if (g.log_m == 0) {
+    // First pass: butterfly i's outputs go to i*L + v, so the tile's outputs
+    // are the contiguous block [tile*C*L, (tile+1)*C*L).  Stage them in
+    // shared memory (row c padded to L+1 slots) and write linearly.
+    constexpr int RS = L + 1;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < P::E; ++w) smem[c * RS + t + w * P::TP] = x[w];
+    __syncthreads();
+    const long long base = tile * C * L;
+#pragma unroll
+    for (int w = 0; w < P::E; ++w) {
+      const int o = threadIdx.x + w * PassConfig<T, LOGL>::THREADS;
+      const int cc = o / L, v = o % L;
+      if (tile * C + cc < cols) store(b, base + o, smem[cc * RS + v]);
+    }
+  } else if (active) {
+    const long long m = 1LL << g.log_m;
+    const long long q = i >> g.log_m, p = i & (m - 1);
+    const long long base = q * L * m + p;
+#pragma unroll
+    for (int w = 0; w < P::E; ++w) store(b, base + (long long)(t + w * P::TP) * m, x[w]);
+  }
+}
+
+template <typename T, int LOGL, int DIR, class Load, class Store>
+cudaError_t launch_pass_t(Load load, Store store, int log_n, int log_m, int twiddle,
+                          long long batch, cudaStream_t st) {
+  using C = PassConfig<T, LOGL>;
+  auto kern = fft_pass_kernel<T, LOGL, DIR, Load, Store>;
+  if (C::SMEM > 48 * 1024) {
+    static cudaError_t attr = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    if (attr != cudaSuccess) return attr;
+  }
+  const long long cols = 1LL << (log_n - LOGL);
+  PassGeom g{log_n, log_m, twiddle, (cols + C::C - 1) / C::C};
+  const long long grid = g.tiles * batch;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM, st>>>(load, store, g);
+  return cudaGetLastError();
+}
+
+template <typename T, int DIR, int MAXLOG, int LOGL = 1>
+cudaError_t dispatch_pass(const PassArgs &a, const void *in, void *out, cudaStream_t st) {
+  if constexpr (LOGL > MAXLOG) {
+    return cudaErrorInvalidValue;
+  } else {
+    if (a.log_l == LOGL) {
+      using V = vec2_t<T>;
+      const long long n = 1LL << a.log_n;
+      return launch_pass_t<T, LOGL, DIR>(LoadComplex<V>{static_cast<const V *>(in), n},
+                                         StoreComplex<V>{static_cast<V *>(out), n}, a.log_n,
+                                         a.log_m, a.twiddle, a.batch, st);
+    }
+    return dispatch_pass<T, DIR, MAXLOG, LOGL + 1>(a, in, out, st);
+  }
+}
+
+}  // namespace
+}  // namespace fftgb

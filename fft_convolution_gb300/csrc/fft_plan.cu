@@ -1,0 +1,296 @@
+// fft_plan.cu -- host side of the library: plans, argument checks, the
+// choice of kernels, and the exported C ABI declared in include/fft_gb300.h.
+//
+// The pages' own boundary is `solve(signal, spectrum, N)` on interleaved
+// fp32 device buffers ("FFT on GPU", section FFT on GPU), which launches one
+// kernel per butterfly stage with a device-wide synchronisation after each.
+// Here a plan fixes the kernel sequence once; fft_exec only enqueues it on
+// the caller's stream (1 kernel for on-chip lengths, 2 for 2D, 2-4 for long
+// 1D transforms) and never synchronises.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "../../include/fft_gb300.h"
+#include "internal.h"
+
+using namespace fftgb;
+
+namespace {
+
+thread_local int g_status = FFT_OK;
+thread_local cudaError_t g_cuda_error = cudaSuccess;
+
+enum Kind { KIND_ROWS = 0, KIND_MULTI = 1, KIND_2D = 2 };
+
+constexpr int kMaxPasses = 8;
+
+int ilog2_exact(int64_t n) {
+  int l = 0;
+  while (((int64_t)1 << l) < n) ++l;
+  return l;
+}
+
+bool is_pow2(int64_t n) { return n > 0 && (n & (n - 1)) == 0; }
+
+int cuda_fail(cudaError_t e) {
+  g_cuda_error = e;
+  return e == cudaErrorMemoryAllocation ? FFT_ERR_ALLOC : FFT_ERR_CUDA;
+}
+
+bool misaligned(const void *p) { return ((uintptr_t)p & 15u) != 0; }
+
+// Largest on-chip factor (log2) per HBM pass of a long 1D transform.  The
+// default 9 keeps every pass tile at 64 KB with 16 (fp32) / 8 (fp64)
+// contiguous columns; FFT_GB300_PASS_LOG overrides it (4 .. 14 fp32,
+// 4 .. 13 fp64) for tuning.
+int pass_log_limit(int dtype) {
+  int lim = 9;
+  const char *env = getenv("FFT_GB300_PASS_LOG");
+  if (env && *env) {
+    int v = atoi(env);
+    if (v >= 4) lim = v;
+  }
+  const int hard = dtype == FFT_C2C_F32 ? kPassMaxLogF32 : kPassMaxLogF64;
+  return lim > hard ? hard : lim;
+}
+
+cudaError_t launch_rows(int dtype, int logn, int dir, const void *in, void *out, long long batch,
+                        cudaStream_t st) {
+  return dtype == FFT_C2C_F32 ? launch_rows_f32(logn, dir, in, out, batch, st)
+                              : launch_rows_f64(logn, dir, in, out, batch, st);
+}
+
+cudaError_t launch_pass(int dtype, int dir, const PassArgs &a, const void *in, void *out,
+                        cudaStream_t st) {
+  return dtype == FFT_C2C_F32 ? launch_pass_f32(dir, a, in, out, st)
+                              : launch_pass_f64(dir, a, in, out, st);
+}
+
+}  // namespace
+
+struct fft_plan {
+  int64_t n;
+  int64_t batch;
+  int dims;
+  int direction;
+  int dtype;
+  int kind;
+  int logn;
+  int npasses;
+  int pass_log[kMaxPasses];
+  void *workspace;
+  size_t workspace_bytes;
+};
+
+extern "C" {
+
+fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int dtype) {
+  g_status = FFT_OK;
+  if (n <= 0 || batch <= 0 || (dims != 1 && dims != 2) ||
+      (direction != FFT_FORWARD && direction != FFT_INVERSE) ||
+      (dtype != FFT_C2C_F32 && dtype != FFT_C2C_F64)) {
+    g_status = FFT_ERR_INVALID_ARG;
+    return nullptr;
+  }
+  if (!is_pow2(n)) {
+    g_status = FFT_ERR_NOT_POW2;
+    return nullptr;
+  }
+  const int logn = ilog2_exact(n);
+  const int on_chip_max = dtype == FFT_C2C_F32 ? RowsMaxLog<float>::value : RowsMaxLog<double>::value;
+  const size_t elem = dtype == FFT_C2C_F32 ? 8 : 16;
+
+  fft_plan *p = new (std::nothrow) fft_plan;
+  if (!p) {
+    g_status = FFT_ERR_ALLOC;
+    return nullptr;
+  }
+  memset(p, 0, sizeof(*p));
+  p->n = n;
+  p->batch = batch;
+  p->dims = dims;
+  p->direction = direction;
+  p->dtype = dtype;
+  p->logn = logn;
+
+  if (dims == 2) {
+    if (logn > on_chip_max || batch > ((int64_t)1 << 40) / (n * n)) {
+      delete p;
+      g_status = FFT_ERR_UNSUPPORTED;
+      return nullptr;
+    }
+    p->kind = KIND_2D;
+    return p;
+  }
+  if (logn <= on_chip_max) {
+    p->kind = KIND_ROWS;
+    return p;
+  }
+  const int max_log_1d = dtype == FFT_C2C_F32 ? 30 : 29;
+  if (logn > max_log_1d || batch > ((int64_t)1 << 40) / n) {
+    delete p;
+    g_status = FFT_ERR_UNSUPPORTED;
+    return nullptr;
+  }
+  // Stockham passes over HBM: logn split into nearly equal factors of at
+  // most pass_log_limit bits, larger factors first.
+  const int lim = pass_log_limit(dtype);
+  int P = (logn + lim - 1) / lim;
+  if (P < 2) P = 2;
+  if (P > kMaxPasses) {
+    delete p;
+    g_status = FFT_ERR_UNSUPPORTED;
+    return nullptr;
+  }
+  p->kind = KIND_MULTI;
+  p->npasses = P;
+  for (int k = 0; k < P; ++k) p->pass_log[k] = logn / P + (k < logn % P ? 1 : 0);
+  p->workspace_bytes = (size_t)batch * (size_t)n * elem;
+  cudaError_t e = cudaMalloc(&p->workspace, p->workspace_bytes);
+  if (e != cudaSuccess) {
+    g_cuda_error = e;
+    delete p;
+    g_status = FFT_ERR_ALLOC;
+    return nullptr;
+  }
+  return p;
+}
+
+void fft_plan_destroy(fft_plan *plan) {
+  if (!plan) return;
+  if (plan->workspace) cudaFree(plan->workspace);
+  delete plan;
+}
+
+size_t fft_plan_workspace_bytes(const fft_plan *plan) { return plan ? plan->workspace_bytes : 0; }
+
+int fft_plan_num_kernels(const fft_plan *plan) {
+  if (!plan) return 0;
+  if (plan->kind == KIND_2D) return plan->logn == 0 ? 1 : 2;
+  return plan->kind == KIND_ROWS ? 1 : plan->npasses;
+}
+
+int fft_exec(const fft_plan *p, const void *in, void *out, void *stream) {
+  if (!p || !in || !out) return FFT_ERR_INVALID_ARG;
+  if (misaligned(in) || misaligned(out)) return FFT_ERR_MISALIGNED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int dir = p->direction;
+  cudaError_t e = cudaSuccess;
+  switch (p->kind) {
+    case KIND_ROWS:
+      e = launch_rows(p->dtype, p->logn, dir, in, out, p->batch, st);
+      break;
+    case KIND_2D: {
+      // Rows (contiguous axis), then columns in place.
+      e = launch_rows(p->dtype, p->logn, dir, in, out, p->batch * p->n, st);
+      if (e != cudaSuccess || p->logn == 0) break;  // 1 x 1: rows already did it
+      PassArgs a{2 * p->logn, p->logn, p->logn, 0, p->batch};
+      e = launch_pass(p->dtype, dir, a, out, out, st);
+      break;
+    }
+    case KIND_MULTI: {
+      // Pass k reads the previous pass's output; intermediates alternate
+      // between the workspace and `out`, the last pass always writes `out`
+      // (it reads and writes the same positions, so in place is safe).
+      int log_m = 0;
+      const void *src = in;
+      for (int k = 0; k < p->npasses; ++k) {
+        void *dst = (k == p->npasses - 1) ? out : (k % 2 == 0 ? p->workspace : out);
+        PassArgs a{p->logn, p->pass_log[k], log_m, 1, p->batch};
+        e = launch_pass(p->dtype, dir, a, src, dst, st);
+        if (e != cudaSuccess) break;
+        src = dst;
+        log_m += p->pass_log[k];
+      }
+      break;
+    }
+    default:
+      return FFT_ERR_INVALID_ARG;
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FFT_OK;
+}
+
+int fft_exec_host(const fft_plan *p, const void *host_in, void *host_out, void *dev_in,
+                  void *dev_out, void *stream) {
+  if (!p || !dev_in || !dev_out) return FFT_ERR_INVALID_ARG;
+  if (misaligned(dev_in) || misaligned(dev_out)) return FFT_ERR_MISALIGNED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t elem = p->dtype == FFT_C2C_F32 ? 8 : 16;
+  const size_t count = (size_t)p->batch * (size_t)p->n * (p->dims == 2 ? (size_t)p->n : 1);
+  const size_t bytes = count * elem;
+  cudaError_t e;
+  if (host_in) {
+    e = cudaMemcpyAsync(dev_in, host_in, bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  int rc = fft_exec(p, dev_in, dev_out, stream);
+  if (rc != FFT_OK) return rc;
+  if (host_out) {
+    e = cudaMemcpyAsync(host_out, dev_out, bytes, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return FFT_OK;
+}
+
+int polymul_batched(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, int64_t *c,
+                    int64_t batch, void *stream) {
+  if (!a || !b || !c || na <= 0 || nb <= 0 || batch <= 0) return FFT_ERR_INVALID_ARG;
+  if (((uintptr_t)a & 7u) || ((uintptr_t)b & 7u) || ((uintptr_t)c & 7u))
+    return FFT_ERR_MISALIGNED;
+  const int64_t nc = na + nb - 1;
+  const int log_len = nc > 1 ? ilog2_exact(nc) : 1;  // at least a 2-point transform
+  if (log_len > 27 || batch > ((int64_t)1 << 36) / ((int64_t)1 << log_len))
+    return FFT_ERR_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)3 * (size_t)batch * ((size_t)1 << log_len) * 16;
+  void *scratch = nullptr;
+  cudaError_t e = cudaMallocAsync(&scratch, bytes, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = launch_polymul(reinterpret_cast<const long long *>(a), na,
+                     reinterpret_cast<const long long *>(b), nb, reinterpret_cast<long long *>(c),
+                     batch, log_len, scratch, st);
+  cudaError_t f = cudaFreeAsync(scratch, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (f != cudaSuccess) return cuda_fail(f);
+  return FFT_OK;
+}
+
+int polymul(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, int64_t *c,
+            void *stream) {
+  return polymul_batched(a, na, b, nb, c, 1, stream);
+}
+
+int fft_debug_radix2_pass(const void *in, void *out, int64_t n, int64_t half, int dtype,
+                          void *stream) {
+  if (!in || !out || n <= 0 || half <= 0 || n % (2 * half) != 0 ||
+      (dtype != FFT_C2C_F32 && dtype != FFT_C2C_F64))
+    return FFT_ERR_INVALID_ARG;
+  if (misaligned(in) || misaligned(out)) return FFT_ERR_MISALIGNED;
+  cudaError_t e = launch_radix2_pass(dtype, in, out, n, half, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FFT_OK;
+}
+
+int fft_last_status(void) { return g_status; }
+
+const char *fft_status_string(int status) {
+  switch (status) {
+    case FFT_OK: return "ok";
+    case FFT_ERR_INVALID_ARG: return "invalid argument";
+    case FFT_ERR_NOT_POW2: return "length is not a power of two";
+    case FFT_ERR_UNSUPPORTED: return "unsupported size, type or dimensionality";
+    case FFT_ERR_CUDA: return "CUDA error";
+    case FFT_ERR_ALLOC: return "device allocation failed";
+    case FFT_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    default: return "unknown status";
+  }
+}
+
+const char *fft_last_cuda_error(void) { return cudaGetErrorString(g_cuda_error); }
+
+}  // extern "C"

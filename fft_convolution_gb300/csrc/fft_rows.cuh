@@ -1,0 +1,94 @@
+// fft_rows.cuh -- batched contiguous transforms done wholly on chip.
+//
+// One thread block holds F whole transforms of length N = 2^LOGN
+// (N <= 2^14 fp32, 2^13 fp64): each thread loads 16 elements straight from
+// HBM (element t + w*N/16, w < 16: a warp reads 32 consecutive elements per
+// load), runs every Stockham stage in registers with shared-memory exchanges
+// between stages, and writes its 16 results back in the same pattern.  The
+// data touches HBM exactly once in each direction ("Stockham FFT Butterfly
+// Algorithm in Parallel GLSL", section Performance: batches of butterfly
+// steps completed on chip before writing back).
+#pragma once
+
+#include "fft_device.cuh"
+#include "internal.h"
+
+namespace fftgb {
+// Kernels and their launchers have internal linkage: every translation unit
+// that instantiates one owns its own copy, so no kernel is registered twice.
+namespace {
+
+template <typename T, int LOGN> struct RowsConfig {
+  using P = StagePlan<LOGN>;
+  // Transforms per block: enough to give the block 256 threads.
+  static constexpr int F = P::TP >= 256 ? 1 : 256 / P::TP;
+  static constexpr int THREADS = P::TP * F;
+  static constexpr size_t SMEM = (size_t)F * P::SMEM_ELEMS * sizeof(vec2_t<T>);
+};
+
+template <typename T, int LOGN, int DIR>
+__global__ void __launch_bounds__(RowsConfig<T, LOGN>::THREADS)
+    fft_rows_kernel(const vec2_t<T> *in, vec2_t<T> *out, long long batch) {
+  using V = vec2_t<T>;
+  using P = StagePlan<LOGN>;
+  constexpr int F = RowsConfig<T, LOGN>::F;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  V *smem = reinterpret_cast<V *>(smem_raw);
+
+  const int t = threadIdx.x % P::TP;
+  const int f = threadIdx.x / P::TP;
+  const long long tr = (long long)blockIdx.x * F + f;
+  const bool active = tr < batch;
+
+  V x[P::E];
+  if (active) {
+    const V *src = in + tr * P::L;
+#pragma unroll
+    for (int w = 0; w < P::E; ++w) x[w] = src[t + w * P::TP];
+  } else {
+#pragma unroll
+    for (int w = 0; w < P::E; ++w) x[w] = make_c<V>((T)0, (T)0);
+  }
+
+  const SmemView<V> sm{smem + f * P::SMEM_ELEMS, 1};
+  fft_on_chip<LOGN, DIR>(x, t, sm);
+
+  if (active) {
+    V *dst = out + tr * P::L;
+#pragma unroll
+    for (int w = 0; w < P::E; ++w) {
+      V v = x[w];
+      if constexpr (DIR > 0) v = c_scale(v, (T)(1.0 / P::L));  // inverse: 1/N
+      dst[t + w * P::TP] = v;
+    }
+  }
+}
+
+template <typename T, int LOGN, int DIR>
+cudaError_t launch_rows_t(const void *in, void *out, long long batch, cudaStream_t st) {
+  using C = RowsConfig<T, LOGN>;
+  auto kern = fft_rows_kernel<T, LOGN, DIR>;
+  if (C::SMEM > 48 * 1024) {
+    static cudaError_t attr = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    if (attr != cudaSuccess) return attr;
+  }
+  const long long grid = (batch + C::F - 1) / C::F;
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM, st>>>(
+      static_cast<const vec2_t<T> *>(in), static_cast<vec2_t<T> *>(out), batch);
+  return cudaGetLastError();
+}
+
+template <typename T, int DIR, int LOGN = 0>
+cudaError_t dispatch_rows(int logn, const void *in, void *out, long long batch,
+                          cudaStream_t st) {
+  if constexpr (LOGN > RowsMaxLog<T>::value) {
+    return cudaErrorInvalidValue;
+  } else {
+    if (logn == LOGN) return launch_rows_t<T, LOGN, DIR>(in, out, batch, st);
+    return dispatch_rows<T, DIR, LOGN + 1>(logn, in, out, batch, st);
+  }
+}
+
+}  // namespace
+}  // namespace fftgb

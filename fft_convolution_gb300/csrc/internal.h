@@ -1,0 +1,55 @@
+// internal.h -- declarations shared between the library's translation units
+// (kernel launchers and the C ABI in fft_plan.cu).  Not installed.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fftgb {
+
+// Largest transform one thread block holds on chip: 2^14 complex fp32 or
+// 2^13 complex fp64 (139 KB of shared memory with padding).
+template <typename T> struct RowsMaxLog;
+template <> struct RowsMaxLog<float> { static constexpr int value = 14; };
+template <> struct RowsMaxLog<double> { static constexpr int value = 13; };
+
+// Batched contiguous transforms of length 2^logn (fft_rows_*.cu).
+cudaError_t launch_rows_f32(int logn, int dir, const void *in, void *out, long long batch,
+                            cudaStream_t st);
+cudaError_t launch_rows_f64(int logn, int dir, const void *in, void *out, long long batch,
+                            cudaStream_t st);
+
+// One pass of a transform that does not fit on chip, or the column pass of
+// a 2D transform (fft_pass_*.cu).  The data of each of `batch` transforms is
+// 2^log_n elements; the pass does 2^(log_n - log_l) on-chip transforms of
+// length 2^log_l, each over the elements i + u * 2^(log_n - log_l),
+// u < 2^log_l, and is the radix-2^log_l Stockham stage whose previous block
+// length is 2^log_m.  With twiddle != 0 input u of butterfly i is first
+// multiplied by W_{2^(log_l+log_m)}^{(i mod 2^log_m) u}.
+struct PassArgs {
+  int log_n;
+  int log_l;
+  int log_m;
+  int twiddle;
+  long long batch;
+};
+cudaError_t launch_pass_f32(int dir, const PassArgs &a, const void *in, void *out,
+                            cudaStream_t st);
+cudaError_t launch_pass_f64(int dir, const PassArgs &a, const void *in, void *out,
+                            cudaStream_t st);
+// Largest on-chip length a pass kernel is built for.
+constexpr int kPassMaxLogF32 = 14;
+constexpr int kPassMaxLogF64 = 13;
+
+// One radix-2 butterfly pass (debug_pass.cu).
+cudaError_t launch_radix2_pass(int dtype, const void *in, void *out, long long n, long long half,
+                               cudaStream_t st);
+
+// Fused polynomial multiplication (polymul.cu).  Scratch must hold
+// 3 * batch * 2^log_len complex doubles.
+cudaError_t launch_polymul(const long long *a, long long na, const long long *b, long long nb,
+                           long long *c, long long batch, int log_len, void *scratch,
+                           cudaStream_t st);
+
+}  // namespace fftgb

@@ -1,0 +1,169 @@
+/*
+ * fft_gb300.h -- C ABI of the GB300 (sm_103a) power-of-two FFT library.
+ *
+ * Operations (all on one GPU, asynchronous on the caller's CUDA stream):
+ *   - batched 1D complex-to-complex transforms of power-of-two length,
+ *     forward (unscaled) and inverse (scaled by 1/N), fp32 or fp64;
+ *   - the separable 2D transform of N x N images (rows, then columns);
+ *   - integer polynomial multiplication through fp64 transforms.
+ *
+ * Definitions followed:
+ *   forward   X_k = sum_{n<N} x_n e^{-i 2 pi k n / N}
+ *             ("FFT on GPU", elwhyjay.github.io/post/fft, section
+ *             Discrete Fourier Transform)
+ *   inverse   x_n = (1/N) sum_{k<N} X_k e^{+i 2 pi k n / N}
+ *             (same page, polynomial-multiplication section: omega replaced
+ *             by omega^{-1} and the factor 1/N)
+ *   2D        1D transforms along every row, then along every column
+ *             ("Stockham FFT Butterfly Algorithm in Parallel GLSL",
+ *             section Multi-Dimensional Transforms and Separability)
+ *   polymul   c_k = sum_i a_i b_{k-i}, computed as transform, pointwise
+ *             product of the point values, inverse transform ("FFT on GPU",
+ *             polynomial-multiplication section, whole pipeline)
+ *
+ * Data layout: complex arrays are interleaved (re, im) pairs of float
+ * (FFT_C2C_F32) or double (FFT_C2C_F64) -- the layout of the pages' CUDA
+ * code, and of torch.complex64 / torch.complex128.  A batch is contiguous:
+ * transform b starts at element b*N (1D) or b*N*N (2D, row-major rows of N).
+ *
+ * Ownership: the caller owns every buffer passed in.  A plan owns only its
+ * own workspace (allocated in fft_plan_create, freed in fft_plan_destroy).
+ * polymul allocates its fp64 scratch stream-ordered on the given stream and
+ * frees it the same way before returning.
+ *
+ * Errors: every call returns FFT_OK (0) or one FFT_ERR_* code; calls that
+ * return a pointer return NULL and record the code for fft_last_status()
+ * (per host thread).  Arguments are validated before anything is enqueued;
+ * FFT_ERR_CUDA means a CUDA runtime call or kernel launch failed, and
+ * fft_last_cuda_error() names it.  No call synchronises the device.
+ */
+#ifndef FFT_GB300_H
+#define FFT_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define FFT_OK 0
+#define FFT_ERR_INVALID_ARG 1 /* null pointer, size <= 0, bad enum value       */
+#define FFT_ERR_NOT_POW2 2    /* transform length is not a power of two         */
+#define FFT_ERR_UNSUPPORTED 3 /* valid but not implemented (size / dtype / dims) */
+#define FFT_ERR_CUDA 4        /* CUDA runtime error or launch failure           */
+#define FFT_ERR_ALLOC 5       /* device allocation failed                       */
+#define FFT_ERR_MISALIGNED 6  /* a data pointer is not 16-byte aligned          */
+
+/* Direction: the sign of the exponent. */
+#define FFT_FORWARD (-1) /* e^{-i...}, unscaled          */
+#define FFT_INVERSE (+1) /* e^{+i...}, scaled by 1/N     */
+
+/* Element type. */
+#define FFT_C2C_F32 0 /* interleaved float  (re, im), 8 bytes  */
+#define FFT_C2C_F64 1 /* interleaved double (re, im), 16 bytes */
+
+typedef struct fft_plan fft_plan;
+
+/*
+ * fft_plan_create -- plan `batch` transforms of length n (dims = 1) or of
+ * n x n images (dims = 2) in the given direction and element type.
+ *   n         power of two, 1 <= n.  dims = 1: n <= 2^30 (fp32) / 2^29 (fp64)
+ *             and batch * n * element size must fit the device.  dims = 2:
+ *             n <= 2^14 (fp32) / 2^13 (fp64).
+ *   batch     number of independent transforms, >= 1.
+ *   dims      1 or 2.
+ *   direction FFT_FORWARD or FFT_INVERSE.
+ *   dtype     FFT_C2C_F32 or FFT_C2C_F64.
+ * Lengths up to 2^14 (fp32) / 2^13 (fp64) run as one kernel in which one
+ * thread block holds a whole transform on chip (one HBM read, one HBM write).
+ * Longer 1D transforms run as 2-4 passes over HBM (a Stockham decomposition
+ * into factors of at most 2^9) and need a workspace of batch * n elements,
+ * allocated here on the current device.  Returns NULL on error
+ * (fft_last_status(): INVALID_ARG, NOT_POW2, UNSUPPORTED, ALLOC).
+ */
+fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int dtype);
+
+/* Frees the plan and its workspace.  NULL is ignored.  The caller must make
+ * sure no fft_exec of this plan is still running on the GPU. */
+void fft_plan_destroy(fft_plan *plan);
+
+/* Bytes of device workspace the plan owns (0 for single-kernel plans). */
+size_t fft_plan_workspace_bytes(const fft_plan *plan);
+
+/* Number of kernels one fft_exec of this plan launches. */
+int fft_plan_num_kernels(const fft_plan *plan);
+
+/*
+ * fft_exec -- run the planned transforms.
+ *   in, out   device pointers to batch-contiguous interleaved complex data
+ *             of the plan's type, 16-byte aligned (else FFT_ERR_MISALIGNED).
+ *             in == out (in place) is allowed; other overlaps are not.
+ *             `in` is only read unless in == out.
+ *   stream    a cudaStream_t (NULL = the legacy default stream).
+ * Enqueues the kernels and returns; no synchronisation.
+ */
+int fft_exec(const fft_plan *plan, const void *in, void *out, void *stream);
+
+/*
+ * fft_exec_host -- fft_exec with host-side staging, all on `stream`:
+ * if host_in is not NULL, copy host_in -> dev_in (cudaMemcpyAsync); run the
+ * transform dev_in -> dev_out; if host_out is not NULL, copy
+ * dev_out -> host_out.  Host buffers should be pinned for the copies to be
+ * asynchronous.  dev_in / dev_out are caller-owned device buffers of the
+ * plan's full size (they may be equal).  Allocates nothing.
+ */
+int fft_exec_host(const fft_plan *plan, const void *host_in, void *host_out, void *dev_in,
+                  void *dev_out, void *stream);
+
+/*
+ * polymul -- c = a * b for integer coefficient vectors (device pointers,
+ * int64, 8-byte aligned): a has na >= 1 coefficients, b has nb >= 1,
+ * c receives na + nb - 1.  The product is formed with fp64 transforms of
+ * length L = the smallest power of two >= na + nb - 1 (zero padding), the
+ * pointwise product of the two spectra, the inverse transform, and rounding
+ * to the nearest integer.  The result is exact while every |c_k| and the
+ * transform's rounding error stay well below 2^52 and 0.5 respectively
+ * (e.g. coefficients in [0, 9] with na, nb <= 2^20 give |c_k| < 2^27 and an
+ * error of order 1e-7).  L <= 2^27.  Scratch (3 * L * 16 bytes) is
+ * allocated with cudaMallocAsync on `stream` and freed the same way.
+ */
+int polymul(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, int64_t *c,
+            void *stream);
+
+/* polymul over `batch` independent pairs: pair p uses a + p*na, b + p*nb
+ * and writes c + p*(na+nb-1).  Scratch is 3 * batch * L * 16 bytes. */
+int polymul_batched(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, int64_t *c,
+                    int64_t batch, void *stream);
+
+/*
+ * fft_debug_radix2_pass -- test hook (not part of the transform API): one
+ * gather-shaped radix-2 butterfly pass, "The Butterfly: One Thread, One
+ * Output" (gpu.rocks FFT butterfly, task 2).  Output cell i takes
+ * j = floor(i/half) mod 2, base = i - j*half, r = i mod half,
+ * a = in[base], b = in[base+half], w = e^{-i pi r / half} and writes
+ * a + w b (j = 0) or a - w b (j = 1).
+ *   in, out  device pointers, n interleaved complex values of `dtype`;
+ *            must not overlap.
+ *   n        > 0, a multiple of 2*half;  half >= 1.
+ */
+int fft_debug_radix2_pass(const void *in, void *out, int64_t n, int64_t half, int dtype,
+                          void *stream);
+
+/* Last status recorded on this host thread by a call that returns a
+ * pointer (fft_plan_create). */
+int fft_last_status(void);
+
+/* Static description of a status code. */
+const char *fft_status_string(int status);
+
+/* Name of the last CUDA error seen by this library on this host thread
+ * ("no error" if none). */
+const char *fft_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FFT_GB300_H */

@@ -16,3 +16,21 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+def build_library():
+    """Build libfftgb300.so in-tree if stale (loaded by path: importing the
+    package needs the built library)."""
+    import importlib.util
+    path = os.path.join(ROOT, "fft_convolution_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("fft_convolution_gb300_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()
+
+
+@pytest.fixture(scope="session")
+def fg_lib():
+    build_library()
+    import fft_convolution_gb300
+    return fft_convolution_gb300

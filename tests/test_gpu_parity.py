@@ -1,0 +1,228 @@
+"""GPU parity: every transform the library runs, through the C ABI, against
+the fp64 CPU oracle on the same seeded inputs.
+
+Tolerances (relative L2 error per transform, maximum over the batch):
+fp32 <= 1e-5 * log2(N), fp64 <= 1e-13 * log2(N), with N the number of
+points of one transform (N*N for 2D).  Integer polynomial products are
+compared bit for bit.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+F32, F64 = 0, 1
+TOL = {F32: 1e-5, F64: 1e-13}
+NP = {F32: np.complex64, F64: np.complex128}
+
+
+@pytest.fixture(scope="module")
+def fg(fg_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return fg_lib
+
+
+def stream():
+    return int(torch.cuda.current_stream().cuda_stream)
+
+
+def rel_rows(y, ref):
+    y = np.asarray(y, np.complex128).reshape(ref.shape[0], -1)
+    ref = np.asarray(ref, np.complex128).reshape(ref.shape[0], -1)
+    num = np.linalg.norm(y - ref, axis=1)
+    den = np.linalg.norm(ref, axis=1)
+    den[den == 0] = 1
+    return num / den
+
+
+def tol(dtype, npoints):
+    return TOL[dtype] * max(1, int(np.log2(npoints)))
+
+
+def run_plan(fg, x, n, batch, dims, direction, dtype, inplace=False):
+    p = fg.Plan(n, batch, dims, direction, dtype)
+    d = torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    out = d if inplace else torch.empty_like(d)
+    p.exec(d, out)
+    torch.cuda.synchronize()
+    y = out.cpu().numpy()
+    p.close()
+    return y
+
+
+# --- batched 1D, on chip -------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [F32, F64])
+@pytest.mark.parametrize("logn", list(range(0, 15)))
+def test_rows_forward_inverse(fg, dtype, logn):
+    if dtype == F64 and logn > 13:
+        pytest.skip("fp64 on-chip limit is 2^13")
+    n = 1 << logn
+    batch = 5 if n >= 256 else 37   # ragged against the per-block transform count
+    x = workloads.normal_complex((batch, n), 1000 + logn, NP[dtype])
+    x64 = x.astype(np.complex128)
+    y = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, dtype)
+    ref = oracle.fft(x64)
+    assert rel_rows(y, ref).max() <= tol(dtype, n)
+    if n <= 1024:
+        assert rel_rows(y[:2], np.stack([oracle.dft(r) for r in x64[:2]])).max() <= tol(dtype, n)
+    z = run_plan(fg, y, n, batch, 1, fg.FFT_INVERSE, dtype)
+    refi = oracle.ifft(y.astype(np.complex128))
+    assert rel_rows(z, refi).max() <= tol(dtype, n)
+
+
+@pytest.mark.parametrize("dtype", [F32, F64])
+def test_rows_in_place(fg, dtype):
+    n, batch = 4096, 9
+    x = workloads.uniform_complex((batch, n), 7, NP[dtype])
+    y = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, dtype, inplace=True)
+    assert rel_rows(y, oracle.fft(x.astype(np.complex128))).max() <= tol(dtype, n)
+
+
+def test_rows_closed_forms(fg):
+    n = 2048
+    x = np.zeros((3, n), np.complex64)
+    x[0, 0] = 1                                    # delta -> all ones
+    x[1, :] = 0.5 - 0.25j                          # constant -> N c at bin 0
+    f = 77                                         # single integer tone -> N at bin f
+    x[2] = np.exp(2j * np.pi * ((f * np.arange(n)) % n) / n)
+    y = run_plan(fg, x, n, 3, 1, fg.FFT_FORWARD, F32)
+    assert np.max(np.abs(y[0] - 1)) < 1e-6
+    assert abs(y[1, 0] - n * (0.5 - 0.25j)) < 1e-3 and np.max(np.abs(y[1, 1:])) < 1e-3
+    e = np.zeros(n)
+    e[f] = n
+    assert np.max(np.abs(y[2] - e)) < 5e-3
+
+
+# --- long 1D: multi-pass -------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,logn", [(F32, 15), (F32, 16), (F32, 18), (F32, 19), (F32, 20),
+                                        (F64, 14), (F64, 15), (F64, 17), (F64, 19)])
+def test_multipass_forward_inverse(fg, dtype, logn):
+    n = 1 << logn
+    batch = 2
+    x = workloads.normal_complex((batch, n), 2000 + logn, NP[dtype])
+    y = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, dtype)
+    assert rel_rows(y, oracle.fft(x.astype(np.complex128))).max() <= tol(dtype, n)
+    z = run_plan(fg, y, n, batch, 1, fg.FFT_INVERSE, dtype, inplace=True)
+    assert rel_rows(z, oracle.ifft(y.astype(np.complex128))).max() <= tol(dtype, n)
+
+
+@pytest.mark.parametrize("passlog", [5, 7, 9, 13])
+def test_multipass_factorisations(fg, monkeypatch, passlog):
+    # The same 2^18 transform split into 2, 3 or 4 passes.
+    monkeypatch.setenv("FFT_GB300_PASS_LOG", str(passlog))
+    n = 1 << 18
+    x = workloads.uniform_complex((1, n), 31, np.complex64)
+    y = run_plan(fg, x, n, 1, 1, fg.FFT_FORWARD, F32)
+    assert rel_rows(y, oracle.fft(x.astype(np.complex128))).max() <= tol(F32, n)
+
+
+# --- 2D -----------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [F32, F64])
+@pytest.mark.parametrize("logn", [0, 1, 2, 4, 5, 7, 8, 9])
+def test_2d_forward_inverse(fg, dtype, logn):
+    n = 1 << logn
+    batch = 3
+    x = workloads.normal_complex((batch, n, n), 3000 + logn, NP[dtype])
+    y = run_plan(fg, x, n, batch, 2, fg.FFT_FORWARD, dtype)
+    ref = oracle.fft2d(x.astype(np.complex128))
+    assert rel_rows(y, ref).max() <= tol(dtype, n * n)
+    z = run_plan(fg, y, n, batch, 2, fg.FFT_INVERSE, dtype)
+    assert rel_rows(z, oracle.fft2d(y.astype(np.complex128), +1)).max() <= tol(dtype, n * n)
+
+
+@pytest.mark.parametrize("dtype,logn", [(F32, 11), (F32, 13), (F64, 12)])
+def test_2d_large_sides(fg, dtype, logn):
+    n = 1 << logn
+    x = workloads.uniform_complex((1, n, n), 3100 + logn, NP[dtype])
+    y = run_plan(fg, x, n, 1, 2, fg.FFT_FORWARD, dtype)
+    # separable check against numpy's 2D FFT computed in fp64 (independent)
+    ref = np.fft.fft2(x.astype(np.complex128))
+    assert rel_rows(y, ref).max() <= tol(dtype, n * n)
+    if logn <= 11:
+        assert rel_rows(y, oracle.fft2d(x.astype(np.complex128))).max() <= tol(dtype, n * n)
+
+
+# --- polynomial multiplication ----------------------------------------------
+
+@pytest.mark.parametrize("na,nb,batch", [(1, 1, 1), (1, 5, 2), (5, 7, 3), (16, 16, 4),
+                                         (100, 1000, 2), (1000, 3000, 2), (4096, 4096, 3),
+                                         (4097, 10, 1), (1 << 15, 1 << 15, 2)])
+def test_polymul_exact(fg, na, nb, batch):
+    g = workloads.generator(na * 7 + nb)
+    a = g.integers(0, 10, size=(batch, na), dtype=np.int64)
+    b = g.integers(0, 10, size=(batch, nb), dtype=np.int64)
+    c = fg.polymul_tensors(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda())
+    torch.cuda.synchronize()
+    c = c.cpu().numpy()
+    for p in range(batch):
+        if na * nb <= 1 << 24:
+            assert np.array_equal(c[p], oracle.polymul_schoolbook(a[p], b[p]))
+        else:
+            idx = workloads.sample_indices(512, na + nb - 1, p)
+            assert np.array_equal(c[p][idx], oracle.polymul_schoolbook_at(a[p], b[p], idx))
+            assert np.array_equal(c[p], oracle.polymul_fft(a[p], b[p]))
+
+
+def test_polymul_signed_coefficients(fg):
+    g = workloads.generator(5)
+    a = g.integers(-1000, 1001, size=3000, dtype=np.int64)
+    b = g.integers(-1000, 1001, size=2000, dtype=np.int64)
+    c = fg.polymul_tensors(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(c.cpu().numpy(), oracle.polymul_schoolbook(a, b))
+
+
+# --- the single butterfly pass ------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [F32, F64])
+def test_radix2_pass_8_points(fg, dtype):
+    s = workloads.p1_spectrum().astype(NP[dtype])
+    d = torch.from_numpy(s).cuda()
+    y = d
+    for half in (1, 2, 4):
+        out = torch.empty_like(d)
+        assert fg.fft_debug_radix2_pass(d.data_ptr(), out.data_ptr(), 8, half, dtype,
+                                        stream()) == 0
+        torch.cuda.synchronize()
+        ref = oracle.radix2_pass(s.astype(np.complex128), half)
+        assert np.max(np.abs(out.cpu().numpy() - ref)) < (1e-6 if dtype == F32 else 1e-15)
+    # bit-reversed input through half = 1, 2, 4 is the 8-point DFT
+    y = torch.from_numpy(oracle.bit_reverse(s.astype(np.complex128)).astype(NP[dtype])).cuda()
+    for half in (1, 2, 4):
+        out = torch.empty_like(y)
+        assert fg.fft_debug_radix2_pass(y.data_ptr(), out.data_ptr(), 8, half, dtype,
+                                        stream()) == 0
+        y = out
+    torch.cuda.synchronize()
+    assert rel_rows(y.cpu().numpy()[None], oracle.dft(s.astype(np.complex128))[None]).max() \
+        <= tol(dtype, 8)
+
+
+def test_radix2_pass_large(fg):
+    n = 1 << 16
+    x = workloads.normal_complex(n, 9, np.complex64)
+    d = torch.from_numpy(x).cuda()
+    for half in (1, 8, 1 << 15):
+        out = torch.empty_like(d)
+        assert fg.fft_debug_radix2_pass(d.data_ptr(), out.data_ptr(), n, half, F32, stream()) == 0
+        torch.cuda.synchronize()
+        ref = oracle.radix2_pass(x.astype(np.complex128), half)
+        assert rel_rows(out.cpu().numpy()[None], ref[None]).max() < 1e-6
+
+
+# --- error reporting on a GPU ------------------------------------------------
+
+def test_misaligned_device_pointer(fg):
+    p = fg.Plan(64, 1, 1, fg.FFT_FORWARD, F32)
+    buf = torch.zeros(2 * 64 + 8, dtype=torch.complex64, device="cuda")
+    assert fg.fft_exec(p.handle, buf.data_ptr() + 8, buf.data_ptr() + 1024, stream()) == \
+        fg.FFT_ERR_MISALIGNED
+    p.close()
