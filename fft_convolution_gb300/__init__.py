@@ -6,8 +6,8 @@ of every transform runs in the library's CUDA kernels.  PyTorch is used only
 for device memory and streams (the tensor helpers at the end).
 
 Importing this package loads the in-tree shared library and raises
-``ImportError`` if it has not been built (``python -m
-fft_convolution_gb300.build``); there is no fallback implementation.
+``ImportError`` if it has not been built (``python
+fft_convolution_gb300/build.py``); there is no fallback implementation.
 """
 from __future__ import annotations
 
@@ -42,6 +42,7 @@ SIGNATURES = {
     "fft_exec_host": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP]),
     "polymul": (_INT, [_VP, _I64, _VP, _I64, _VP, _VP]),
     "polymul_batched": (_INT, [_VP, _I64, _VP, _I64, _VP, _I64, _VP]),
+    "polymul_noalloc": (_INT, [_VP, _I64, _VP, _I64, _VP, _VP]),
     "fft_debug_radix2_pass": (_INT, [_VP, _VP, _I64, _I64, _INT, _VP]),
     "fft_last_status": (_INT, []),
     "fft_status_string": (ctypes.c_char_p, [_INT]),
@@ -53,7 +54,7 @@ def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
             f"{LIB_PATH} is missing: build the CUDA library first "
-            "(python -m fft_convolution_gb300.build); there is no CPU fallback")
+            "(python fft_convolution_gb300/build.py); there is no CPU fallback")
     lib = ctypes.CDLL(LIB_PATH)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)
@@ -117,6 +118,15 @@ def polymul(a_ptr: int, na: int, b_ptr: int, nb: int, c_ptr: int, stream: int) -
 def polymul_batched(a_ptr: int, na: int, b_ptr: int, nb: int, c_ptr: int, batch: int,
                     stream: int) -> int:
     return _lib.polymul_batched(a_ptr, na, b_ptr, nb, c_ptr, batch, stream)
+
+
+def polymul_noalloc(a_ptr: int, na: int, b_ptr: int, nb: int, c_ptr: int, stream: int) -> int:
+    """polymul without device allocation (fixed scratch; na+nb-1 <=
+    POLYMUL_NOALLOC_MAX_LEN).  For callers that may not allocate."""
+    return _lib.polymul_noalloc(a_ptr, na, b_ptr, nb, c_ptr, stream)
+
+
+POLYMUL_NOALLOC_MAX_LEN = 65536
 
 
 def fft_debug_radix2_pass(in_ptr: int, out_ptr: int, n: int, half: int, dtype: int,

@@ -1,8 +1,8 @@
 """Build the CUDA library in-tree: every ``csrc/*.cu`` is compiled for
 sm_103a in parallel, then linked into ``libfftgb300.so`` next to this file.
 
-    python -m fft_convolution_gb300.build          # build if stale
-    python -m fft_convolution_gb300.build --force  # rebuild everything
+    python fft_convolution_gb300/build.py          # build if stale
+    python fft_convolution_gb300/build.py --force  # rebuild everything
 """
 from __future__ import annotations
 

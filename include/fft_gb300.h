@@ -138,6 +138,28 @@ int polymul_batched(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, 
                     int64_t batch, void *stream);
 
 /*
+ * polymul_noalloc -- the same product as polymul for one pair, for callers
+ * that must not allocate device memory where they need it (a plug-in whose
+ * host application owns the device-memory budget, or a latency-critical
+ * loop where an allocation could wait on the device or fail).  The source
+ * pages have no counterpart: this is a property of this library's memory
+ * handling, not of the method.
+ *   a, b, c  as for polymul (device pointers, int64, 8-byte aligned).
+ *   na + nb - 1 must be at most FFT_POLYMUL_NOALLOC_MAX_LEN; longer products
+ *            return FFT_ERR_UNSUPPORTED (use polymul for them).
+ * Scratch: a fixed 3 MiB array in the library's device image (every GPU that
+ * loads the library holds it until the process exits).  No call allocates
+ * or frees memory.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current -- make that
+ * first call outside any stream capture.  All calls on a device share the
+ * array: calls that overlap on the GPU race and give wrong results, so order
+ * them on one stream.  Nothing in the array needs clearing between calls.
+ */
+#define FFT_POLYMUL_NOALLOC_MAX_LEN 65536
+int polymul_noalloc(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, int64_t *c,
+                    void *stream);
+
+/*
  * fft_debug_radix2_pass -- test hook (not part of the transform API): one
  * gather-shaped radix-2 butterfly pass, "The Butterfly: One Thread, One
  * Output" (gpu.rocks FFT butterfly, task 2).  Output cell i takes
