@@ -48,8 +48,18 @@ def log2i(n: int) -> int:
 # Workload descriptions (bytes / flops / units per step)
 # ---------------------------------------------------------------------------
 
+SIZE_OVERRIDE = {}
+
+
+def config_of(name: str) -> dict:
+    """The workload's sizes, with any --n / --batch override applied."""
+    c = dict(workloads.CONFIGS[name])
+    c.update(SIZE_OVERRIDE)
+    return c
+
+
 def workload_info(name: str, pass_log: int = 9):
-    c = workloads.CONFIGS[name]
+    c = config_of(name)
     n, batch = c["n"], c["batch"]
     if c["kind"] == "fft1d":
         elem = 8
@@ -191,7 +201,7 @@ def cpu_oracle_sample(name: str, budget_s: float = 12.0):
     the metric's unit.  Single-threaded."""
     import oracle
     info = workload_info(name)
-    c = workloads.CONFIGS[name]
+    c = config_of(name)
     t0 = time.perf_counter()
     done_units = 0.0  # fraction of one step's work
     sample = ""
@@ -269,14 +279,14 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
     name = args.config
-    c = workloads.CONFIGS[name]
+    c = config_of(name)
     info = workload_info(name)
     stream = torch.cuda.Stream(device=dev)
     sh = int(stream.cuda_stream)
 
     # Inputs: seeded on the host, resident in HBM before timing.
     if info["kind"] == "polymul":
-        a_h, b_h = workloads.config_input(name)
+        a_h, b_h = workloads.poly_coeffs((c["batch"], c["n"]), c["seed"])
         a_d, b_d = torch.from_numpy(a_h).to(dev), torch.from_numpy(b_h).to(dev)
         c_d = torch.empty(c["batch"], 2 * c["n"] - 1, dtype=torch.int64, device=dev)
         plans = []
@@ -292,7 +302,7 @@ def run_gpu(args):
             assert rc == 0, fg.fft_status_string(rc)
         kernels_per_step = 3 * max(1, math.ceil(log2i(info["L"]) / 9))
     else:
-        x_h = workloads.config_input(name)
+        x_h = sized_input(name, c)
         x_d = torch.from_numpy(x_h).to(dev)
         y_d = torch.empty_like(x_d)
         z_d = torch.empty_like(x_d)
@@ -465,7 +475,20 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def sized_input(name: str, c: dict):
+    if not SIZE_OVERRIDE:
+        return workloads.config_input(name)
+    if c["kind"] == "fft2d":
+        return workloads.normal_complex((c["batch"], c["n"], c["n"]), c["seed"])
+    if name == "c3":
+        return workloads.tones_plus_noise(c["n"], c["seed"]).reshape(1, -1)
+    return workloads.normal_complex((c["batch"], c["n"]), c["seed"])
+
+
 def workload_label(name: str) -> str:
+    if SIZE_OVERRIDE:
+        c = config_of(name)
+        return f"{name} reduced for profiling: n={c['n']}, batch={c['batch']}"
     c = workloads.CONFIGS[name]
     if name == "c1":
         return "1D C2C forward, N=1024, batch 1, fp32"
@@ -535,7 +558,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    ap.add_argument("--n", type=int, default=None,
+                    help="override the transform length (small profiling cases)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the batch (small profiling cases)")
     args = ap.parse_args()
+    if args.n is not None:
+        SIZE_OVERRIDE["n"] = args.n
+    if args.batch is not None:
+        SIZE_OVERRIDE["batch"] = args.batch
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":

@@ -39,6 +39,9 @@ template <typename T, int LOGL> struct PassConfig {
       TILE_BYTES_TARGET / ((long long)P::L * (long long)sizeof(vec2_t<T>));
   static constexpr int C = C_RAW < 1 ? 1 : (C_RAW > 64 ? 64 : (int)C_RAW);
   static constexpr int THREADS = C * P::TP;
+  // Ask for registers that let 1024 threads (two 512-thread tiles) share an
+  // SM, so one tile's loads overlap another's compute and stores.
+  static constexpr int MIN_BLOCKS = THREADS >= 1024 ? 1 : 1024 / THREADS;
   static constexpr int ROW_ELEMS =
       P::SMEM_ELEMS > P::L + 1 ? P::SMEM_ELEMS : P::L + 1;  // exchange or transpose
   static constexpr size_t SMEM = (size_t)C * ROW_ELEMS * sizeof(vec2_t<T>);
@@ -68,7 +71,7 @@ struct PassGeom {
 };
 
 template <typename T, int LOGL, int DIR, class Load, class Store>
-__global__ void __launch_bounds__(PassConfig<T, LOGL>::THREADS)
+__global__ void __launch_bounds__(PassConfig<T, LOGL>::THREADS, PassConfig<T, LOGL>::MIN_BLOCKS)
     fft_pass_kernel(Load load, Store store, PassGeom g) {
   using V = vec2_t<T>;
   using P = StagePlan<LOGL>;
