@@ -63,11 +63,17 @@ template <typename V> struct StoreComplex {
   }
 };
 
+// Which tiles a launch covers.  Block r of a transform takes tile
+// tile_lo + (r mod tile_run) + (r / tile_run) * tile_jump; a launch over all
+// tiles has tile_lo = 0, tile_run = grid_per_batch, tile_jump = 0.
 struct PassGeom {
   int log_n;
   int log_m;
   int twiddle;
-  long long tiles;  // tiles per transform
+  long long grid_per_batch;  // blocks per transform in this launch
+  long long tile_lo;
+  long long tile_run;
+  long long tile_jump;
 };
 
 template <typename T, int LOGL, int DIR, class Load, class Store>
@@ -82,8 +88,9 @@ __global__ void __launch_bounds__(PassConfig<T, LOGL>::THREADS, PassConfig<T, LO
 
   const int c = threadIdx.x % C;   // column within the tile
   const int t = threadIdx.x / C;   // thread within the column
-  const long long tile = blockIdx.x % g.tiles;
-  const long long b = blockIdx.x / g.tiles;
+  const long long r = blockIdx.x % g.grid_per_batch;
+  const long long b = blockIdx.x / g.grid_per_batch;
+  const long long tile = g.tile_lo + r % g.tile_run + (r / g.tile_run) * g.tile_jump;
   const long long cols = 1LL << (g.log_n - LOGL);  // N / L butterflies
   const long long i = tile * C + c;
   const bool active = i < cols;
@@ -141,9 +148,16 @@ __global__ void __launch_bounds__(PassConfig<T, LOGL>::THREADS, PassConfig<T, LO
   }
 }
 
+// Tiles (of C consecutive butterflies) a pass with on-chip length 2^log_l
+// has per transform.
+template <typename T, int LOGL> long long pass_tiles(int log_n) {
+  const long long cols = 1LL << (log_n - LOGL);
+  return (cols + PassConfig<T, LOGL>::C - 1) / PassConfig<T, LOGL>::C;
+}
+
 template <typename T, int LOGL, int DIR, class Load, class Store>
 cudaError_t launch_pass_t(Load load, Store store, int log_n, int log_m, int twiddle,
-                          long long batch, cudaStream_t st) {
+                          long long batch, cudaStream_t st, const TileSet *subset = nullptr) {
   using C = PassConfig<T, LOGL>;
   auto kern = fft_pass_kernel<T, LOGL, DIR, Load, Store>;
   if (C::SMEM > 48 * 1024) {
@@ -151,10 +165,16 @@ cudaError_t launch_pass_t(Load load, Store store, int log_n, int log_m, int twid
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (attr != cudaSuccess) return attr;
   }
-  const long long cols = 1LL << (log_n - LOGL);
-  PassGeom g{log_n, log_m, twiddle, (cols + C::C - 1) / C::C};
-  const long long grid = g.tiles * batch;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const long long tiles = pass_tiles<T, LOGL>(log_n);
+  PassGeom g{log_n, log_m, twiddle, tiles, 0, tiles, 0};
+  if (subset) {
+    g.grid_per_batch = subset->runs * subset->run;
+    g.tile_lo = subset->lo;
+    g.tile_run = subset->run;
+    g.tile_jump = subset->jump;
+  }
+  const long long grid = g.grid_per_batch * batch;
+  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<(unsigned)grid, C::THREADS, C::SMEM, st>>>(load, store, g);
   return cudaGetLastError();
 }
@@ -169,7 +189,8 @@ cudaError_t dispatch_pass(const PassArgs &a, const void *in, void *out, cudaStre
       const long long n = 1LL << a.log_n;
       return launch_pass_t<T, LOGL, DIR>(LoadComplex<V>{static_cast<const V *>(in), n},
                                          StoreComplex<V>{static_cast<V *>(out), n}, a.log_n,
-                                         a.log_m, a.twiddle, a.batch, st);
+                                         a.log_m, a.twiddle, a.batch, st,
+                                         a.subset.runs > 0 ? &a.subset : nullptr);
     }
     return dispatch_pass<T, DIR, MAXLOG, LOGL + 1>(a, in, out, st);
   }

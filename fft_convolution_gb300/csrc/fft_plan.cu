@@ -58,6 +58,22 @@ int pass_log_limit(int dtype) {
   return lim > hard ? hard : lim;
 }
 
+// Bytes of data an L2-grouped schedule keeps in flight between two
+// dependent kernels so that the second finds the first's output in L2.
+// Measured on GB300, grouping 2D images (32 MiB) or fusing the first two
+// passes of a 2^26 transform by 32 MiB groups is slower than whole-array
+// passes (more, smaller launches with partial last waves), so grouping is
+// off by default (0) and FFT_GB300_L2_BYTES turns it on for tuning.
+size_t l2_group_bytes() {
+  size_t v = 0;
+  const char *env = getenv("FFT_GB300_L2_BYTES");
+  if (env && *env) {
+    long long x = atoll(env);
+    if (x > 0) v = (size_t)x;
+  }
+  return v;
+}
+
 cudaError_t launch_rows(int dtype, int logn, int dir, const void *in, void *out, long long batch,
                         cudaStream_t st) {
   return dtype == FFT_C2C_F32 ? launch_rows_f32(logn, dir, in, out, batch, st)
@@ -168,49 +184,167 @@ void fft_plan_destroy(fft_plan *plan) {
 
 size_t fft_plan_workspace_bytes(const fft_plan *plan) { return plan ? plan->workspace_bytes : 0; }
 
+}  // extern "C"
+
+namespace {
+
+// Enqueues (or, with dry = true, only counts) the kernels of one fft_exec.
+struct Schedule {
+  const fft_plan *p;
+  cudaStream_t st;
+  bool dry;
+  int count = 0;
+
+  size_t elem() const { return p->dtype == FFT_C2C_F32 ? 8 : 16; }
+
+  cudaError_t rows(const void *in, void *out, long long batch) {
+    ++count;
+    return dry ? cudaSuccess : launch_rows(p->dtype, p->logn, p->direction, in, out, batch, st);
+  }
+  cudaError_t pass(const PassArgs &a, const void *in, void *out) {
+    ++count;
+    return dry ? cudaSuccess : launch_pass(p->dtype, p->direction, a, in, out, st);
+  }
+  int tile_cols(int log_l) const {
+    return p->dtype == FFT_C2C_F32 ? pass_tile_cols_f32(log_l) : pass_tile_cols_f64(log_l);
+  }
+
+  // 2D: rows (contiguous axis), then the columns in place, one L2-sized
+  // group of images at a time so the column pass reads the row pass's
+  // output from L2.
+  cudaError_t run_2d(const char *in, char *out) {
+    const long long n = p->n;
+    const size_t img = (size_t)n * (size_t)n * elem();
+    const size_t budget = l2_group_bytes();
+    long long g = budget ? (long long)(budget / img) : p->batch;
+    if (g < 1) g = 1;
+    for (long long b0 = 0; b0 < p->batch; b0 += g) {
+      const long long nb = p->batch - b0 < g ? p->batch - b0 : g;
+      const size_t off = (size_t)b0 * img;
+      cudaError_t e = rows(in + off, out + off, nb * n);
+      if (e != cudaSuccess || p->logn == 0) {  // 1 x 1: rows already did it
+        if (e != cudaSuccess) return e;
+        continue;
+      }
+      PassArgs a{2 * p->logn, p->logn, p->logn, 0, nb, {}};
+      e = pass(a, out + off, out + off);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+
+  // Passes k_begin.. of `batch` transforms.  Pass k reads the previous
+  // pass's output; intermediates alternate between the workspace and `out`
+  // and the last pass always writes `out` (it reads and writes the same
+  // positions, so in place is safe).
+  cudaError_t run_passes(const char *in, char *out, char *ws, long long batch, int k_begin) {
+    int log_m = 0;
+    for (int k = 0; k < k_begin; ++k) log_m += p->pass_log[k];
+    const char *src = k_begin == 0 ? in : (k_begin % 2 == 1 ? ws : out);
+    for (int k = k_begin; k < p->npasses; ++k) {
+      char *dst = (k == p->npasses - 1) ? out : (k % 2 == 0 ? ws : out);
+      PassArgs a{p->logn, p->pass_log[k], log_m, 1, batch, {}};
+      cudaError_t e = pass(a, src, dst);
+      if (e != cudaSuccess) return e;
+      src = dst;
+      log_m += p->pass_log[k];
+    }
+    return cudaSuccess;
+  }
+
+  // Passes 0 and 1 of one transform fused through L2.  Pass-1 butterfly
+  // q*L0 + p (q < Q = N/(L0 L1)) reads exactly the outputs of the pass-0
+  // butterflies q + u*Q (u < L1), so for a group of G consecutive q both
+  // passes close over G*L0*L1 elements: run pass 0 for the group (its
+  // output stays in L2), then pass 1 for the group, group after group.
+  // Returns false (nothing launched) when the sizes do not allow it.
+  bool fused_01(const char *in, char *out, char *ws, cudaError_t *err) {
+    const int l0 = p->pass_log[0], l1 = p->pass_log[1];
+    const long long L0 = 1LL << l0, L1 = 1LL << l1;
+    const long long Q = 1LL << (p->logn - l0 - l1);
+    const long long C0 = tile_cols(l0), C1 = tile_cols(l1);
+    long long G = (long long)(l2_group_bytes() / ((size_t)L0 * L1 * elem()));
+    if (G < C0) G = C0;
+    while (G & (G - 1)) G &= G - 1;  // power of two
+    if (C0 <= 0 || C1 <= 0 || Q < C0 || G > Q || Q % G || (G * L0) % C1) return false;
+    for (long long q0 = 0; q0 < Q; q0 += G) {
+      PassArgs a0{p->logn, l0, 0, 1, 1, {q0 / C0, G / C0, Q / C0, L1}};
+      *err = pass(a0, in, ws);
+      if (*err != cudaSuccess) return true;
+      PassArgs a1{p->logn, l1, l0, 1, 1, {q0 * L0 / C1, G * L0 / C1, 0, 1}};
+      *err = pass(a1, ws, out);
+      if (*err != cudaSuccess) return true;
+    }
+    *err = cudaSuccess;
+    return true;
+  }
+
+  cudaError_t run_multi(const char *in, char *out) {
+    char *ws = static_cast<char *>(p->workspace);
+    const size_t tbytes = (size_t)p->n * elem();
+    const size_t budget = l2_group_bytes();
+    if (budget == 0) return run_passes(in, out, ws, p->batch, 0);
+    if (tbytes <= budget) {
+      // Whole transforms fit in L2: all passes of one group, then the next.
+      long long g = (long long)(budget / tbytes);
+      if (g < 1) g = 1;
+      for (long long b0 = 0; b0 < p->batch; b0 += g) {
+        const long long nb = p->batch - b0 < g ? p->batch - b0 : g;
+        const size_t off = (size_t)b0 * tbytes;
+        cudaError_t e = run_passes(in + off, out + off, ws + off, nb, 0);
+        if (e != cudaSuccess) return e;
+      }
+      return cudaSuccess;
+    }
+    // Larger than L2: fuse the first two passes through L2 when the result
+    // may not overwrite the input early (out of place) and there is a pass
+    // left to run after them.
+    if (in != out && p->npasses >= 3) {
+      bool fused = true;
+      for (long long b = 0; b < p->batch && fused; ++b) {
+        const size_t off = (size_t)b * tbytes;
+        cudaError_t e = cudaSuccess;
+        fused = fused_01(in + off, out + off, ws + off, &e);
+        if (e != cudaSuccess) return e;
+      }
+      if (fused) return run_passes(in, out, ws, p->batch, 2);
+    }
+    return run_passes(in, out, ws, p->batch, 0);
+  }
+
+  cudaError_t run(const void *in, void *out) {
+    const char *i = static_cast<const char *>(in);
+    char *o = static_cast<char *>(out);
+    switch (p->kind) {
+      case KIND_ROWS:
+        return rows(in, out, p->batch);
+      case KIND_2D:
+        return run_2d(i, o);
+      case KIND_MULTI:
+        return run_multi(i, o);
+      default:
+        return cudaErrorInvalidValue;
+    }
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
 int fft_plan_num_kernels(const fft_plan *plan) {
   if (!plan) return 0;
-  if (plan->kind == KIND_2D) return plan->logn == 0 ? 1 : 2;
-  return plan->kind == KIND_ROWS ? 1 : plan->npasses;
+  // Count an out-of-place execution (distinct dummy addresses).
+  Schedule s{plan, nullptr, true};
+  s.run(reinterpret_cast<const void *>(16), reinterpret_cast<void *>(32));
+  return s.count;
 }
 
 int fft_exec(const fft_plan *p, const void *in, void *out, void *stream) {
   if (!p || !in || !out) return FFT_ERR_INVALID_ARG;
   if (misaligned(in) || misaligned(out)) return FFT_ERR_MISALIGNED;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int dir = p->direction;
-  cudaError_t e = cudaSuccess;
-  switch (p->kind) {
-    case KIND_ROWS:
-      e = launch_rows(p->dtype, p->logn, dir, in, out, p->batch, st);
-      break;
-    case KIND_2D: {
-      // Rows (contiguous axis), then columns in place.
-      e = launch_rows(p->dtype, p->logn, dir, in, out, p->batch * p->n, st);
-      if (e != cudaSuccess || p->logn == 0) break;  // 1 x 1: rows already did it
-      PassArgs a{2 * p->logn, p->logn, p->logn, 0, p->batch};
-      e = launch_pass(p->dtype, dir, a, out, out, st);
-      break;
-    }
-    case KIND_MULTI: {
-      // Pass k reads the previous pass's output; intermediates alternate
-      // between the workspace and `out`, the last pass always writes `out`
-      // (it reads and writes the same positions, so in place is safe).
-      int log_m = 0;
-      const void *src = in;
-      for (int k = 0; k < p->npasses; ++k) {
-        void *dst = (k == p->npasses - 1) ? out : (k % 2 == 0 ? p->workspace : out);
-        PassArgs a{p->logn, p->pass_log[k], log_m, 1, p->batch};
-        e = launch_pass(p->dtype, dir, a, src, dst, st);
-        if (e != cudaSuccess) break;
-        src = dst;
-        log_m += p->pass_log[k];
-      }
-      break;
-    }
-    default:
-      return FFT_ERR_INVALID_ARG;
-  }
+  Schedule s{p, static_cast<cudaStream_t>(stream), false};
+  cudaError_t e = s.run(in, out);
   if (e != cudaSuccess) return cuda_fail(e);
   return FFT_OK;
 }

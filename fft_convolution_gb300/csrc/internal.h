@@ -20,20 +20,35 @@ cudaError_t launch_rows_f32(int logn, int dir, const void *in, void *out, long l
 cudaError_t launch_rows_f64(int logn, int dir, const void *in, void *out, long long batch,
                             cudaStream_t st);
 
+// A subset of a pass's tiles: `runs` runs of `run` consecutive tiles, run k
+// starting at tile lo + k * jump.  runs = 0 means every tile.
+struct TileSet {
+  long long lo;
+  long long run;
+  long long jump;
+  long long runs;
+};
+
 // One pass of a transform that does not fit on chip, or the column pass of
 // a 2D transform (fft_pass_*.cu).  The data of each of `batch` transforms is
 // 2^log_n elements; the pass does 2^(log_n - log_l) on-chip transforms of
 // length 2^log_l, each over the elements i + u * 2^(log_n - log_l),
 // u < 2^log_l, and is the radix-2^log_l Stockham stage whose previous block
 // length is 2^log_m.  With twiddle != 0 input u of butterfly i is first
-// multiplied by W_{2^(log_l+log_m)}^{(i mod 2^log_m) u}.
+// multiplied by W_{2^(log_l+log_m)}^{(i mod 2^log_m) u}.  `subset` limits
+// the launch to some of the pass's tiles.
 struct PassArgs {
   int log_n;
   int log_l;
   int log_m;
   int twiddle;
   long long batch;
+  TileSet subset;
 };
+// Columns (consecutive butterflies) one block of the pass kernel takes for an
+// on-chip length 2^log_l (fft_pass_*.cu).
+int pass_tile_cols_f32(int log_l);
+int pass_tile_cols_f64(int log_l);
 cudaError_t launch_pass_f32(int dir, const PassArgs &a, const void *in, void *out,
                             cudaStream_t st);
 cudaError_t launch_pass_f64(int dir, const PassArgs &a, const void *in, void *out,

@@ -74,7 +74,7 @@ def test_plan_create_rejects(fg, args, status):
 
 @pytest.mark.parametrize("n,dims,dtype,kernels", [
     (1, 1, 0, 1), (1024, 1, 0, 1), (1 << 14, 1, 0, 1), (1 << 13, 1, 1, 1),
-    (2048, 2, 0, 2), (1 << 13, 2, 1, 2)])
+    (64, 2, 0, 2), (2048, 2, 0, 2), (1 << 13, 2, 1, 2), (1, 2, 0, 1)])
 def test_on_chip_plans_need_no_device(fg, n, dims, dtype, kernels):
     # Single-kernel and 2D plans own no workspace, so they are created
     # without touching the device.
@@ -82,6 +82,15 @@ def test_on_chip_plans_need_no_device(fg, n, dims, dtype, kernels):
     assert h
     assert fg.fft_plan_num_kernels(h) == kernels
     assert fg.fft_plan_workspace_bytes(h) == 0
+    fg.fft_plan_destroy(h)
+
+
+def test_2d_l2_grouping_kernel_count(fg, monkeypatch):
+    # With an L2 budget of one 32 MiB image, 3 images run as 3 groups of
+    # (row kernel, column pass).
+    monkeypatch.setenv("FFT_GB300_L2_BYTES", str(32 << 20))
+    h = fg._lib.fft_plan_create(2048, 3, 2, -1, 0)
+    assert fg.fft_plan_num_kernels(h) == 6
     fg.fft_plan_destroy(h)
 
 

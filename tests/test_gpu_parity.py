@@ -123,6 +123,45 @@ def test_multipass_factorisations(fg, monkeypatch, passlog):
     assert rel_rows(y, oracle.fft(x.astype(np.complex128))).max() <= tol(F32, n)
 
 
+@pytest.mark.parametrize("dtype,logn,budget", [
+    (F32, 22, 1 << 20),   # passes 8,7,7: four L2 groups of the fused first two passes
+    (F32, 20, 1 << 19),   # passes 7,7,6: one group
+    (F64, 20, 1 << 20),   # passes 7,7,6 fp64: two groups
+])
+def test_multipass_fused_l2_groups(fg, monkeypatch, dtype, logn, budget):
+    # A transform larger than the L2 budget runs its first two passes group
+    # by group through L2 (out of place), or all passes in turn (in place).
+    monkeypatch.setenv("FFT_GB300_L2_BYTES", str(budget))
+    n = 1 << logn
+    x = workloads.normal_complex((1, n), 4000 + logn, NP[dtype])
+    ref = oracle.fft(x.astype(np.complex128))
+    y = run_plan(fg, x, n, 1, 1, fg.FFT_FORWARD, dtype)
+    assert rel_rows(y, ref).max() <= tol(dtype, n)
+    y2 = run_plan(fg, x, n, 1, 1, fg.FFT_FORWARD, dtype, inplace=True)
+    assert rel_rows(y2, ref).max() <= tol(dtype, n)
+    z = run_plan(fg, y, n, 1, 1, fg.FFT_INVERSE, dtype)
+    assert rel_rows(z, x.astype(np.complex128)).max() <= 2 * tol(dtype, n)
+
+
+def test_multipass_batch_groups(fg, monkeypatch):
+    # Transforms that fit the L2 budget run all their passes group by group.
+    monkeypatch.setenv("FFT_GB300_L2_BYTES", str(2 * (1 << 16) * 8))
+    n, batch = 1 << 16, 5
+    x = workloads.uniform_complex((batch, n), 77, np.complex64)
+    y = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, F32)
+    assert rel_rows(y, oracle.fft(x.astype(np.complex128))).max() <= tol(F32, n)
+
+
+def test_2d_l2_groups(fg, monkeypatch):
+    monkeypatch.setenv("FFT_GB300_L2_BYTES", str(256 * 256 * 8))  # one image per group
+    n, batch = 256, 5
+    x = workloads.normal_complex((batch, n, n), 78, np.complex64)
+    y = run_plan(fg, x, n, batch, 2, fg.FFT_FORWARD, F32)
+    assert rel_rows(y, oracle.fft2d(x.astype(np.complex128))).max() <= tol(F32, n * n)
+    y2 = run_plan(fg, x, n, batch, 2, fg.FFT_FORWARD, F32, inplace=True)
+    assert rel_rows(y2, oracle.fft2d(x.astype(np.complex128))).max() <= tol(F32, n * n)
+
+
 # --- 2D -----------------------------------------------------------------------
 
 @pytest.mark.parametrize("dtype", [F32, F64])
