@@ -24,6 +24,7 @@ FFT_ERR_UNSUPPORTED = 3
 FFT_ERR_CUDA = 4
 FFT_ERR_ALLOC = 5
 FFT_ERR_MISALIGNED = 6
+FFT_ERR_DEVICE_TIMEOUT = 7
 
 FFT_FORWARD = -1
 FFT_INVERSE = +1
@@ -44,6 +45,7 @@ SIGNATURES = {
     "polymul_batched": (_INT, [_VP, _I64, _VP, _I64, _VP, _I64, _VP]),
     "polymul_noalloc": (_INT, [_VP, _I64, _VP, _I64, _VP, _VP]),
     "fft_debug_radix2_pass": (_INT, [_VP, _VP, _I64, _I64, _INT, _VP]),
+    "fft_device_status": (_INT, [_VP]),
     "fft_last_status": (_INT, []),
     "fft_status_string": (ctypes.c_char_p, [_INT]),
     "fft_last_cuda_error": (ctypes.c_char_p, []),
@@ -132,6 +134,10 @@ POLYMUL_NOALLOC_MAX_LEN = 65536
 def fft_debug_radix2_pass(in_ptr: int, out_ptr: int, n: int, half: int, dtype: int,
                           stream: int) -> int:
     return _lib.fft_debug_radix2_pass(in_ptr, out_ptr, n, half, dtype, stream)
+
+
+def fft_device_status(stream: int) -> int:
+    return int(_lib.fft_device_status(stream))
 
 
 def fft_last_status() -> int:

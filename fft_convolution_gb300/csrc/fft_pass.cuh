@@ -179,6 +179,10 @@ cudaError_t launch_pass_t(Load load, Store store, int log_n, int log_m, int twid
   return cudaGetLastError();
 }
 
+template <typename T, int LOGL, int DIR>
+cudaError_t launch_pass_tma_t(const void *in, void *out, int log_n, int log_m, int twiddle,
+                              long long batch, cudaStream_t st);
+
 template <typename T, int DIR, int MAXLOG, int LOGL = 1>
 cudaError_t dispatch_pass(const PassArgs &a, const void *in, void *out, cudaStream_t st) {
   if constexpr (LOGL > MAXLOG) {
@@ -187,6 +191,11 @@ cudaError_t dispatch_pass(const PassArgs &a, const void *in, void *out, cudaStre
     if (a.log_l == LOGL) {
       using V = vec2_t<T>;
       const long long n = 1LL << a.log_n;
+      if (a.subset.runs == 0) {
+        cudaError_t e = launch_pass_tma_t<T, LOGL, DIR>(in, out, a.log_n, a.log_m, a.twiddle,
+                                                        a.batch, st);
+        if (e != cudaErrorNotSupported) return e;
+      }
       return launch_pass_t<T, LOGL, DIR>(LoadComplex<V>{static_cast<const V *>(in), n},
                                          StoreComplex<V>{static_cast<V *>(out), n}, a.log_n,
                                          a.log_m, a.twiddle, a.batch, st,

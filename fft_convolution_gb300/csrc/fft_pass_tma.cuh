@@ -1,0 +1,327 @@
+// fft_pass_tma.cuh -- the HBM pass kernel of fft_pass.cuh with its strided
+// tiles moved by the Tensor Memory Accelerator.
+//
+// Same computation as fft_pass_kernel (one radix-L Stockham stage over HBM
+// whose L-point butterflies are on-chip transforms of C consecutive
+// columns), organised for sm_103a:
+//   * persistent blocks (one per SM), each walking the tiles
+//     blockIdx.x, blockIdx.x + gridDim.x, ...;
+//   * the input tile (L rows x C columns, rows 8*cols bytes apart) arrives
+//     by cp.async.bulk.tensor into one of two shared-memory buffers, tracked
+//     by an mbarrier, while the block computes the previous tile from the
+//     other buffer -- HBM reads overlap the arithmetic inside one block and
+//     the load/store units carry only the shared-memory exchanges;
+//   * outputs of passes with m > 1 (rows m elements apart) leave by a TMA
+//     tensor store from the same buffer; the first pass (m = 1), whose tile
+//     output is one contiguous block, keeps its linear coalesced stores.
+// Every mbarrier wait is bounded: a wait that runs out records
+// kDeviceErrorTimeout in the device status word and the block stops
+// (fft_device_status reports it).
+#pragma once
+
+#include <cuda.h>
+
+#include "fft_pass.cuh"
+
+namespace fftgb {
+
+constexpr int kDeviceErrorTimeout = 1;
+
+namespace {
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Bounded wait: false if the phase did not complete within ~2^22 polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  for (uint32_t it = 0; it < (1u << 22); ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, const void *src, int x, int y,
+                                             int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group"
+      " [%0, {%2, %3, %4, %5}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <typename T, int LOGL> struct TmaConfig {
+  using P = StagePlan<LOGL>;
+  using V = vec2_t<T>;
+  static constexpr int L = P::L;
+  static constexpr int C = PassConfig<T, LOGL>::C;
+  static constexpr int THREADS = C * P::TP;
+  static constexpr int ROWS_PER_BOX = L < 256 ? L : 256;  // TMA box limit per dimension
+  static constexpr int BOXES = L / ROWS_PER_BOX;
+  static constexpr uint32_t TILE_BYTES = (uint32_t)(C * L * sizeof(V));
+  static constexpr int RAW_ELEMS = PassConfig<T, LOGL>::ROW_ELEMS * C;  // exchange / transpose
+  static constexpr int BUF_ELEMS =
+      ((RAW_ELEMS * (int)sizeof(V) + 127) / 128) * 128 / (int)sizeof(V);
+  static constexpr size_t SMEM = 256 + 2 * (size_t)BUF_ELEMS * sizeof(V);
+};
+
+struct TmaGeom {
+  int log_n;
+  int log_m;
+  int twiddle;
+  long long tiles_per_batch;
+  long long total_tiles;
+};
+
+template <typename T, int LOGL, int DIR>
+__global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, 1)
+    fft_pass_tma_kernel(const __grid_constant__ CUtensorMap tin,
+                        const __grid_constant__ CUtensorMap tout, vec2_t<T> *out_linear,
+                        TmaGeom g, int *status) {
+  using Cfg = TmaConfig<T, LOGL>;
+  using P = StagePlan<LOGL>;
+  using V = vec2_t<T>;
+  constexpr int C = Cfg::C;
+  constexpr int L = Cfg::L;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  // TMA destinations must be 128-byte aligned: round the base up (the
+  // allocation carries 128 spare bytes for this).
+  unsigned char *base = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
+  uint64_t *bar = reinterpret_cast<uint64_t *>(base);
+  V *const buf0 = reinterpret_cast<V *>(base + 128);
+
+  const int tid = threadIdx.x;
+  const int c = tid % C;
+  const int t = tid / C;
+  const long long cols = 1LL << (g.log_n - LOGL);
+
+  auto issue_load = [&](long long tile, int s) {
+    const long long b = tile / g.tiles_per_batch;
+    const long long i0 = (tile % g.tiles_per_batch) * C;
+    V *dst = buf0 + s * Cfg::BUF_ELEMS;
+    mbar_expect_tx(&bar[s], Cfg::TILE_BYTES);
+#pragma unroll
+    for (int k = 0; k < Cfg::BOXES; ++k)
+      tma_load_3d(dst + k * Cfg::ROWS_PER_BOX * C, &tin, &bar[s], (int)(2 * i0),
+                  k * Cfg::ROWS_PER_BOX, (int)b);
+  };
+
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (tid == 0 && blockIdx.x < g.total_tiles) issue_load(blockIdx.x, 0);
+
+  int k = 0;
+  for (long long tile = blockIdx.x; tile < g.total_tiles; tile += gridDim.x, ++k) {
+    const int s = k & 1;
+    V *const cur = buf0 + s * Cfg::BUF_ELEMS;
+    const long long next = tile + gridDim.x;
+    __syncthreads();  // every thread is done with buffer s^1 (previous tile)
+    if (tid == 0 && next < g.total_tiles) {
+      bulk_wait_read_all();  // the previous tile's TMA store has left buffer s^1
+      issue_load(next, s ^ 1);
+    }
+    const bool ok = mbar_wait(&bar[s], (uint32_t)(k >> 1) & 1u);
+    if (__syncthreads_or(!ok)) {
+      if (tid == 0) {
+        atomicExch(status, kDeviceErrorTimeout);
+        // Let the prefetch issued above land before the block exits.
+        if (next < g.total_tiles) mbar_wait(&bar[s ^ 1], (uint32_t)((k + 1) >> 1) & 1u);
+      }
+      break;
+    }
+
+    const long long b = tile / g.tiles_per_batch;
+    const long long i = (tile % g.tiles_per_batch) * C + c;
+    V x[P::E];
+#pragma unroll
+    for (int w = 0; w < P::E; ++w) x[w] = cur[(t + w * P::TP) * C + c];
+    if (g.twiddle && g.log_m > 0) {
+      const long long p = i & ((1LL << g.log_m) - 1);
+      const int log_lm = g.log_m + LOGL;
+      const V a = twiddle<DIR>(p * t, log_lm, T());
+      const V step = twiddle<DIR>(p * P::TP, log_lm, T());
+      V pw[P::E];
+      powers<P::E>(step, pw);
+#pragma unroll
+      for (int w = 0; w < P::E; ++w) x[w] = c_mul(x[w], c_mul(a, pw[w]));
+    }
+    __syncthreads();  // the tile is in registers; buffer s becomes the exchange space
+
+    fft_on_chip<LOGL, DIR>(x, t, SmemView<V>{cur + c, C});
+    if constexpr (DIR > 0) {
+#pragma unroll
+      for (int w = 0; w < P::E; ++w) x[w] = c_scale(x[w], (T)(1.0 / L));
+    }
+
+    __syncthreads();  // the last exchange has been read
+    if (g.log_m == 0) {
+      // Outputs of butterfly i go to i*L + v: one contiguous block per tile.
+      constexpr int RS = L + 1;
+#pragma unroll
+      for (int w = 0; w < P::E; ++w) cur[c * RS + t + w * P::TP] = x[w];
+      __syncthreads();
+      V *dst = out_linear + b * (1LL << g.log_n) + (tile % g.tiles_per_batch) * C * L;
+#pragma unroll
+      for (int w = 0; w < P::E; ++w) {
+        const int o = tid + w * Cfg::THREADS;
+        dst[o] = cur[(o / L) * RS + (o % L)];
+      }
+    } else {
+      // Rows of the output tile are m elements apart: TMA tensor store.
+#pragma unroll
+      for (int w = 0; w < P::E; ++w) cur[(t + w * P::TP) * C + c] = x[w];
+      fence_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        const long long m = 1LL << g.log_m;
+        const long long q = i >> g.log_m;  // same for the whole tile (C <= m)
+        const long long p0 = (tile % g.tiles_per_batch) * C & (m - 1);
+#pragma unroll
+        for (int kb = 0; kb < Cfg::BOXES; ++kb)
+          tma_store_4d(&tout, cur + kb * Cfg::ROWS_PER_BOX * C, (int)(2 * p0),
+                       kb * Cfg::ROWS_PER_BOX, (int)q, (int)b);
+        bulk_commit();
+      }
+    }
+  }
+  if (tid == 0) bulk_wait_all();
+  (void)cols;
+}
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps and the persistent launch.
+// ---------------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, found through the runtime (no
+// link-time dependency on libcuda).
+inline EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+inline bool tma_disabled() {
+  const char *e = getenv("FFT_GB300_NO_TMA");
+  return e && *e && *e != '0';
+}
+
+// Multiprocessors of the current device (cached per device).
+inline int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!cache[dev]) cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev);
+  return cache[dev];
+}
+
+// Launches the TMA pass kernel, or returns cudaErrorNotSupported (nothing
+// launched) when the shape does not suit it: tiles narrower than 2 columns
+// (16-byte TMA rows), fewer columns than one tile, output blocks shorter than
+// a tile, FFT_GB300_NO_TMA set, or no driver entry point.
+template <typename T, int LOGL, int DIR>
+cudaError_t launch_pass_tma_t(const void *in, void *out, int log_n, int log_m, int twiddle,
+                              long long batch, cudaStream_t st) {
+  using Cfg = TmaConfig<T, LOGL>;
+  if constexpr (Cfg::C < 2 || LOGL < 4) {
+    return cudaErrorNotSupported;
+  } else {
+    const long long cols = 1LL << (log_n - LOGL);
+    EncodeTiledFn enc = encode_tiled();
+    const int sms = sm_count();
+    // An output tile must not straddle two blocks of length m (C <= m).
+    if (tma_disabled() || cols < Cfg::C || (log_m > 0 && (1LL << log_m) < Cfg::C) || !enc ||
+        sms <= 0 || batch > 0xffffffffLL)
+      return cudaErrorNotSupported;
+    const CUtensorMapDataType dt =
+        sizeof(T) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT64;
+    const cuuint64_t es = sizeof(vec2_t<T>);
+    const cuuint64_t n = 1ull << log_n;
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    // Input: [batch][L rows][cols] complex, as scalars (re, im) on the
+    // innermost axis.
+    CUtensorMap tin, tout;
+    const cuuint64_t din[3] = {2ull * (cuuint64_t)cols, (cuuint64_t)Cfg::L, (cuuint64_t)batch};
+    const cuuint64_t sin_[2] = {(cuuint64_t)cols * es, n * es};
+    const cuuint32_t box3[3] = {2u * Cfg::C, (cuuint32_t)Cfg::ROWS_PER_BOX, 1u};
+    if (enc(&tin, dt, 3, const_cast<void *>(in), din, sin_, box3, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    if (log_m > 0) {
+      // Output q*L*m + p + v*m: [batch][q][L rows v][m columns p].
+      const cuuint64_t m = 1ull << log_m;
+      const cuuint64_t Q = n / ((cuuint64_t)Cfg::L * m);
+      const cuuint64_t dout[4] = {2ull * m, (cuuint64_t)Cfg::L, Q, (cuuint64_t)batch};
+      const cuuint64_t sout[3] = {m * es, (cuuint64_t)Cfg::L * m * es, n * es};
+      const cuuint32_t box4[4] = {2u * Cfg::C, (cuuint32_t)Cfg::ROWS_PER_BOX, 1u, 1u};
+      if (enc(&tout, dt, 4, out, dout, sout, box4, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    } else {
+      tout = tin;  // unused: the first pass stores linearly
+    }
+    auto kern = fft_pass_tma_kernel<T, LOGL, DIR>;
+    static cudaError_t attr = cudaFuncSetAttribute(
+        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
+    if (attr != cudaSuccess) return attr;
+    TmaGeom g{log_n, log_m, twiddle, cols / Cfg::C, (cols / Cfg::C) * batch};
+    long long grid = (long long)sms;
+    if (grid > g.total_tiles) grid = g.total_tiles;
+    kern<<<(unsigned)grid, Cfg::THREADS, Cfg::SMEM, st>>>(
+        tin, tout, static_cast<vec2_t<T> *>(out), g, device_status_word());
+    return cudaGetLastError();
+  }
+}
+
+}  // namespace
+}  // namespace fftgb

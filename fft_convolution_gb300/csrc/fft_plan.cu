@@ -19,6 +19,22 @@
 
 using namespace fftgb;
 
+// Device status word of the bounded in-kernel waits (0 = no error).
+static __device__ int g_device_status;
+
+namespace fftgb {
+int *device_status_word() {
+  static int *cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess) cache[dev] = static_cast<int *>(p);
+  }
+  return cache[dev];
+}
+}  // namespace fftgb
+
 namespace {
 
 thread_local int g_status = FFT_OK;
@@ -410,6 +426,24 @@ int fft_debug_radix2_pass(const void *in, void *out, int64_t n, int64_t half, in
   return FFT_OK;
 }
 
+int fft_device_status(void *stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int *word = device_status_word();
+  if (!word) return cuda_fail(cudaErrorInvalidDevice);
+  int v = 0;
+  e = cudaMemcpy(&v, word, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpy(word, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return FFT_ERR_DEVICE_TIMEOUT;
+  }
+  return FFT_OK;
+}
+
 int fft_last_status(void) { return g_status; }
 
 const char *fft_status_string(int status) {
@@ -421,6 +455,7 @@ const char *fft_status_string(int status) {
     case FFT_ERR_CUDA: return "CUDA error";
     case FFT_ERR_ALLOC: return "device allocation failed";
     case FFT_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case FFT_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel ran out";
     default: return "unknown status";
   }
 }

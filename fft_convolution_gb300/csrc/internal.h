@@ -57,6 +57,10 @@ cudaError_t launch_pass_f64(int dir, const PassArgs &a, const void *in, void *ou
 constexpr int kPassMaxLogF32 = 14;
 constexpr int kPassMaxLogF64 = 13;
 
+// Device status word that bounded in-kernel waits set when they run out
+// (fft_plan.cu; fft_device_status reads and clears it).
+int *device_status_word();
+
 // One radix-2 butterfly pass (debug_pass.cu).
 cudaError_t launch_radix2_pass(int dtype, const void *in, void *out, long long n, long long half,
                                cudaStream_t st);

@@ -55,6 +55,7 @@ extern "C" {
 #define FFT_ERR_CUDA 4        /* CUDA runtime error or launch failure           */
 #define FFT_ERR_ALLOC 5       /* device allocation failed                       */
 #define FFT_ERR_MISALIGNED 6  /* a data pointer is not 16-byte aligned          */
+#define FFT_ERR_DEVICE_TIMEOUT 7 /* a bounded wait inside a kernel ran out      */
 
 /* Direction: the sign of the exponent. */
 #define FFT_FORWARD (-1) /* e^{-i...}, unscaled          */
@@ -172,6 +173,17 @@ int polymul_noalloc(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, 
  */
 int fft_debug_radix2_pass(const void *in, void *out, int64_t n, int64_t half, int dtype,
                           void *stream);
+
+/*
+ * fft_device_status -- synchronises `stream`, then reads and clears the
+ * library's device status word on the current device.  Kernels that wait
+ * for their own asynchronous copies (the TMA-staged HBM passes) bound every
+ * wait; a wait that runs out sets the word and the kernel stops early, so
+ * its output is incomplete.  Returns FFT_OK, FFT_ERR_DEVICE_TIMEOUT, or
+ * FFT_ERR_CUDA if the synchronisation itself failed.  Diagnostic: no
+ * transform call reads the word by itself.
+ */
+int fft_device_status(void *stream);
 
 /* Last status recorded on this host thread by a call that returns a
  * pointer (fft_plan_create). */

@@ -1,0 +1,165 @@
+"""GPU parity at the benchmark sizes, in the launch configuration bench.py
+times (out-of-place plans over the whole batch), on outputs the oracle can
+compute one by one, plus properties that hold at any size.
+
+* 16384 x 4096 fp32: 48 sampled transforms against the recursive CT; the
+  inverse returns the input for every transform.
+* one 2^26 fp32 transform (16 tones + noise): 32 sampled bins (the 16 tone
+  bins and 16 random ones) against the direct DFT of those bins -- relative
+  error at each tone bin, RMS-relative error at the noise bins, and a
+  stratified estimate of the whole vector's relative L2 error; Parseval and
+  the inverse round trip over the whole vector.
+* 8 images of 2048 x 2048 fp32: images 0 and 7 against the oracle's 2D
+  transform; the inverse round trip for all 8.
+* 64 polynomial pairs of 2^20 coefficients: 4096 sampled coefficients (64 per
+  pair) exact against the schoolbook sum; C(t) = A(t) B(t) mod 2^61 - 1 at two
+  points for every pair (covers every coefficient).
+
+All floating-point bounds are the relative-L2 tolerance 1e-5 * log2(N).
+"""
+import multiprocessing as mp
+import os
+import tempfile
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+TOL32 = 1e-5
+
+
+@pytest.fixture(scope="module")
+def fg(fg_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return fg_lib
+
+
+def rel_rows(y, ref):
+    y = np.asarray(y, np.complex128).reshape(ref.shape[0], -1)
+    ref = np.asarray(ref, np.complex128).reshape(ref.shape[0], -1)
+    return np.linalg.norm(y - ref, axis=1) / np.linalg.norm(ref, axis=1)
+
+
+def _bins_worker(args):
+    path, ks = args
+    x = np.load(path, mmap_mode="r")
+    return oracle.dft_bins(np.asarray(x), ks)
+
+
+def test_c2_batched_4096(fg):
+    c = workloads.CONFIGS["c2"]
+    n, batch = c["n"], c["batch"]
+    x = workloads.config_input("c2")
+    xd = torch.from_numpy(x).cuda()
+    yd = torch.empty_like(xd)
+    zd = torch.empty_like(xd)
+    pf = fg.Plan(n, batch, 1, fg.FFT_FORWARD, fg.FFT_C2C_F32)
+    pi = fg.Plan(n, batch, 1, fg.FFT_INVERSE, fg.FFT_C2C_F32)
+    pf.exec(xd, yd)
+    pi.exec(yd, zd)
+    torch.cuda.synchronize()
+    idx = np.unique(workloads.sample_indices(48, batch, 21))
+    y = yd[torch.from_numpy(idx).cuda()].cpu().numpy()
+    ref = oracle.fft(x[idx].astype(np.complex128))
+    assert rel_rows(y, ref).max() <= TOL32 * 12
+    z = zd.cpu().numpy()
+    assert rel_rows(z, x).max() <= 2 * TOL32 * 12
+    assert fg.fft_device_status(int(torch.cuda.current_stream().cuda_stream)) == 0
+    pf.close()
+    pi.close()
+
+
+def test_c3_single_2e26(fg):
+    c = workloads.CONFIGS["c3"]
+    n = c["n"]
+    x = workloads.config_input("c3")[0]
+    xd = torch.from_numpy(x).cuda()
+    yd = torch.empty_like(xd)
+    zd = torch.empty_like(xd)
+    pf = fg.Plan(n, 1, 1, fg.FFT_FORWARD, fg.FFT_C2C_F32)
+    pi = fg.Plan(n, 1, 1, fg.FFT_INVERSE, fg.FFT_C2C_F32)
+    pf.exec(xd, yd)
+    pi.exec(yd, zd)
+    torch.cuda.synchronize()
+    y = yd.cpu().numpy().astype(np.complex128)
+    z = zd.cpu().numpy().astype(np.complex128)
+    x64 = x.astype(np.complex128)
+    # Sampled bins: the 16 tone bins and 16 seeded random bins.
+    bins, _, _ = workloads.tone_params(n, c["seed"])
+    ks = np.concatenate([bins, workloads.sample_indices(16, n, 33)])
+    with tempfile.TemporaryDirectory() as td:
+        path = os.path.join(td, "x.npy")
+        np.save(path, x64)
+        chunks = [(path, ks[i::8]) for i in range(8)]
+        with mp.get_context("spawn").Pool(8) as pool:
+            parts = pool.map(_bins_worker, chunks)
+    ref = np.empty(ks.size, np.complex128)
+    for i in range(8):
+        ref[i::8] = parts[i]
+    tol = TOL32 * 26
+    err = y[ks] - ref
+    # Tone bins (magnitude N): relative error of each.
+    assert np.max(np.abs(err[:16]) / np.abs(ref[:16])) <= tol
+    # Noise bins: error against the spectrum's RMS magnitude.
+    rms = np.linalg.norm(y) / np.sqrt(n)
+    assert np.linalg.norm(err[16:]) / (np.sqrt(16) * rms) <= tol
+    # Stratified estimate of the whole transform's relative L2 error: the 16
+    # tone bins exactly, the other N - 16 bins from the 16-bin sample.
+    est = np.sum(np.abs(err[:16]) ** 2) + (n - 16) / 16 * np.sum(np.abs(err[16:]) ** 2)
+    assert np.sqrt(est) / np.linalg.norm(y) <= tol
+    # Tones: magnitude N at their bins.
+    assert np.all(np.abs(np.abs(ref[:16]) - n) < 0.01 * n)
+    # Parseval and the round trip over the whole vector.
+    ex, eX = np.sum(np.abs(x64) ** 2), np.sum(np.abs(y) ** 2) / n
+    assert abs(ex - eX) / ex <= TOL32 * 26
+    assert np.linalg.norm(z - x64) / np.linalg.norm(x64) <= 2 * TOL32 * 26
+    assert fg.fft_device_status(int(torch.cuda.current_stream().cuda_stream)) == 0
+    pf.close()
+    pi.close()
+
+
+def test_c4_2d_2048(fg):
+    c = workloads.CONFIGS["c4"]
+    n, batch = c["n"], c["batch"]
+    x = workloads.config_input("c4")
+    xd = torch.from_numpy(x).cuda()
+    yd = torch.empty_like(xd)
+    zd = torch.empty_like(xd)
+    pf = fg.Plan(n, batch, 2, fg.FFT_FORWARD, fg.FFT_C2C_F32)
+    pi = fg.Plan(n, batch, 2, fg.FFT_INVERSE, fg.FFT_C2C_F32)
+    pf.exec(xd, yd)
+    pi.exec(yd, zd)
+    torch.cuda.synchronize()
+    for b in (0, batch - 1):
+        y = yd[b].cpu().numpy()
+        ref = oracle.fft2d(x[b].astype(np.complex128))
+        assert rel_rows(y[None], ref[None]).max() <= TOL32 * 22
+    z = zd.cpu().numpy()
+    assert rel_rows(z, x).max() <= 2 * TOL32 * 22
+    pf.close()
+    pi.close()
+
+
+def test_c5_polymul_64_pairs(fg):
+    c = workloads.CONFIGS["c5"]
+    n, batch = c["n"], c["batch"]
+    a, b = workloads.config_input("c5")
+    cd = fg.polymul_tensors(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda())
+    torch.cuda.synchronize()
+    out = cd.cpu().numpy()
+    nc = 2 * n - 1
+    assert out.shape == (batch, nc)
+    for p in range(batch):
+        idx = workloads.sample_indices(64, nc, 1000 + p)
+        assert np.array_equal(out[p][idx], oracle.polymul_schoolbook_at(a[p], b[p], idx)), p
+        for t in workloads.sample_indices(2, oracle.MOD_P, 2000 + p):
+            t = int(t)
+            lhs = oracle.poly_eval_mod(out[p], t)
+            rhs = oracle.poly_eval_mod(a[p], t) * oracle.poly_eval_mod(b[p], t) % oracle.MOD_P
+            assert lhs == rhs, p

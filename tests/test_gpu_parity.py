@@ -143,6 +143,26 @@ def test_multipass_fused_l2_groups(fg, monkeypatch, dtype, logn, budget):
     assert rel_rows(z, x.astype(np.complex128)).max() <= 2 * tol(dtype, n)
 
 
+@pytest.mark.parametrize("dims,dtype,logn", [(1, F32, 18), (1, F32, 22), (1, F64, 17),
+                                              (2, F32, 11), (2, F64, 9)])
+def test_lsu_pass_kernel(fg, monkeypatch, dims, dtype, logn):
+    # The pass kernel with plain loads/stores (what runs when the TMA path
+    # does not apply) on shapes that normally take the TMA path.
+    monkeypatch.setenv("FFT_GB300_NO_TMA", "1")
+    n = 1 << logn
+    shape = (1, n) if dims == 1 else (1, n, n)
+    x = workloads.normal_complex(shape, 5000 + logn, NP[dtype])
+    y = run_plan(fg, x, n, 1, dims, fg.FFT_FORWARD, dtype)
+    ref = oracle.fft(x.astype(np.complex128)) if dims == 1 else np.fft.fft2(x.astype(np.complex128))
+    npts = n if dims == 1 else n * n
+    assert rel_rows(y, ref).max() <= tol(dtype, npts)
+
+
+def test_device_status_clear_after_transforms(fg):
+    # No bounded in-kernel wait ran out during the transforms above.
+    assert fg.fft_device_status(stream()) == 0
+
+
 def test_multipass_batch_groups(fg, monkeypatch):
     # Transforms that fit the L2 budget run all their passes group by group.
     monkeypatch.setenv("FFT_GB300_L2_BYTES", str(2 * (1 << 16) * 8))
