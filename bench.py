@@ -300,7 +300,7 @@ def run_gpu(args):
                 if events is not None:
                     events[1].record(stream)
             assert rc == 0, fg.fft_status_string(rc)
-        kernels_per_step = 3 * max(1, math.ceil(log2i(info["L"]) / 9))
+        kernels_per_step = fg.polymul_num_kernels(c["n"], c["n"])
     else:
         x_h = sized_input(name, c)
         x_d = torch.from_numpy(x_h).to(dev)

@@ -44,6 +44,7 @@ SIGNATURES = {
     "polymul": (_INT, [_VP, _I64, _VP, _I64, _VP, _VP]),
     "polymul_batched": (_INT, [_VP, _I64, _VP, _I64, _VP, _I64, _VP]),
     "polymul_noalloc": (_INT, [_VP, _I64, _VP, _I64, _VP, _VP]),
+    "polymul_num_kernels": (_INT, [_I64, _I64]),
     "fft_debug_radix2_pass": (_INT, [_VP, _VP, _I64, _I64, _INT, _VP]),
     "fft_device_status": (_INT, [_VP]),
     "fft_last_status": (_INT, []),
@@ -129,6 +130,10 @@ def polymul_noalloc(a_ptr: int, na: int, b_ptr: int, nb: int, c_ptr: int, stream
 
 
 POLYMUL_NOALLOC_MAX_LEN = 65536
+
+
+def polymul_num_kernels(na: int, nb: int) -> int:
+    return int(_lib.polymul_num_kernels(na, nb))
 
 
 def fft_debug_radix2_pass(in_ptr: int, out_ptr: int, n: int, half: int, dtype: int,

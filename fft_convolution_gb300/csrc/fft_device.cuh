@@ -196,6 +196,12 @@ template <int LOGL> struct StagePlan {
   }
   // Shared-memory elements needed for the exchanges (padded by one per 16).
   static constexpr int SMEM_ELEMS = NS > 1 ? L + L / 16 : 0;
+  // Twiddle table (optional): stage k > 0 keeps W_{R m}^{p u} for u < R,
+  // p < m at tw_offset(k) + u*m + p.
+  __host__ __device__ static constexpr int tw_offset(int k) {
+    return k <= 1 ? 0 : tw_offset(k - 1) + (radix(k - 1) << log_m(k - 1));
+  }
+  static constexpr int TW_ELEMS = NS > 1 ? tw_offset(NS) : 0;
 };
 
 // Padded shared-memory position: one spare slot every 16 elements keeps the
@@ -217,8 +223,10 @@ template <typename V> struct SmemView {
 // i = t + s*TP; its inputs are x[s + u*(E/R)] and its outputs go back to the
 // same registers.  m = 2^LOGM is the previous block length (twiddle
 // W_{R m}^{(i mod m) u} on input u).
-template <int R, int E, int TP, int LOGM, int DIR, typename V>
-__device__ __forceinline__ void stage_compute(V *x, int t) {
+// With a twiddle table (tw != nullptr, this stage's part of it) the
+// twiddles are read from it instead of computed.
+template <int R, int E, int TP, int LOGM, int DIR, bool TABLE, typename V>
+__device__ __forceinline__ void stage_compute(V *x, int t, const V *tw) {
   constexpr int S = E / R;
 #pragma unroll
   for (int s = 0; s < S; ++s) {
@@ -230,11 +238,16 @@ __device__ __forceinline__ void stage_compute(V *x, int t) {
       constexpr int M = 1 << LOGM;
       const int i = t + s * TP;
       const int p = i & (M - 1);
-      V w = twiddle<DIR>((long long)p, LOGM + ilog2(R), T());
-      V pw[R];
-      powers<R>(w, pw);
+      if constexpr (TABLE) {
 #pragma unroll
-      for (int u = 1; u < R; ++u) y[u] = c_mul(y[u], pw[u]);
+        for (int u = 1; u < R; ++u) y[u] = c_mul(y[u], tw[u * M + p]);
+      } else {
+        V w = twiddle<DIR>((long long)p, LOGM + ilog2(R), T());
+        V pw[R];
+        powers<R>(w, pw);
+#pragma unroll
+        for (int u = 1; u < R; ++u) y[u] = c_mul(y[u], pw[u]);
+      }
     }
     dft_reg<R, DIR>(y);
 #pragma unroll
@@ -258,8 +271,8 @@ __device__ __forceinline__ void stage_store(const V *x, int t, const SmemView<V>
   }
 }
 
-template <int LOGL, int K, int DIR, typename V>
-__device__ __forceinline__ void run_stages(V *x, int t, const SmemView<V> &sm) {
+template <int LOGL, int K, int DIR, bool TABLE, typename V>
+__device__ __forceinline__ void run_stages(V *x, int t, const SmemView<V> &sm, const V *tw) {
   using P = StagePlan<LOGL>;
   if constexpr (K < P::NS) {
     constexpr int R = P::radix(K);
@@ -268,23 +281,70 @@ __device__ __forceinline__ void run_stages(V *x, int t, const SmemView<V> &sm) {
 #pragma unroll
       for (int w = 0; w < P::E; ++w) x[w] = sm.ld(t + w * P::TP);
     }
-    stage_compute<R, P::E, P::TP, LOGM, DIR>(x, t);
+    stage_compute<R, P::E, P::TP, LOGM, DIR, TABLE>(x, t, TABLE ? tw + P::tw_offset(K) : tw);
     if constexpr (K + 1 < P::NS) {
       __syncthreads();  // everyone has read the previous stage's data
       stage_store<R, P::E, P::TP, LOGM>(x, t, sm);
       __syncthreads();  // this stage's data is complete
     }
-    run_stages<LOGL, K + 1, DIR>(x, t, sm);
+    run_stages<LOGL, K + 1, DIR, TABLE>(x, t, sm, tw);
   }
 }
 
 // The whole on-chip transform of length 2^LOGL.  On entry x[w] is element
 // t + w*TP of the input (natural order); on exit x[w] is element t + w*TP of
 // its DFT (natural order).  Every thread of the block must call this the
-// same number of times (it contains __syncthreads when L > 16).
+// same number of times (it contains __syncthreads when L > 16).  With
+// TABLE, the stage twiddles come from `tw` (filled by fill_twiddle_table).
+template <int LOGL, int DIR, bool TABLE = false, typename V>
+__device__ __forceinline__ void fft_on_chip(V *x, int t, const SmemView<V> &sm,
+                                            const V *tw = nullptr) {
+  run_stages<LOGL, 0, DIR, TABLE>(x, t, sm, tw);
+}
+
+// Fills the stage-twiddle table of an on-chip transform of length 2^LOGL
+// (StagePlan::TW_ELEMS entries), each entry from one accurate evaluation.
+// Threads tid = 0 .. nthreads-1 of the block share the work; the caller
+// synchronises before use.
 template <int LOGL, int DIR, typename V>
-__device__ __forceinline__ void fft_on_chip(V *x, int t, const SmemView<V> &sm) {
-  run_stages<LOGL, 0, DIR>(x, t, sm);
+__device__ __forceinline__ void fill_twiddle_table(V *tw, int tid, int nthreads) {
+  using P = StagePlan<LOGL>;
+  using T = decltype(V::x);
+  for (int k = 1; k < P::NS; ++k) {
+    const int R = P::radix(k), lm = P::log_m(k), M = 1 << lm;
+    V *dst = tw + P::tw_offset(k);
+    for (int e = tid; e < R * M; e += nthreads) {
+      const int u = e >> lm, p = e & (M - 1);
+      dst[e] = twiddle<DIR>((long long)p * u, lm + ilog2(R), T());
+    }
+  }
+}
+
+// x[w] *= a * s^w for w < E (the inter-pass twiddle of one thread's
+// elements): the factors a s^w are built as a, a s, a s^2, a s^3 and then
+// stepped by s^4, at most five products deep.
+template <int E, typename V> __device__ __forceinline__ void apply_geometric(V *x, V a, V s) {
+  if constexpr (E >= 4 && E % 4 == 0) {
+    const V s2 = c_mul(s, s), s4 = c_mul(s2, s2);
+    V q[4];
+    q[0] = a;
+    q[1] = c_mul(a, s);
+    q[2] = c_mul(a, s2);
+    q[3] = c_mul(q[1], s2);
+#pragma unroll
+    for (int blk = 0; blk < E / 4; ++blk) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[4 * blk + j] = c_mul(x[4 * blk + j], q[j]);
+        if (blk + 1 < E / 4) q[j] = c_mul(q[j], s4);
+      }
+    }
+  } else {
+    V pw[E];
+    powers<E>(s, pw);
+#pragma unroll
+    for (int w = 0; w < E; ++w) x[w] = c_mul(x[w], c_mul(a, pw[w]));
+  }
 }
 
 }  // namespace fftgb

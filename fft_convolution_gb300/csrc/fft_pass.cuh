@@ -44,7 +44,9 @@ template <typename T, int LOGL> struct PassConfig {
   static constexpr int MIN_BLOCKS = THREADS >= 1024 ? 1 : 1024 / THREADS;
   static constexpr int ROW_ELEMS =
       P::SMEM_ELEMS > P::L + 1 ? P::SMEM_ELEMS : P::L + 1;  // exchange or transpose
-  static constexpr size_t SMEM = (size_t)C * ROW_ELEMS * sizeof(vec2_t<T>);
+  static constexpr int EXCHANGE_ELEMS = C * ROW_ELEMS;
+  // Exchange space, then the stage-twiddle table shared by the tile's columns.
+  static constexpr size_t SMEM = ((size_t)EXCHANGE_ELEMS + P::TW_ELEMS) * sizeof(vec2_t<T>);
 };
 
 // Plain complex load / store (element `pos` of transform `b`).
@@ -66,85 +68,115 @@ template <typename V> struct StoreComplex {
 // Which tiles a launch covers.  Block r of a transform takes tile
 // tile_lo + (r mod tile_run) + (r / tile_run) * tile_jump; a launch over all
 // tiles has tile_lo = 0, tile_run = grid_per_batch, tile_jump = 0.
+// Optional two-level table of the inter-pass twiddles W_{L m}^e for this
+// pass's direction: W^e = hi[e >> lo_bits] * lo[e & (2^lo_bits - 1)].
+// Used where sincospi is expensive (fp64); lo == nullptr computes them.
+// The tables are built for W_{2^log_size}; a pass with L m < 2^log_size
+// scales its exponent up.
+template <typename V> struct TwiddleTables {
+  const V *lo;
+  const V *hi;
+  int lo_bits;
+  int log_size;
+};
+
 struct PassGeom {
   int log_n;
   int log_m;
   int twiddle;
-  long long grid_per_batch;  // blocks per transform in this launch
+  long long grid_per_batch;  // tiles per transform in this launch
   long long tile_lo;
   long long tile_run;
   long long tile_jump;
+  long long total;  // grid_per_batch * batch: the tiles of the launch
 };
 
+// Persistent: each block fills the stage-twiddle table once, then walks
+// the launch's tiles blockIdx.x, blockIdx.x + gridDim.x, ...
 template <typename T, int LOGL, int DIR, class Load, class Store>
 __global__ void __launch_bounds__(PassConfig<T, LOGL>::THREADS, PassConfig<T, LOGL>::MIN_BLOCKS)
-    fft_pass_kernel(Load load, Store store, PassGeom g) {
+    fft_pass_kernel(Load load, Store store, PassGeom g, TwiddleTables<vec2_t<T>> tt) {
   using V = vec2_t<T>;
   using P = StagePlan<LOGL>;
-  constexpr int C = PassConfig<T, LOGL>::C;
+  using Cfg = PassConfig<T, LOGL>;
+  constexpr int C = Cfg::C;
   constexpr int L = P::L;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   V *smem = reinterpret_cast<V *>(smem_raw);
+  V *twt = smem + Cfg::EXCHANGE_ELEMS;
 
   const int c = threadIdx.x % C;   // column within the tile
   const int t = threadIdx.x / C;   // thread within the column
-  const long long r = blockIdx.x % g.grid_per_batch;
-  const long long b = blockIdx.x / g.grid_per_batch;
-  const long long tile = g.tile_lo + r % g.tile_run + (r / g.tile_run) * g.tile_jump;
   const long long cols = 1LL << (g.log_n - LOGL);  // N / L butterflies
-  const long long i = tile * C + c;
-  const bool active = i < cols;
+  fill_twiddle_table<LOGL, DIR>(twt, threadIdx.x, Cfg::THREADS);
+  __syncthreads();
 
-  V x[P::E];
-  if (active) {
+  for (long long blk = blockIdx.x; blk < g.total; blk += gridDim.x) {
+    const long long r = blk % g.grid_per_batch;
+    const long long b = blk / g.grid_per_batch;
+    const long long tile = g.tile_lo + r % g.tile_run + (r / g.tile_run) * g.tile_jump;
+    const long long i = tile * C + c;
+    const bool active = i < cols;
+
+    V x[P::E];
+    if (active) {
 #pragma unroll
-    for (int w = 0; w < P::E; ++w) x[w] = load(b, i + (long long)(t + w * P::TP) * cols);
-    if (g.twiddle && g.log_m > 0) {
-      // W_{L m}^{p u} for u = t + w*TP:  W^{p t} * (W^{p TP})^w.
-      const long long p = i & ((1LL << g.log_m) - 1);
-      const int log_lm = g.log_m + LOGL;
-      const V a = twiddle<DIR>(p * t, log_lm, T());
-      const V step = twiddle<DIR>(p * P::TP, log_lm, T());
-      V pw[P::E];
-      powers<P::E>(step, pw);
+      for (int w = 0; w < P::E; ++w) x[w] = load(b, i + (long long)(t + w * P::TP) * cols);
+      if (g.twiddle && g.log_m > 0) {
+        // W_{L m}^{p u} for u = t + w*TP.
+        const long long p = i & ((1LL << g.log_m) - 1);
+        const int log_lm = g.log_m + LOGL;
+        if (tt.lo) {
+          const long long emask = (1LL << log_lm) - 1, lmask = (1LL << tt.lo_bits) - 1;
+          const int up = tt.log_size - log_lm;
 #pragma unroll
-      for (int w = 0; w < P::E; ++w) x[w] = c_mul(x[w], c_mul(a, pw[w]));
+          for (int w = 0; w < P::E; ++w) {
+            const long long e = ((p * (t + w * P::TP)) & emask) << up;
+            x[w] = c_mul(x[w], c_mul(tt.hi[e >> tt.lo_bits], tt.lo[e & lmask]));
+          }
+        } else {
+          // W^{p t} * (W^{p TP})^w.
+          apply_geometric<P::E>(x, twiddle<DIR>(p * t, log_lm, T()),
+                                twiddle<DIR>(p * P::TP, log_lm, T()));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int w = 0; w < P::E; ++w) x[w] = make_c<V>((T)0, (T)0);
     }
-  } else {
-#pragma unroll
-    for (int w = 0; w < P::E; ++w) x[w] = make_c<V>((T)0, (T)0);
-  }
 
-  const SmemView<V> sm{smem + c, C};
-  fft_on_chip<LOGL, DIR>(x, t, sm);
+    const SmemView<V> sm{smem + c, C};
+    fft_on_chip<LOGL, DIR, true>(x, t, sm, twt);
 
-  if constexpr (DIR > 0) {
+    if constexpr (DIR > 0) {
 #pragma unroll
-    for (int w = 0; w < P::E; ++w) x[w] = c_scale(x[w], (T)(1.0 / L));  // 1/L per pass
-  }
-
-  if (g.log_m == 0) {
-    // First pass: butterfly i's outputs go to i*L + v, so the tile's outputs
-    // are the contiguous block [tile*C*L, (tile+1)*C*L).  Stage them in
-    // shared memory (row c padded to L+1 slots) and write linearly.
-    constexpr int RS = L + 1;
-    __syncthreads();
-#pragma unroll
-    for (int w = 0; w < P::E; ++w) smem[c * RS + t + w * P::TP] = x[w];
-    __syncthreads();
-    const long long base = tile * C * L;
-#pragma unroll
-    for (int w = 0; w < P::E; ++w) {
-      const int o = threadIdx.x + w * PassConfig<T, LOGL>::THREADS;
-      const int cc = o / L, v = o % L;
-      if (tile * C + cc < cols) store(b, base + o, smem[cc * RS + v]);
+      for (int w = 0; w < P::E; ++w) x[w] = c_scale(x[w], (T)(1.0 / L));  // 1/L per pass
     }
-  } else if (active) {
-    const long long m = 1LL << g.log_m;
-    const long long q = i >> g.log_m, p = i & (m - 1);
-    const long long base = q * L * m + p;
+
+    if (g.log_m == 0) {
+      // First pass: butterfly i's outputs go to i*L + v, so the tile's outputs
+      // are the contiguous block [tile*C*L, (tile+1)*C*L).  Stage them in
+      // shared memory (row c padded to L+1 slots) and write linearly.
+      constexpr int RS = L + 1;
+      __syncthreads();
 #pragma unroll
-    for (int w = 0; w < P::E; ++w) store(b, base + (long long)(t + w * P::TP) * m, x[w]);
+      for (int w = 0; w < P::E; ++w) smem[c * RS + t + w * P::TP] = x[w];
+      __syncthreads();
+      const long long base = tile * C * L;
+#pragma unroll
+      for (int w = 0; w < P::E; ++w) {
+        const int o = threadIdx.x + w * Cfg::THREADS;
+        const int cc = o / L, v = o % L;
+        if (tile * C + cc < cols) store(b, base + o, smem[cc * RS + v]);
+      }
+    } else if (active) {
+      const long long m = 1LL << g.log_m;
+      const long long q = i >> g.log_m, p = i & (m - 1);
+      const long long base = q * L * m + p;
+#pragma unroll
+      for (int w = 0; w < P::E; ++w) store(b, base + (long long)(t + w * P::TP) * m, x[w]);
+    }
+    __syncthreads();  // shared memory is free for the next tile
   }
 }
 
@@ -157,7 +189,8 @@ template <typename T, int LOGL> long long pass_tiles(int log_n) {
 
 template <typename T, int LOGL, int DIR, class Load, class Store>
 cudaError_t launch_pass_t(Load load, Store store, int log_n, int log_m, int twiddle,
-                          long long batch, cudaStream_t st, const TileSet *subset = nullptr) {
+                          long long batch, cudaStream_t st, const TileSet *subset = nullptr,
+                          TwiddleTables<vec2_t<T>> tt = {nullptr, nullptr, 0, 0}) {
   using C = PassConfig<T, LOGL>;
   auto kern = fft_pass_kernel<T, LOGL, DIR, Load, Store>;
   if (C::SMEM > 48 * 1024) {
@@ -166,16 +199,27 @@ cudaError_t launch_pass_t(Load load, Store store, int log_n, int log_m, int twid
     if (attr != cudaSuccess) return attr;
   }
   const long long tiles = pass_tiles<T, LOGL>(log_n);
-  PassGeom g{log_n, log_m, twiddle, tiles, 0, tiles, 0};
+  PassGeom g{log_n, log_m, twiddle, tiles, 0, tiles, 0, 0};
   if (subset) {
     g.grid_per_batch = subset->runs * subset->run;
     g.tile_lo = subset->lo;
     g.tile_run = subset->run;
     g.tile_jump = subset->jump;
   }
-  const long long grid = g.grid_per_batch * batch;
-  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)grid, C::THREADS, C::SMEM, st>>>(load, store, g);
+  g.total = g.grid_per_batch * batch;
+  if (g.total <= 0) return cudaErrorInvalidConfiguration;
+  // Persistent grid: as many blocks as fit on the device at once.
+  static int per_sm = 0;
+  if (per_sm == 0 &&
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::THREADS, C::SMEM) !=
+          cudaSuccess)
+    return cudaGetLastError();
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long grid = (long long)(per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
+  if (grid > g.total) grid = g.total;
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM, st>>>(load, store, g, tt);
   return cudaGetLastError();
 }
 

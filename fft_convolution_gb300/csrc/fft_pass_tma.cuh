@@ -95,7 +95,11 @@ template <typename T, int LOGL> struct TmaConfig {
   static constexpr int RAW_ELEMS = PassConfig<T, LOGL>::ROW_ELEMS * C;  // exchange / transpose
   static constexpr int BUF_ELEMS =
       ((RAW_ELEMS * (int)sizeof(V) + 127) / 128) * 128 / (int)sizeof(V);
-  static constexpr size_t SMEM = 256 + 2 * (size_t)BUF_ELEMS * sizeof(V);
+  // Stage-twiddle table shared by the block's columns (rounded to 128 B).
+  static constexpr int TW_ELEMS =
+      ((P::TW_ELEMS * (int)sizeof(V) + 127) / 128) * 128 / (int)sizeof(V);
+  static constexpr size_t SMEM =
+      256 + (size_t)TW_ELEMS * sizeof(V) + 2 * (size_t)BUF_ELEMS * sizeof(V);
 };
 
 struct TmaGeom {
@@ -121,7 +125,8 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, 1)
   // allocation carries 128 spare bytes for this).
   unsigned char *base = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
   uint64_t *bar = reinterpret_cast<uint64_t *>(base);
-  V *const buf0 = reinterpret_cast<V *>(base + 128);
+  V *const twt = reinterpret_cast<V *>(base + 128);
+  V *const buf0 = twt + Cfg::TW_ELEMS;
 
   const int tid = threadIdx.x;
   const int c = tid % C;
@@ -144,6 +149,7 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, 1)
     mbar_init(&bar[1], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  fill_twiddle_table<LOGL, DIR>(twt, tid, Cfg::THREADS);
   __syncthreads();
   if (tid == 0 && blockIdx.x < g.total_tiles) issue_load(blockIdx.x, 0);
 
@@ -175,16 +181,12 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, 1)
     if (g.twiddle && g.log_m > 0) {
       const long long p = i & ((1LL << g.log_m) - 1);
       const int log_lm = g.log_m + LOGL;
-      const V a = twiddle<DIR>(p * t, log_lm, T());
-      const V step = twiddle<DIR>(p * P::TP, log_lm, T());
-      V pw[P::E];
-      powers<P::E>(step, pw);
-#pragma unroll
-      for (int w = 0; w < P::E; ++w) x[w] = c_mul(x[w], c_mul(a, pw[w]));
+      apply_geometric<P::E>(x, twiddle<DIR>(p * t, log_lm, T()),
+                            twiddle<DIR>(p * P::TP, log_lm, T()));
     }
     __syncthreads();  // the tile is in registers; buffer s becomes the exchange space
 
-    fft_on_chip<LOGL, DIR>(x, t, SmemView<V>{cur + c, C});
+    fft_on_chip<LOGL, DIR, true>(x, t, SmemView<V>{cur + c, C}, twt);
     if constexpr (DIR > 0) {
 #pragma unroll
       for (int w = 0; w < P::E; ++w) x[w] = c_scale(x[w], (T)(1.0 / L));

@@ -393,11 +393,11 @@ int polymul_batched(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, 
   if (((uintptr_t)a & 7u) || ((uintptr_t)b & 7u) || ((uintptr_t)c & 7u))
     return FFT_ERR_MISALIGNED;
   const int64_t nc = na + nb - 1;
-  const int log_len = nc > 1 ? ilog2_exact(nc) : 1;  // at least a 2-point transform
+  const int log_len = nc > 4 ? ilog2_exact(nc) : 2;  // at least a 4-point transform
   if (log_len > 27 || batch > ((int64_t)1 << 36) / ((int64_t)1 << log_len))
     return FFT_ERR_UNSUPPORTED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t bytes = (size_t)3 * (size_t)batch * ((size_t)1 << log_len) * 16;
+  const size_t bytes = polymul_scratch_bytes(batch, log_len);
   void *scratch = nullptr;
   cudaError_t e = cudaMallocAsync(&scratch, bytes, st);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -408,6 +408,14 @@ int polymul_batched(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, 
   if (e != cudaSuccess) return cuda_fail(e);
   if (f != cudaSuccess) return cuda_fail(f);
   return FFT_OK;
+}
+
+int polymul_num_kernels(int64_t na, int64_t nb) {
+  if (na <= 0 || nb <= 0) return 0;
+  const int64_t nc = na + nb - 1;
+  const int log_len = nc > 4 ? ilog2_exact(nc) : 2;
+  if (log_len > 27) return 0;
+  return fftgb::polymul_num_kernels(log_len);
 }
 
 int polymul(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, int64_t *c,

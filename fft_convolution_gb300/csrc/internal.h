@@ -65,8 +65,11 @@ int *device_status_word();
 cudaError_t launch_radix2_pass(int dtype, const void *in, void *out, long long n, long long half,
                                cudaStream_t st);
 
-// Fused polynomial multiplication (polymul.cu).  Scratch must hold
-// 3 * batch * 2^log_len complex doubles.
+// Fused polynomial multiplication (polymul.cu): transforms of length
+// 2^log_len (2 <= log_len <= 27) over `batch` pairs; scratch must hold
+// polymul_scratch_bytes(batch, log_len) bytes.
+size_t polymul_scratch_bytes(long long batch, int log_len);
+int polymul_num_kernels(int log_len);
 cudaError_t launch_polymul(const long long *a, long long na, const long long *b, long long nb,
                            long long *c, long long batch, int log_len, void *scratch,
                            cudaStream_t st);

@@ -3,135 +3,217 @@
 // point values at the roots of unity -> pointwise product -> inverse
 // transform -> coefficients).
 //
-// Both inputs are zero-padded to L = 2^log_len >= na + nb - 1 and
-// transformed with the multi-pass Stockham kernel of fft_pass.cuh; the
-// padding and the int64 -> fp64 conversion happen inside the first pass's
-// loads, the pointwise product inside the last forward pass of b (it reads
-// A_k at the position it is about to write), and the 1/L scaling plus the
-// rounding to int64 inside the last inverse pass's stores.  No separate
-// conversion, product or rounding kernel touches HBM.
+// Both inputs are real, and so is the product, which lets one complex
+// transform of length L carry both inputs and one of length L/2 carry the
+// product back (both identities follow from the DFT definition and the
+// symmetry X_{L-k} = conj(X_k) of a real sequence's spectrum):
+//
+//  1. z = a + i b, zero-padded to L = 2^log_len >= na + nb - 1; Z = FFT_L(z)
+//     (the int64 -> fp64 conversion and the padding happen in the first
+//     pass's loads).
+//  2. combine (one O(L) kernel), for k < L/2:
+//        A_k = (Z_k + conj Z_{L-k}) / 2,   B_k = (Z_k - conj Z_{L-k}) / (2i)
+//        C_k = A_k B_k  (the pointwise product of the point values),
+//     and the same at k + L/2; then
+//        E_k = (C_k + C_{k+L/2}) / 2,  O_k = (C_k - C_{k+L/2}) W_L^{-k} / 2,
+//        Y_k = E_k + i O_k,
+//     which is the L/2-point DFT of y[n] = c[2n] + i c[2n+1].
+//  3. y = IFFT_{L/2}(Y) (1/(L/2) folded into its passes); its last pass
+//     rounds to int64 and stores c[2n] = Re y[n], c[2n+1] = Im y[n].
+//
+// The transforms are the multi-pass Stockham kernels of fft_pass.cuh.
 #include "fft_pass.cuh"
 
 namespace fftgb {
 
-// int64 coefficients, zero beyond na (the padding), as complex fp64.
-struct LoadInt64Pad {
+// a + i b as complex fp64, zero beyond na / nb (the padding).
+struct LoadPairInt64 {
   const long long *a;
-  long long na;
-  __device__ __forceinline__ double2 operator()(long long b, long long pos) const {
-    return pos < na ? make_c<double2>((double)a[b * na + pos], 0.0) : make_c<double2>(0.0, 0.0);
+  const long long *b;
+  long long na, nb;
+  __device__ __forceinline__ double2 operator()(long long p, long long pos) const {
+    return make_c<double2>(pos < na ? (double)a[p * na + pos] : 0.0,
+                           pos < nb ? (double)b[p * nb + pos] : 0.0);
   }
 };
 
-// Pointwise product with the other operand's spectrum: out_k = X_k * A_k.
-struct StoreMulComplex {
-  double2 *out;
-  const double2 *other;
-  long long bstride;
-  __device__ __forceinline__ void operator()(long long b, long long pos, double2 v) const {
-    const long long k = b * bstride + pos;
-    out[k] = c_mul(v, other[k]);
-  }
-};
-
-// Real part rounded to the nearest integer (halves away from zero), only
-// the first nc coefficients.
-struct StoreRoundInt64 {
+// y[n] -> c[2n] = round(Re y[n]), c[2n+1] = round(Im y[n]) (halves away from
+// zero), only the first nc coefficients.
+struct StoreRoundPairsInt64 {
   long long *c;
   long long nc;
-  __device__ __forceinline__ void operator()(long long b, long long pos, double2 v) const {
-    if (pos < nc) c[b * nc + pos] = llround(v.x);
+  __device__ __forceinline__ void operator()(long long p, long long pos, double2 v) const {
+    const long long k = 2 * pos;
+    if (k < nc) c[p * nc + k] = llround(v.x);
+    if (k + 1 < nc) c[p * nc + k + 1] = llround(v.y);
   }
 };
 
+// W_L^{+k} = T_hi[k >> lb] * T_lo[k & (2^lb - 1)] for k < L/2: two short
+// tables instead of one sincospi per element.
+__global__ void poly_twiddle_tables(double2 *lo, int n_lo, double2 *hi, int n_hi, int lb,
+                                    int log_len) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j < n_lo) lo[j] = twiddle<+1>((long long)j, log_len, 0.0);
+  if (j < n_hi) hi[j] = twiddle<+1>((long long)j << lb, log_len, 0.0);
+}
+
+__global__ void poly_combine(const double2 *__restrict__ Z, double2 *__restrict__ Y,
+                             const double2 *__restrict__ tw_lo, const double2 *__restrict__ tw_hi,
+                             int lb, int log_len, long long batch) {
+  const long long L = 1LL << log_len, H = L >> 1;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= batch * H) return;
+  const long long p = idx / H, k = idx % H;
+  const double2 *z = Z + p * L;
+  const double2 zk = z[k], zmk = z[(L - k) & (L - 1)];
+  const double2 zh = z[k + H], zmh = z[H - k];
+  // A B = (u + conj w)(u - conj w) / (2i) / 2 = (u^2 - conj(w)^2) (-i/4) with
+  // u = Z_k, w = Z_{L-k}; returned halved (C/2), the factor E and O need.
+  auto half_product = [](double2 u, double2 w) {
+    const double re = u.x * u.y + w.x * w.y;                    // Im(u^2 - conj(w)^2) / 2
+    const double im = (u.x * u.x - u.y * u.y) - (w.x * w.x - w.y * w.y);  // Re(...)
+    return make_c<double2>(0.25 * re, -0.125 * im);
+  };
+  const double2 Ck = half_product(zk, zmk), Ch = half_product(zh, zmh);  // C/2
+  const double2 w = c_mul(tw_hi[k >> lb], tw_lo[k & ((1LL << lb) - 1)]);  // W_L^{-k}
+  const double2 O = c_mul(c_sub(Ck, Ch), w);                               // O_k
+  Y[p * H + k] = make_c<double2>(Ck.x + Ch.x - O.y, Ck.y + Ch.y + O.x);    // E_k + i O_k
+}
+
+// Inter-pass twiddle tables W_{2^log_lm}^e (direction dir) for e < 2^log_lm.
+__global__ void poly_pass_tables(double2 *lo, int lo_bits, double2 *hi, int log_lm, int dir) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  const int n_lo = 1 << lo_bits, n_hi = 1 << (log_lm - lo_bits);
+  if (dir < 0) {
+    if (j < n_lo) lo[j] = twiddle<-1>((long long)j, log_lm, 0.0);
+    if (j < n_hi) hi[j] = twiddle<-1>((long long)j << lo_bits, log_lm, 0.0);
+  } else {
+    if (j < n_lo) lo[j] = twiddle<+1>((long long)j, log_lm, 0.0);
+    if (j < n_hi) hi[j] = twiddle<+1>((long long)j << lo_bits, log_lm, 0.0);
+  }
+}
+
 // Largest on-chip factor used per pass for the fp64 polynomial transforms.
-constexpr int kPolyPassLog = 9;
+constexpr int kPolyPassLog = 11;
 
 template <int DIR, class Load, class Store, int LOGL = 1>
 cudaError_t poly_pass(int log_l, Load load, Store store, int log_n, int log_m, long long batch,
-                      cudaStream_t st) {
+                      cudaStream_t st, TwiddleTables<double2> tt) {
   if constexpr (LOGL > kPolyPassLog) {
     return cudaErrorInvalidValue;
   } else {
     if (log_l == LOGL)
       return launch_pass_t<double, LOGL, DIR>(load, store, log_n, log_m, /*twiddle=*/1, batch,
-                                              st);
-    return poly_pass<DIR, Load, Store, LOGL + 1>(log_l, load, store, log_n, log_m, batch, st);
+                                              st, nullptr, tt);
+    return poly_pass<DIR, Load, Store, LOGL + 1>(log_l, load, store, log_n, log_m, batch, st,
+                                                 tt);
   }
+}
+
+// Split log_len into nearly equal factors of at most kPolyPassLog bits.
+static int split_passes(int log_len, int *logs) {
+  int P = (log_len + kPolyPassLog - 1) / kPolyPassLog;
+  if (P < 1) P = 1;
+  for (int k = 0; k < P; ++k) logs[k] = log_len / P + (k < log_len % P ? 1 : 0);
+  return P;
+}
+
+// Two buffers of batch * L complex doubles plus the twiddle tables: two
+// two-level tables of the inter-pass twiddles (forward, length L; inverse,
+// length L/2) and one of W_L^{-k} for the combine step -- six tables of at
+// most 2^ceil(log_len/2) entries each.
+static long long table_stride(int log_len) { return 1LL << ((log_len + 1) / 2); }
+
+size_t polymul_scratch_bytes(long long batch, int log_len) {
+  const size_t L = (size_t)1 << log_len;
+  return (2 * (size_t)batch * L + 6 * (size_t)table_stride(log_len)) * sizeof(double2);
 }
 
 cudaError_t launch_polymul(const long long *a, long long na, const long long *b, long long nb,
                            long long *c, long long batch, int log_len, void *scratch,
                            cudaStream_t st) {
-  const long long L = 1LL << log_len;
+  if (log_len < 2 || log_len > 27) return cudaErrorInvalidValue;
+  const long long L = 1LL << log_len, H = L >> 1;
   const long long nc = na + nb - 1;
-  double2 *S[3];
-  for (int k = 0; k < 3; ++k) S[k] = static_cast<double2 *>(scratch) + (long long)k * batch * L;
-
-  // Split log_len into P nearly equal factors of at most kPolyPassLog bits.
-  int P = (log_len + kPolyPassLog - 1) / kPolyPassLog;
-  if (P < 1) P = 1;
-  int logs[8];
-  for (int k = 0; k < P; ++k) logs[k] = log_len / P + (k < log_len % P ? 1 : 0);
+  double2 *R[2] = {static_cast<double2 *>(scratch),
+                   static_cast<double2 *>(scratch) + batch * L};
+  double2 *tables = R[1] + batch * L;
+  const long long ts = table_stride(log_len);
+  double2 *tw_lo = tables, *tw_hi = tables + ts;                 // combine
+  double2 *f_lo = tables + 2 * ts, *f_hi = tables + 3 * ts;      // forward passes
+  double2 *i_lo = tables + 4 * ts, *i_hi = tables + 5 * ts;      // inverse passes
+  const int lb = log_len / 2;  // k < L/2 splits into lb low bits and log_len-1-lb high bits
+  const int n_lo = 1 << lb, n_hi = 1 << (log_len - 1 - lb);
+  const int f_bits = (log_len + 1) / 2, i_bits = log_len / 2;
 
   using LC = LoadComplex<double2>;
   using SC = StoreComplex<double2>;
-  cudaError_t e = cudaSuccess;
+  cudaError_t e;
 
-  // Plain complex -> complex passes use the library's fp64 pass kernels.
-  auto plain = [&](int dir, int log_l, const double2 *in, double2 *out, int log_m) {
-    PassArgs pa{log_len, log_l, log_m, 1, batch};
-    return launch_pass_f64(dir, pa, in, out, st);
-  };
+  // Twiddle tables (a few thousand sincospi in all).
+  {
+    const int blocks = (int)(ts / 256) + 1;
+    poly_twiddle_tables<<<blocks, 256, 0, st>>>(tw_lo, n_lo, tw_hi, n_hi, lb, log_len);
+    poly_pass_tables<<<blocks, 256, 0, st>>>(f_lo, f_bits, f_hi, log_len, -1);
+    poly_pass_tables<<<blocks, 256, 0, st>>>(i_lo, i_bits, i_hi, log_len - 1, +1);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const TwiddleTables<double2> ftt{f_lo, f_hi, f_bits, log_len},
+      itt{i_lo, i_hi, i_bits, log_len - 1};
 
-  // Forward transform of one int64 operand.  Pass k writes S[k % 2] except
-  // the last, which goes through `last_store`.
-  auto forward = [&](const long long *src, long long nsrc, auto last_store) -> cudaError_t {
-    int log_m = 0;
-    const double2 *prev = nullptr;
-    for (int k = 0; k < P; ++k) {
-      const bool first = k == 0, final_pass = k == P - 1;
-      cudaError_t r;
-      if (first && final_pass)
-        r = poly_pass<-1>(logs[k], LoadInt64Pad{src, nsrc}, last_store, log_len, log_m, batch, st);
-      else if (first)
-        r = poly_pass<-1>(logs[k], LoadInt64Pad{src, nsrc}, SC{S[k % 2], L}, log_len, log_m,
-                          batch, st);
-      else if (final_pass)
-        r = poly_pass<-1>(logs[k], LC{prev, L}, last_store, log_len, log_m, batch, st);
-      else
-        r = plain(-1, logs[k], prev, S[k % 2], log_m);
-      if (r != cudaSuccess) return r;
-      prev = S[k % 2];
-      log_m += logs[k];
-    }
-    return cudaSuccess;
-  };
-
-  // A = FFT(a) into S[2].
-  e = forward(a, na, SC{S[2], L});
-  if (e != cudaSuccess) return e;
-  // B = FFT(b) * A into S[(P-1) % 2].
-  double2 *Bbuf = S[(P - 1) % 2];
-  e = forward(b, nb, StoreMulComplex{Bbuf, S[2], L});
-  if (e != cudaSuccess) return e;
-
-  // c = round(IFFT(B)); intermediates alternate over the two other buffers.
+  // 1. Z = FFT_L(a + i b): pass k writes R[k % 2].
+  int logs[8];
+  const int P = split_passes(log_len, logs);
   int log_m = 0;
-  const double2 *prev = Bbuf;
-  double2 *other[2] = {S[P % 2], S[2]};
   for (int k = 0; k < P; ++k) {
-    const bool final_pass = k == P - 1;
-    cudaError_t r;
-    if (final_pass)
-      r = poly_pass<+1>(logs[k], LC{prev, L}, StoreRoundInt64{c, nc}, log_len, log_m, batch, st);
+    SC dst{R[k % 2], L};
+    if (k == 0)
+      e = poly_pass<-1>(logs[k], LoadPairInt64{a, b, na, nb}, dst, log_len, log_m, batch, st,
+                        ftt);
     else
-      r = plain(+1, logs[k], prev, other[k % 2], log_m);
-    if (r != cudaSuccess) return r;
-    if (!final_pass) prev = other[k % 2];
+      e = poly_pass<-1>(logs[k], LC{R[(k - 1) % 2], L}, dst, log_len, log_m, batch, st, ftt);
+    if (e != cudaSuccess) return e;
     log_m += logs[k];
   }
+  double2 *Z = R[(P - 1) % 2];
+  double2 *Y = R[P % 2];
+
+  // 2. Y_k from Z (point-value product, then the even/odd packing).
+  {
+    const long long total = batch * H;
+    poly_combine<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(Z, Y, tw_lo, tw_hi, lb,
+                                                                  log_len, batch);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+
+  // 3. y = IFFT_{L/2}(Y), the last pass rounds into c.  Intermediates
+  // alternate between Z's buffer and Y's.
+  int ilogs[8];
+  const int IP = split_passes(log_len - 1, ilogs);
+  const double2 *src = Y;
+  double2 *bufs[2] = {Z, Y};
+  log_m = 0;
+  for (int k = 0; k < IP; ++k) {
+    if (k == IP - 1) {
+      e = poly_pass<+1>(ilogs[k], LC{src, H}, StoreRoundPairsInt64{c, nc}, log_len - 1, log_m,
+                        batch, st, itt);
+    } else {
+      double2 *dst = bufs[k % 2];
+      e = poly_pass<+1>(ilogs[k], LC{src, H}, SC{dst, H}, log_len - 1, log_m, batch, st, itt);
+      src = dst;
+    }
+    if (e != cudaSuccess) return e;
+    log_m += ilogs[k];
+  }
   return cudaSuccess;
+}
+
+int polymul_num_kernels(int log_len) {
+  int logs[8];
+  return 3 + 1 + split_passes(log_len, logs) + split_passes(log_len - 1, logs);
 }
 
 }  // namespace fftgb

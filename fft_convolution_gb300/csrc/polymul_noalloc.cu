@@ -30,9 +30,10 @@ namespace {
 
 constexpr long long kMaxLen = FFT_POLYMUL_NOALLOC_MAX_LEN;  // largest transform length L
 
-// Three fp64 complex buffers of kMaxLen elements (3 MiB).  In host code this
-// name is only a stand-in for the device array: its device address comes
-// from cudaGetSymbolAddress below, once per device.
+// 3 MiB of fp64 complex scratch: room for the transforms of one product of
+// length up to kMaxLen.  In host code this name is only a stand-in for the
+// device array: its device address comes from cudaGetSymbolAddress below,
+// once per device.
 static __device__ __align__(256) double2 g_noalloc_scratch[3 * kMaxLen];
 
 constexpr int kMaxDevices = 64;
@@ -53,8 +54,10 @@ extern "C" int polymul_noalloc(const int64_t *a, int64_t na, const int64_t *b, i
   if (((uintptr_t)a & 7u) || ((uintptr_t)b & 7u) || ((uintptr_t)c & 7u))
     return FFT_ERR_MISALIGNED;
   const long long nc = (long long)na + (long long)nb - 1;
-  const int log_len = nc > 1 ? ilog2_ceil(nc) : 1;
-  if ((1LL << log_len) > kMaxLen) return FFT_ERR_UNSUPPORTED;  // beyond the fixed scratch
+  const int log_len = nc > 4 ? ilog2_ceil(nc) : 2;
+  if ((1LL << log_len) > kMaxLen ||
+      fftgb::polymul_scratch_bytes(1, log_len) > sizeof(g_noalloc_scratch))
+    return FFT_ERR_UNSUPPORTED;  // beyond the fixed scratch
 
   // Set-up, once per device, with that device current: the device address
   // of the scratch array.

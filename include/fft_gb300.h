@@ -127,14 +127,21 @@ int fft_exec_host(const fft_plan *plan, const void *host_in, void *host_out, voi
  * to the nearest integer.  The result is exact while every |c_k| and the
  * transform's rounding error stay well below 2^52 and 0.5 respectively
  * (e.g. coefficients in [0, 9] with na, nb <= 2^20 give |c_k| < 2^27 and an
- * error of order 1e-7).  L <= 2^27.  Scratch (3 * L * 16 bytes) is
+ * error of order 1e-7).  L <= 2^27.  Both inputs ride in one complex
+ * transform (a + i b) and the real product comes back through one of length
+ * L/2.  Scratch (2 * L * 16 bytes plus 256 KiB of twiddle tables) is
  * allocated with cudaMallocAsync on `stream` and freed the same way.
  */
 int polymul(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, int64_t *c,
             void *stream);
 
+/* Number of kernels one polymul / polymul_batched / polymul_noalloc call
+ * with these lengths launches (0 if the lengths are invalid). */
+int polymul_num_kernels(int64_t na, int64_t nb);
+
 /* polymul over `batch` independent pairs: pair p uses a + p*na, b + p*nb
- * and writes c + p*(na+nb-1).  Scratch is 3 * batch * L * 16 bytes. */
+ * and writes c + p*(na+nb-1).  Scratch is 2 * batch * L * 16 bytes plus
+ * 256 KiB. */
 int polymul_batched(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, int64_t *c,
                     int64_t batch, void *stream);
 

@@ -230,6 +230,28 @@ def test_polymul_exact(fg, na, nb, batch):
             assert np.array_equal(c[p], oracle.polymul_fft(a[p], b[p]))
 
 
+def test_polymul_three_pass_forward(fg):
+    # L = 2^23: the forward transform takes three passes (the inter-pass
+    # twiddle tables serve a pass with L m < L), the inverse two.
+    na = nb = 1 << 22
+    g = workloads.generator(23)
+    a = g.integers(0, 10, size=na, dtype=np.int64)
+    b = g.integers(0, 10, size=nb, dtype=np.int64)
+    c = fg.polymul_tensors(torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda())
+    torch.cuda.synchronize()
+    c = c.cpu().numpy()
+    idx = workloads.sample_indices(48, na + nb - 1, 24)
+    assert np.array_equal(c[idx], oracle.polymul_schoolbook_at(a, b, idx))
+    for t in (3, 123456789):
+        assert oracle.poly_eval_mod(c, t) == \
+            oracle.poly_eval_mod(a, t) * oracle.poly_eval_mod(b, t) % oracle.MOD_P
+
+
+def test_polymul_kernel_count(fg):
+    assert fg.polymul_num_kernels(1 << 20, 1 << 20) == 8   # 3 tables, 2 + 2 passes, combine
+    assert fg.polymul_num_kernels(0, 5) == 0
+
+
 def test_polymul_signed_coefficients(fg):
     g = workloads.generator(5)
     a = g.integers(-1000, 1001, size=3000, dtype=np.int64)
