@@ -41,6 +41,7 @@ SIGNATURES = {
     "fft_plan_num_kernels": (_INT, [_VP]),
     "fft_exec": (_INT, [_VP, _VP, _VP, _VP]),
     "fft_exec_host": (_INT, [_VP, _VP, _VP, _VP, _VP, _VP]),
+    "fft_exec_host_chain": (_INT, [_VP, _INT, _VP, _VP, _VP, _VP, _I64, _VP]),
     "polymul": (_INT, [_VP, _I64, _VP, _I64, _VP, _VP]),
     "polymul_batched": (_INT, [_VP, _I64, _VP, _I64, _VP, _I64, _VP]),
     "polymul_noalloc": (_INT, [_VP, _I64, _VP, _I64, _VP, _VP]),
@@ -112,6 +113,13 @@ def fft_exec(plan: int, in_ptr: int, out_ptr: int, stream: int) -> int:
 def fft_exec_host(plan: int, host_in: int, host_out: int, dev_in: int, dev_out: int,
                   stream: int) -> int:
     return _lib.fft_exec_host(plan, host_in, host_out, dev_in, dev_out, stream)
+
+
+def fft_exec_host_chain(plans, nplans: int, host_in: int, host_out: int, dev_a: int, dev_b: int,
+                        chunk: int, stream: int) -> int:
+    """plans: a sequence of plan handles (marshalled to a C array)."""
+    arr = (ctypes.c_void_p * len(plans))(*plans)
+    return _lib.fft_exec_host_chain(arr, nplans, host_in, host_out, dev_a, dev_b, chunk, stream)
 
 
 def polymul(a_ptr: int, na: int, b_ptr: int, nb: int, c_ptr: int, stream: int) -> int:
@@ -221,6 +229,13 @@ class Plan:
         hout = host_out.data_ptr() if host_out is not None else None
         _check(fft_exec_host(self.handle, hin, hout, dev_in.data_ptr(), dev_out.data_ptr(),
                              _stream_handle(stream)), "fft_exec_host")
+
+    def chain_host(self, others, host_in, host_out, dev_a, dev_b, chunk: int, stream=None):
+        """fft_exec_host_chain over [self] + others on host tensors."""
+        plans = [self.handle] + [o.handle for o in others]
+        _check(fft_exec_host_chain(plans, len(plans), host_in.data_ptr(), host_out.data_ptr(),
+                                   dev_a.data_ptr(), dev_b.data_ptr(), chunk,
+                                   _stream_handle(stream)), "fft_exec_host_chain")
 
     def close(self):
         if getattr(self, "handle", None):

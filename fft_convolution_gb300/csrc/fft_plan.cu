@@ -12,6 +12,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
 #include <new>
 
 #include "../../include/fft_gb300.h"
@@ -209,6 +210,8 @@ struct Schedule {
   const fft_plan *p;
   cudaStream_t st;
   bool dry;
+  long long batch;  // transforms this run covers (a range of the plan's batch)
+  char *ws;         // the workspace slice of that range
   int count = 0;
 
   size_t elem() const { return p->dtype == FFT_C2C_F32 ? 8 : 16; }
@@ -232,10 +235,10 @@ struct Schedule {
     const long long n = p->n;
     const size_t img = (size_t)n * (size_t)n * elem();
     const size_t budget = l2_group_bytes();
-    long long g = budget ? (long long)(budget / img) : p->batch;
+    long long g = budget ? (long long)(budget / img) : batch;
     if (g < 1) g = 1;
-    for (long long b0 = 0; b0 < p->batch; b0 += g) {
-      const long long nb = p->batch - b0 < g ? p->batch - b0 : g;
+    for (long long b0 = 0; b0 < batch; b0 += g) {
+      const long long nb = batch - b0 < g ? batch - b0 : g;
       const size_t off = (size_t)b0 * img;
       cudaError_t e = rows(in + off, out + off, nb * n);
       if (e != cudaSuccess || p->logn == 0) {  // 1 x 1: rows already did it
@@ -296,16 +299,15 @@ struct Schedule {
   }
 
   cudaError_t run_multi(const char *in, char *out) {
-    char *ws = static_cast<char *>(p->workspace);
     const size_t tbytes = (size_t)p->n * elem();
     const size_t budget = l2_group_bytes();
-    if (budget == 0) return run_passes(in, out, ws, p->batch, 0);
+    if (budget == 0) return run_passes(in, out, ws, batch, 0);
     if (tbytes <= budget) {
       // Whole transforms fit in L2: all passes of one group, then the next.
       long long g = (long long)(budget / tbytes);
       if (g < 1) g = 1;
-      for (long long b0 = 0; b0 < p->batch; b0 += g) {
-        const long long nb = p->batch - b0 < g ? p->batch - b0 : g;
+      for (long long b0 = 0; b0 < batch; b0 += g) {
+        const long long nb = batch - b0 < g ? batch - b0 : g;
         const size_t off = (size_t)b0 * tbytes;
         cudaError_t e = run_passes(in + off, out + off, ws + off, nb, 0);
         if (e != cudaSuccess) return e;
@@ -317,15 +319,15 @@ struct Schedule {
     // left to run after them.
     if (in != out && p->npasses >= 3) {
       bool fused = true;
-      for (long long b = 0; b < p->batch && fused; ++b) {
+      for (long long b = 0; b < batch && fused; ++b) {
         const size_t off = (size_t)b * tbytes;
         cudaError_t e = cudaSuccess;
         fused = fused_01(in + off, out + off, ws + off, &e);
         if (e != cudaSuccess) return e;
       }
-      if (fused) return run_passes(in, out, ws, p->batch, 2);
+      if (fused) return run_passes(in, out, ws, batch, 2);
     }
-    return run_passes(in, out, ws, p->batch, 0);
+    return run_passes(in, out, ws, batch, 0);
   }
 
   cudaError_t run(const void *in, void *out) {
@@ -333,7 +335,7 @@ struct Schedule {
     char *o = static_cast<char *>(out);
     switch (p->kind) {
       case KIND_ROWS:
-        return rows(in, out, p->batch);
+        return rows(in, out, batch);
       case KIND_2D:
         return run_2d(i, o);
       case KIND_MULTI:
@@ -351,7 +353,7 @@ extern "C" {
 int fft_plan_num_kernels(const fft_plan *plan) {
   if (!plan) return 0;
   // Count an out-of-place execution (distinct dummy addresses).
-  Schedule s{plan, nullptr, true};
+  Schedule s{plan, nullptr, true, plan->batch, static_cast<char *>(plan->workspace)};
   s.run(reinterpret_cast<const void *>(16), reinterpret_cast<void *>(32));
   return s.count;
 }
@@ -359,7 +361,8 @@ int fft_plan_num_kernels(const fft_plan *plan) {
 int fft_exec(const fft_plan *p, const void *in, void *out, void *stream) {
   if (!p || !in || !out) return FFT_ERR_INVALID_ARG;
   if (misaligned(in) || misaligned(out)) return FFT_ERR_MISALIGNED;
-  Schedule s{p, static_cast<cudaStream_t>(stream), false};
+  Schedule s{p, static_cast<cudaStream_t>(stream), false, p->batch,
+             static_cast<char *>(p->workspace)};
   cudaError_t e = s.run(in, out);
   if (e != cudaSuccess) return cuda_fail(e);
   return FFT_OK;
@@ -384,6 +387,133 @@ int fft_exec_host(const fft_plan *p, const void *host_in, void *host_out, void *
     e = cudaMemcpyAsync(host_out, dev_out, bytes, cudaMemcpyDeviceToHost, st);
     if (e != cudaSuccess) return cuda_fail(e);
   }
+  return FFT_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Streams and events of the host-staged pipeline, created once per device.
+struct HostPipe {
+  cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
+  cudaEvent_t fork = nullptr, join_comp = nullptr, join_out = nullptr;
+  cudaEvent_t *loaded = nullptr, *done = nullptr;  // per chunk
+  int nev = 0;
+};
+std::mutex g_pipe_mutex;
+HostPipe g_pipes[64];
+
+cudaError_t pipe_for_device(int chunks, HostPipe **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  HostPipe &hp = g_pipes[dev];
+  if (!hp.in) {
+    const unsigned f = cudaStreamNonBlocking;
+    if ((e = cudaStreamCreateWithFlags(&hp.in, f)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&hp.comp, f)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&hp.out, f)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.fork, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.join_comp, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.join_out, cudaEventDisableTiming)) != cudaSuccess)
+      return e;
+  }
+  if (hp.nev < chunks) {
+    cudaEvent_t *l = new (std::nothrow) cudaEvent_t[chunks];
+    cudaEvent_t *d = new (std::nothrow) cudaEvent_t[chunks];
+    if (!l || !d) {
+      delete[] l;
+      delete[] d;
+      return cudaErrorMemoryAllocation;
+    }
+    for (int k = 0; k < hp.nev; ++k) {
+      l[k] = hp.loaded[k];
+      d[k] = hp.done[k];
+    }
+    for (int k = hp.nev; k < chunks; ++k) {
+      if ((e = cudaEventCreateWithFlags(&l[k], cudaEventDisableTiming)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&d[k], cudaEventDisableTiming)) != cudaSuccess) {
+        delete[] l;
+        delete[] d;
+        return e;
+      }
+    }
+    delete[] hp.loaded;
+    delete[] hp.done;
+    hp.loaded = l;
+    hp.done = d;
+    hp.nev = chunks;
+  }
+  *out = &hp;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fft_exec_host_chain(const fft_plan *const *plans, int nplans, const void *host_in,
+                        void *host_out, void *dev_a, void *dev_b, int64_t chunk, void *stream) {
+  if (!plans || nplans <= 0 || !host_in || !host_out || !dev_a || !dev_b || chunk <= 0)
+    return FFT_ERR_INVALID_ARG;
+  const fft_plan *p0 = plans[0];
+  for (int k = 0; k < nplans; ++k) {
+    const fft_plan *q = plans[k];
+    if (!q || q->n != p0->n || q->dims != p0->dims || q->dtype != p0->dtype ||
+        q->batch != p0->batch)
+      return FFT_ERR_INVALID_ARG;
+  }
+  if (misaligned(dev_a) || misaligned(dev_b)) return FFT_ERR_MISALIGNED;
+  const long long batch = p0->batch;
+  if (chunk > batch) chunk = batch;
+  const long long nchunks = (batch + chunk - 1) / chunk;
+  if (nchunks > 4096) return FFT_ERR_INVALID_ARG;
+  const size_t elem = p0->dtype == FFT_C2C_F32 ? 8 : 16;
+  const size_t tbytes = (size_t)p0->n * (p0->dims == 2 ? (size_t)p0->n : 1) * elem;
+
+  std::lock_guard<std::mutex> lock(g_pipe_mutex);
+  HostPipe *hp = nullptr;
+  cudaError_t e = pipe_for_device((int)nchunks, &hp);
+  if (e != cudaSuccess) return cuda_fail(e);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  // Fork: the three pipeline streams start after the work already on `stream`.
+  if ((e = cudaEventRecord(hp->fork, st)) != cudaSuccess) return cuda_fail(e);
+  cudaStreamWaitEvent(hp->in, hp->fork, 0);
+  cudaStreamWaitEvent(hp->comp, hp->fork, 0);
+  cudaStreamWaitEvent(hp->out, hp->fork, 0);
+
+  char *bufs[2] = {static_cast<char *>(dev_a), static_cast<char *>(dev_b)};
+  for (long long k = 0; k < nchunks; ++k) {
+    const long long b0 = k * chunk;
+    const long long cnt = batch - b0 < chunk ? batch - b0 : chunk;
+    const size_t off = (size_t)b0 * tbytes, bytes = (size_t)cnt * tbytes;
+    e = cudaMemcpyAsync(bufs[0] + off, static_cast<const char *>(host_in) + off, bytes,
+                        cudaMemcpyHostToDevice, hp->in);
+    if (e != cudaSuccess) return cuda_fail(e);
+    cudaEventRecord(hp->loaded[k], hp->in);
+    cudaStreamWaitEvent(hp->comp, hp->loaded[k], 0);
+    for (int j = 0; j < nplans; ++j) {
+      const fft_plan *q = plans[j];
+      char *ws = q->workspace ? static_cast<char *>(q->workspace) + off : nullptr;
+      Schedule s{q, hp->comp, false, cnt, ws};
+      e = s.run(bufs[j % 2] + off, bufs[(j + 1) % 2] + off);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    cudaEventRecord(hp->done[k], hp->comp);
+    cudaStreamWaitEvent(hp->out, hp->done[k], 0);
+    e = cudaMemcpyAsync(static_cast<char *>(host_out) + off, bufs[nplans % 2] + off, bytes,
+                        cudaMemcpyDeviceToHost, hp->out);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  // Join: `stream` continues after the last download.
+  cudaEventRecord(hp->join_comp, hp->comp);
+  cudaEventRecord(hp->join_out, hp->out);
+  cudaStreamWaitEvent(st, hp->join_comp, 0);
+  e = cudaStreamWaitEvent(st, hp->join_out, 0);
+  if (e != cudaSuccess) return cuda_fail(e);
   return FFT_OK;
 }
 

@@ -119,6 +119,28 @@ int fft_exec_host(const fft_plan *plan, const void *host_in, void *host_out, voi
                   void *dev_out, void *stream);
 
 /*
+ * fft_exec_host_chain -- run plans[0], plans[1], ... plans[nplans-1] one
+ * after the other on host data, streaming it through the device in chunks
+ * of `chunk` transforms so that uploads, transforms and downloads of
+ * different chunks overlap.  For each chunk: copy host_in -> dev_a, run
+ * plans[0] dev_a -> dev_b, plans[1] dev_b -> dev_a, ..., copy the last
+ * result (dev_a if nplans is even, dev_b if odd) -> host_out.
+ *   plans     nplans >= 1 plans with the same n, dims, dtype and batch.
+ *   host_in, host_out  host buffers of the full batch (pinned for the copies
+ *             to overlap); host_in is only read.
+ *   dev_a, dev_b       caller-owned device buffers of the full batch,
+ *             16-byte aligned; both are overwritten.
+ *   chunk     transforms per chunk (>= 1; at most 4096 chunks).
+ * Ordered after the work already on `stream`; `stream` waits for the last
+ * download, so the call is asynchronous on `stream` like fft_exec.  Uses
+ * three internal non-blocking streams and per-chunk events, created on the
+ * first call on a device (calls on one device are serialised by a lock
+ * while they enqueue).  Allocates no device memory.
+ */
+int fft_exec_host_chain(const fft_plan *const *plans, int nplans, const void *host_in,
+                        void *host_out, void *dev_a, void *dev_b, int64_t chunk, void *stream);
+
+/*
  * polymul -- c = a * b for integer coefficient vectors (device pointers,
  * int64, 8-byte aligned): a has na >= 1 coefficients, b has nb >= 1,
  * c receives na + nb - 1.  The product is formed with fp64 transforms of
