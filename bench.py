@@ -158,14 +158,26 @@ class ClockSampler:
 # Committed ncu traffic summary (null once the kernels have changed)
 # ---------------------------------------------------------------------------
 
-def kernel_source_hash() -> str:
+# Sources of the kernels each workload's roofline entry measures.
+KERNEL_SOURCES = {
+    "c1": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_f32.cu"],
+    "c2": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_f32.cu"],
+    "c3": ["fft_device.cuh", "fft_pass.cuh", "fft_pass_tma.cuh", "fft_pass_f32.cu",
+           "fft_plan.cu"],
+    "c4": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_f32.cu", "fft_pass.cuh",
+           "fft_pass_tma.cuh", "fft_pass_f32.cu", "fft_plan.cu"],
+    "c5": ["fft_device.cuh", "fft_pass.cuh", "fft_pass_tma.cuh", "fft_pass_f64.cu",
+           "polymul.cu"],
+}
+
+
+def kernel_source_hash(config: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fft_convolution_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode())
-                h.update(f.read())
+    for fn in sorted(KERNEL_SOURCES[config]):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -177,7 +189,7 @@ def committed_traffic(config: str):
     except (OSError, ValueError):
         return None
     ent = data.get(config)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or ent.get("source_hash") != kernel_source_hash(config):
         return None
     return ent
 
