@@ -348,14 +348,24 @@ def run_gpu(args):
         step()
     torch.cuda.synchronize(dev)
 
-    # Timed region.
+    # Clock sampling: nvidia-smi samples every 100 ms, longer than most timed
+    # regions here, so the sampler runs over an untimed soak of the same
+    # steps (>= args.clock_soak seconds of load) that leads straight into
+    # the timed region; the clocks reported are those of the GPU under this
+    # load.
     nev = 3
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
     clocks = ClockSampler(local)
+    clocks.start()
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.clock_soak:
+        for _ in range(4):
+            step()
+        torch.cuda.synchronize(dev)
+
+    # Timed region.
     barrier()
     torch.cuda.synchronize(dev)
-    clocks.start()
-    time.sleep(0.3)  # let the sampler start before the work
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -475,6 +485,7 @@ def run_gpu(args):
         "roofline": roofline,
         "e2e": e2e,
         "clocks": clk,
+        "clock_soak_s": args.clock_soak,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_sample(name)
@@ -569,6 +580,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
+    ap.add_argument("--clock-soak", type=float, default=0.6,
+                    help="seconds of untimed load sampled for clocks before the timed region")
     ap.add_argument("--n", type=int, default=None,
                     help="override the transform length (small profiling cases)")
     ap.add_argument("--batch", type=int, default=None,
