@@ -272,6 +272,24 @@ def cpu_oracle_sample(name: str, budget_s: float = 12.0):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The maximum of `value` over all ranks (the job's time is its slowest
+    rank's); the identity when world == 1."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(bytes_per_step: float, world: int, ms_step: float) -> float:
+    """Weak scaling: every rank moves bytes_per_step per step; the job's GB/s
+    is all ranks' bytes over the slowest rank's step time."""
+    return bytes_per_step * world / (ms_step * 1e-3) / 1e9
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -375,13 +393,8 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     barrier()
     clk = clocks.stop()
-    ms_total = t_start.elapsed_time(t_end)
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     ms_step = ms_total / args.steps
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
-        ms_step = ms_total / args.steps
 
     # Per-launch durations of the dominant kernel (the forward transform;
     # for 1-kernel plans that is one launch per exec).
@@ -442,7 +455,7 @@ def run_gpu(args):
                "ms_per_step": round(e2e_ms, 4)}
 
     peak, peak_kind = measured_peaks()
-    value = info["bytes_per_step"] * world / (ms_step * 1e-3) / 1e9
+    value = whole_job_value(info["bytes_per_step"], world, ms_step)
 
     if info["kind"] == "polymul":
         dom_ms = statistics.mean(fwd_ms)

@@ -48,6 +48,7 @@ SIGNATURES = {
     "polymul_num_kernels": (_INT, [_I64, _I64]),
     "fft_debug_radix2_pass": (_INT, [_VP, _VP, _I64, _I64, _INT, _VP]),
     "fft_device_status": (_INT, [_VP]),
+    "fft_debug_wait_timeout": (_INT, [_I64, _VP]),
     "fft_last_status": (_INT, []),
     "fft_status_string": (ctypes.c_char_p, [_INT]),
     "fft_last_cuda_error": (ctypes.c_char_p, []),
@@ -147,6 +148,10 @@ def polymul_num_kernels(na: int, nb: int) -> int:
 def fft_debug_radix2_pass(in_ptr: int, out_ptr: int, n: int, half: int, dtype: int,
                           stream: int) -> int:
     return _lib.fft_debug_radix2_pass(in_ptr, out_ptr, n, half, dtype, stream)
+
+
+def fft_debug_wait_timeout(polls: int, stream: int) -> int:
+    return int(_lib.fft_debug_wait_timeout(polls, stream))
 
 
 def fft_device_status(stream: int) -> int:

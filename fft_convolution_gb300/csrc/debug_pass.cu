@@ -7,8 +7,7 @@
 // b = in[base + half], w = e^{-i pi r / half}; the cell receives a + w b
 // (lower) or a - w b (upper).  Nothing is swapped and no thread writes two
 // cells.
-#include "fft_device.cuh"
-#include "internal.h"
+#include "fft_pass_tma.cuh"
 
 namespace fftgb {
 
@@ -28,6 +27,31 @@ __global__ void radix2_pass_kernel(const vec2_t<T> *in, vec2_t<T> *out, long lon
   else sincospi((double)r / (double)half, &s, &c);
   const V wb = c_mul(make_c<V>(c, -s), b);  // e^{-i pi r/half} * b
   out[i] = (j == 0) ? c_add(a, wb) : c_sub(a, wb);
+}
+
+// Test hook for the bounded waits: one block arms an mbarrier with a
+// 16-byte transaction that nothing delivers, polls it `polls` times and,
+// when the wait runs out, records kDeviceErrorTimeout in the device status
+// word -- the same path the TMA pass kernel takes.  No copy is issued, so
+// nothing is left in flight when the block exits.
+__global__ void wait_timeout_kernel(long long polls, int *status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_expect_tx(&bar, 16);
+  }
+  __syncthreads();
+  bool ok = false;
+  for (long long it = 0; it < polls && !ok; ++it) ok = mbar_try_wait(&bar, 0);
+  if (__syncthreads_or(!ok) && threadIdx.x == 0) atomicExch(status, kDeviceErrorTimeout);
+}
+
+cudaError_t launch_wait_timeout(long long polls, cudaStream_t st) {
+  int *status = device_status_word();
+  if (!status) return cudaErrorInvalidDevice;
+  wait_timeout_kernel<<<1, 32, 0, st>>>(polls, status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_radix2_pass(int dtype, const void *in, void *out, long long n, long long half,

@@ -564,6 +564,13 @@ int fft_debug_radix2_pass(const void *in, void *out, int64_t n, int64_t half, in
   return FFT_OK;
 }
 
+int fft_debug_wait_timeout(int64_t polls, void *stream) {
+  if (polls <= 0 || polls > ((int64_t)1 << 22)) return FFT_ERR_INVALID_ARG;
+  cudaError_t e = launch_wait_timeout(polls, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FFT_OK;
+}
+
 int fft_device_status(void *stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(st);

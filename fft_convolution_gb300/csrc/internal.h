@@ -61,6 +61,9 @@ constexpr int kPassMaxLogF64 = 13;
 // (fft_plan.cu; fft_device_status reads and clears it).
 int *device_status_word();
 
+// Bounded-wait test hook (debug_pass.cu).
+cudaError_t launch_wait_timeout(long long polls, cudaStream_t st);
+
 // One radix-2 butterfly pass (debug_pass.cu).
 cudaError_t launch_radix2_pass(int dtype, const void *in, void *out, long long n, long long half,
                                cudaStream_t st);

@@ -214,6 +214,16 @@ int fft_debug_radix2_pass(const void *in, void *out, int64_t n, int64_t half, in
  */
 int fft_device_status(void *stream);
 
+/*
+ * fft_debug_wait_timeout -- test hook (not part of the transform API): one
+ * block waits on an mbarrier transaction that never arrives, `polls` times
+ * (1 .. 2^22), and records the timeout in the device status word exactly as
+ * the TMA pass kernel does; fft_device_status then reports
+ * FFT_ERR_DEVICE_TIMEOUT.  Issues no copy and faults nothing.  No
+ * counterpart on the source pages.
+ */
+int fft_debug_wait_timeout(int64_t polls, void *stream);
+
 /* Last status recorded on this host thread by a call that returns a
  * pointer (fft_plan_create). */
 int fft_last_status(void);

@@ -330,6 +330,19 @@ def test_exec_host_chain_matches_device_exec(fg, n, dims, batch, chunk):
 
 # --- error reporting on a GPU ------------------------------------------------
 
+def test_bounded_wait_reports_timeout(fg):
+    # A wait that runs out is reported through the device status word, the
+    # word is cleared by reading it, and the context stays usable.
+    assert fg.fft_device_status(stream()) == 0
+    assert fg.fft_debug_wait_timeout(2000, stream()) == 0
+    assert fg.fft_device_status(stream()) == fg.FFT_ERR_DEVICE_TIMEOUT
+    assert fg.fft_device_status(stream()) == 0
+    x = workloads.uniform_complex((2, 1024), 3, np.complex64)
+    y = run_plan(fg, x, 1024, 2, 1, fg.FFT_FORWARD, F32)
+    assert rel_rows(y, oracle.fft(x.astype(np.complex128))).max() <= tol(F32, 1024)
+    assert fg.fft_debug_wait_timeout(0, stream()) == fg.FFT_ERR_INVALID_ARG
+
+
 def test_misaligned_device_pointer(fg):
     p = fg.Plan(64, 1, 1, fg.FFT_FORWARD, F32)
     buf = torch.zeros(2 * 64 + 8, dtype=torch.complex64, device="cuda")
