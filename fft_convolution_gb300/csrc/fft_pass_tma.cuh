@@ -4,7 +4,7 @@
 // Same computation as fft_pass_kernel (one radix-L Stockham stage over HBM
 // whose L-point butterflies are on-chip transforms of C consecutive
 // columns), organised for sm_103a:
-//   * persistent blocks (one per SM), each walking the tiles
+//   * persistent blocks (as many as fit per SM), each walking the tiles
 //     blockIdx.x, blockIdx.x + gridDim.x, ...;
 //   * the input tile (L rows x C columns, rows 8*cols bytes apart) arrives
 //     by cp.async.bulk.tensor into one of two shared-memory buffers, tracked
@@ -87,12 +87,21 @@ template <typename T, int LOGL> struct TmaConfig {
   using P = StagePlan<LOGL>;
   using V = vec2_t<T>;
   static constexpr int L = P::L;
-  static constexpr int C = PassConfig<T, LOGL>::C;
+  // Half the plain kernel's tile width, but rows of at least 32 bytes:
+  // several double-buffered blocks per SM, whose barrier waits and compute
+  // overlap.  Measured on GB300 (2^26 fp32, L = 512): 16 columns, one block
+  // per SM 0.71 ms; 8 columns, three blocks 0.61 ms; 4 columns 0.76 ms.  At
+  // L = 2048 (4 columns = 32 bytes) the width stays.
+  static constexpr int C_MIN = (int)(32 / sizeof(V));
+  static constexpr int C = PassConfig<T, LOGL>::C / 2 >= C_MIN
+                               ? PassConfig<T, LOGL>::C / 2
+                               : (PassConfig<T, LOGL>::C < C_MIN ? PassConfig<T, LOGL>::C : C_MIN);
   static constexpr int THREADS = C * P::TP;
   static constexpr int ROWS_PER_BOX = L < 256 ? L : 256;  // TMA box limit per dimension
   static constexpr int BOXES = L / ROWS_PER_BOX;
   static constexpr uint32_t TILE_BYTES = (uint32_t)(C * L * sizeof(V));
   static constexpr int RAW_ELEMS = PassConfig<T, LOGL>::ROW_ELEMS * C;  // exchange / transpose
+  static constexpr int MIN_BLOCKS = THREADS >= 1024 ? 1 : (THREADS >= 512 ? 2 : (THREADS >= 256 ? 3 : 4));
   static constexpr int BUF_ELEMS =
       ((RAW_ELEMS * (int)sizeof(V) + 127) / 128) * 128 / (int)sizeof(V);
   // Stage-twiddle table shared by the block's columns (rounded to 128 B).
@@ -111,7 +120,7 @@ struct TmaGeom {
 };
 
 template <typename T, int LOGL, int DIR>
-__global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, 1)
+__global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL>::MIN_BLOCKS)
     fft_pass_tma_kernel(const __grid_constant__ CUtensorMap tin,
                         const __grid_constant__ CUtensorMap tout, vec2_t<T> *out_linear,
                         TmaGeom g, int *status) {
@@ -317,7 +326,11 @@ cudaError_t launch_pass_tma_t(const void *in, void *out, int log_n, int log_m, i
         kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
     if (attr != cudaSuccess) return attr;
     TmaGeom g{log_n, log_m, twiddle, cols / Cfg::C, (cols / Cfg::C) * batch};
-    long long grid = (long long)sms;
+    static int per_sm = 0;
+    if (per_sm == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                           &per_sm, kern, Cfg::THREADS, Cfg::SMEM) != cudaSuccess)
+      return cudaGetLastError();
+    long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);
     if (grid > g.total_tiles) grid = g.total_tiles;
     kern<<<(unsigned)grid, Cfg::THREADS, Cfg::SMEM, st>>>(
         tin, tout, static_cast<vec2_t<T> *>(out), g, device_status_word());
