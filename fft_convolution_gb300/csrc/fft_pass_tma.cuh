@@ -107,8 +107,12 @@ template <typename T, int LOGL> struct TmaConfig {
   // Stage-twiddle table shared by the block's columns (rounded to 128 B).
   static constexpr int TW_ELEMS =
       ((P::TW_ELEMS * (int)sizeof(V) + 127) / 128) * 128 / (int)sizeof(V);
+  // Two buffers (prefetch the next tile while computing this one) when that
+  // still leaves room for three blocks per SM; otherwise one buffer, and the
+  // overlap comes from the other blocks on the SM.
+  static constexpr int NBUF = 2 * BUF_ELEMS * sizeof(V) <= 76 * 1024 ? 2 : 1;
   static constexpr size_t SMEM =
-      256 + (size_t)TW_ELEMS * sizeof(V) + 2 * (size_t)BUF_ELEMS * sizeof(V);
+      256 + (size_t)TW_ELEMS * sizeof(V) + NBUF * (size_t)BUF_ELEMS * sizeof(V);
 };
 
 struct TmaGeom {
@@ -160,24 +164,34 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
   }
   fill_twiddle_table<LOGL, DIR>(twt, tid, Cfg::THREADS);
   __syncthreads();
-  if (tid == 0 && blockIdx.x < g.total_tiles) issue_load(blockIdx.x, 0);
+  if (Cfg::NBUF == 2 && tid == 0 && blockIdx.x < g.total_tiles) issue_load(blockIdx.x, 0);
 
   int k = 0;
   for (long long tile = blockIdx.x; tile < g.total_tiles; tile += gridDim.x, ++k) {
-    const int s = k & 1;
+    const int s = Cfg::NBUF == 2 ? (k & 1) : 0;
     V *const cur = buf0 + s * Cfg::BUF_ELEMS;
     const long long next = tile + gridDim.x;
-    __syncthreads();  // every thread is done with buffer s^1 (previous tile)
-    if (tid == 0 && next < g.total_tiles) {
-      bulk_wait_read_all();  // the previous tile's TMA store has left buffer s^1
-      issue_load(next, s ^ 1);
+    __syncthreads();  // every thread is done with the previous tile's buffer
+    bool prefetched = false;
+    if (tid == 0) {
+      if (Cfg::NBUF == 2) {
+        if (next < g.total_tiles) {
+          bulk_wait_read_all();  // the previous tile's TMA store has left buffer s^1
+          issue_load(next, s ^ 1);
+          prefetched = true;
+        }
+      } else {
+        bulk_wait_read_all();  // the previous tile's TMA store has left the buffer
+        issue_load(tile, 0);
+      }
     }
-    const bool ok = mbar_wait(&bar[s], (uint32_t)(k >> 1) & 1u);
+    const uint32_t parity = Cfg::NBUF == 2 ? (uint32_t)(k >> 1) & 1u : (uint32_t)k & 1u;
+    const bool ok = mbar_wait(&bar[s], parity);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) {
         atomicExch(status, kDeviceErrorTimeout);
         // Let the prefetch issued above land before the block exits.
-        if (next < g.total_tiles) mbar_wait(&bar[s ^ 1], (uint32_t)((k + 1) >> 1) & 1u);
+        if (prefetched) mbar_wait(&bar[s ^ 1], (uint32_t)((k + 1) >> 1) & 1u);
       }
       break;
     }
