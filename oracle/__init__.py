@@ -24,6 +24,8 @@ arrays.  Every function states the passage it follows:
 * ``bit_reverse`` -- "FFT on GPU", section reverse bit order.
 * ``polymul_*`` / ``poly_eval_mod`` -- "FFT on GPU", sections on the two
   representations of a polynomial and the whole pipeline.
+* ``convolve`` -- the same coefficient convolution c_k = sum_i a_i b_{k-i}
+  for complex signals (linear convolution), summed directly.
 
 Every oracle function here is pinned by a ``-m "not gpu"`` test in
 ``tests/test_oracle.py`` to something other than itself (closed forms,
@@ -85,6 +87,7 @@ def _load():
                 "oracle_polymul_schoolbook_at": [_I64, i64, _I64, i64, _I64, i64, _I64],
                 "oracle_polymul_fft": [_I64, i64, _I64, i64, _I64],
                 "oracle_poly_eval_mod": [_I64, i64, ctypes.c_uint64, _U64],
+                "oracle_convolve": [_D, i64, _D, i64, _D],
             }
             for name, args in sig.items():
                 fn = getattr(lib, name)
@@ -246,3 +249,22 @@ def poly_eval_mod(a, t: int) -> int:
     _check(_load().oracle_poly_eval_mod(_ip(a), a.size, ctypes.c_uint64(int(t) % MOD_P),
                                         ctypes.byref(out)), "poly_eval_mod")
     return int(out.value)
+
+
+def convolve(x, h) -> np.ndarray:
+    """Linear convolution y_k = sum_i x_i h_{k-i} of 1D sequences (complex
+    or real; returned complex128), or of each row of a 2D x with a 1D h, or
+    row-wise with a 2D h of the same number of rows."""
+    x = _c128(x)
+    h = _c128(h)
+    lib = _load()
+    if x.ndim == 1 and h.ndim == 1:
+        out = np.empty(x.size + h.size - 1, dtype=np.complex128)
+        _check(lib.oracle_convolve(_dp(x), x.size, _dp(h), h.size, _dp(out)), "convolve")
+        return out
+    x2 = x.reshape(-1, x.shape[-1])
+    rows = []
+    for r in range(x2.shape[0]):
+        hr = h if h.ndim == 1 else np.ascontiguousarray(h.reshape(-1, h.shape[-1])[r])
+        rows.append(convolve(np.ascontiguousarray(x2[r]), hr))
+    return np.stack(rows)

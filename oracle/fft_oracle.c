@@ -18,6 +18,8 @@
  *     - polynomial multiplication: coefficient convolution
  *       c_k = sum_i a_i b_{k-i}; inverse a_j = (1/N) sum_k A_k omega^{-jk}
  *     - reverse bit order: the 8-point order [x0,x4,x2,x6,x1,x5,x3,x7]
+ *     - the same coefficient convolution written for complex sequences is
+ *       the linear convolution of signals: y_k = sum_i x_i h_{k-i}
  *   "The Butterfly: One Thread, One Output" (gpu.rocks, FFT butterfly task 2)
  *     - one gather-shaped radix-2 pass: j = floor(i/half) mod 2,
  *       base = i - j*half, r = i mod half, w = e^{-i pi r / half}
@@ -361,5 +363,35 @@ int oracle_poly_eval_mod(const int64_t *a, int64_t na, uint64_t t, uint64_t *out
         acc = (acc * tt + ar) % p;
     }
     *out = (uint64_t)acc;
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Linear convolution of complex sequences, the definition written out:
+ *   y_k = sum_i x_i h_{k-i},  k = 0 .. nx+nh-2,
+ * Kahan-compensated on each component.  O(nx * nh).
+ * ------------------------------------------------------------------------- */
+int oracle_convolve(const double *x, int64_t nx, const double *h, int64_t nh, double *y) {
+    if (nx <= 0 || nh <= 0 || x == NULL || h == NULL || y == NULL) return -1;
+    const cplx *xc = (const cplx *)x;
+    const cplx *hc = (const cplx *)h;
+    cplx *out = (cplx *)y;
+    for (int64_t k = 0; k < nx + nh - 1; ++k) {
+        int64_t lo = k - (nh - 1) > 0 ? k - (nh - 1) : 0;
+        int64_t hi = k < nx - 1 ? k : nx - 1;
+        double sr = 0.0, si = 0.0, cr = 0.0, ci = 0.0;
+        for (int64_t i = lo; i <= hi; ++i) {
+            cplx term = xc[i] * hc[k - i];
+            double yr = creal(term) - cr;
+            double tr = sr + yr;
+            cr = (tr - sr) - yr;
+            sr = tr;
+            double yi = cimag(term) - ci;
+            double ti = si + yi;
+            ci = (ti - si) - yi;
+            si = ti;
+        }
+        out[k] = sr + si * I;
+    }
     return 0;
 }

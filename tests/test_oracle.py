@@ -356,3 +356,47 @@ def test_tones_signal_spectrum():
     mask = np.ones(n, bool)
     mask[bins] = False
     assert X[mask].max() < 8 * 0.1 * np.sqrt(2 * n)
+
+
+# --- linear convolution of signals ------------------------------------------
+
+@pytest.mark.parametrize("nx,nh", [(1, 1), (5, 3), (64, 17), (300, 1000)])
+def test_convolve_matches_numpy(nx, nh):
+    x = workloads.normal_complex(nx, nx, np.complex128)
+    h = workloads.normal_complex(nh, nh + 1, np.complex128)
+    y = oracle.convolve(x, h)
+    assert y.size == nx + nh - 1
+    assert rel_l2(y, np.convolve(x, h)) < 1e-14
+
+
+def test_convolve_delta_shift_commute_linear():
+    x = workloads.uniform_complex(50, 3, np.complex128)
+    h = workloads.uniform_complex(20, 4, np.complex128)
+    d = np.zeros(7, complex)
+    d[0] = 1
+    assert np.array_equal(oracle.convolve(x, d)[:50], x)               # delta is the identity
+    d = np.zeros(7, complex)
+    d[4] = 1
+    y = oracle.convolve(x, d)
+    assert np.array_equal(y[4:54], x) and np.all(y[:4] == 0)          # shifted delta shifts
+    assert rel_l2(oracle.convolve(x, h), oracle.convolve(h, x)) < 1e-15  # commutes
+    g = workloads.uniform_complex(50, 5, np.complex128)
+    lhs = oracle.convolve(2 * x - 1j * g, h)
+    assert rel_l2(lhs, 2 * oracle.convolve(x, h) - 1j * oracle.convolve(g, h)) < 1e-14
+
+
+def test_convolve_of_integers_is_the_polynomial_product():
+    a, b = workloads.poly_coeffs(40, 6)
+    y = oracle.convolve(a.astype(float), b.astype(float))
+    assert np.array_equal(np.rint(y.real).astype(np.int64), oracle.polymul_schoolbook(a, b))
+    assert np.max(np.abs(y.imag)) == 0
+
+
+def test_convolve_rows():
+    x = workloads.normal_complex((3, 40), 7, np.complex128)
+    h = workloads.normal_complex((3, 9), 8, np.complex128)
+    y = oracle.convolve(x, h)
+    for r in range(3):
+        assert rel_l2(y[r], np.convolve(x[r], h[r])) < 1e-14
+    y1 = oracle.convolve(x, h[0])
+    assert rel_l2(y1[2], np.convolve(x[2], h[0])) < 1e-14
