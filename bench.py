@@ -81,6 +81,18 @@ def workload_info(name: str, pass_log: int = 9):
             bytes_per_step=2 * 2 * 2 * arr, ideal_bytes_per_step=2 * 2 * arr,
             flops_per_step=2 * 5.0 * n * n * log2i(n * n) * batch,
             transforms_per_step=2 * batch, h2d=arr, d2h=arr)
+    if c["kind"] == "conv":
+        nh = c["nh"]
+        ny = n + nh - 1
+        L = 1 << (ny - 1).bit_length()
+        return dict(
+            kind="conv", n=n, nh=nh, batch=batch, L=L, passes=1, directions=2,
+            array_bytes=batch * n * 4,
+            bytes_per_step=batch * n * 4 + nh * 4 + batch * ny * 4,   # x, h read; y written
+            ideal_bytes_per_step=batch * n * 4 + nh * 4 + batch * ny * 4,
+            flops_per_step=2 * 5.0 * L * log2i(L) * ((batch + 1) // 2),
+            transforms_per_step=2 * ((batch + 1) // 2), h2d=batch * n * 4 + nh * 4,
+            d2h=batch * ny * 4)
     # polymul: fused ideal = int64 inputs read once + int64 output written once
     nc = 2 * n - 1
     L = 1 << (nc - 1).bit_length()
@@ -168,6 +180,7 @@ KERNEL_SOURCES = {
            "fft_pass_tma.cuh", "fft_pass_f32.cu", "fft_plan.cu"],
     "c5": ["fft_device.cuh", "fft_pass.cuh", "fft_pass_tma.cuh", "fft_pass_f64.cu",
            "polymul.cu"],
+    "conv1": ["fft_device.cuh", "fft_rows.cuh", "conv.cuh", "conv_f32.cu"],
 }
 
 
@@ -251,6 +264,14 @@ def cpu_oracle_sample(name: str, budget_s: float = 12.0):
             k += 1
         done_units = k / c["batch"]
         sample = f"{k} of {c['batch']} images {n}x{n} (forward+inverse)"
+    elif info["kind"] == "conv":
+        x, h = workloads.conv_signals(64, c["n"], c["nh"], c["seed"])
+        k = 0
+        while time.perf_counter() - t0 < budget_s and k < 64:
+            oracle.convolve(x[k].astype(np.complex128), h.astype(np.complex128))
+            k += 1
+        done_units = k / c["batch"]
+        sample = f"{k} of {c['batch']} signals (direct sum, {c['n']} x {c['nh']} taps)"
     else:
         n = c["n"]
         m = 1 << 16
@@ -315,7 +336,25 @@ def run_gpu(args):
     sh = int(stream.cuda_stream)
 
     # Inputs: seeded on the host, resident in HBM before timing.
-    if info["kind"] == "polymul":
+    if info["kind"] == "conv":
+        xc_h, hc_h = workloads.conv_signals(c["batch"], c["n"], c["nh"], c["seed"])
+        xc_d, hc_d = torch.from_numpy(xc_h).to(dev), torch.from_numpy(hc_h).to(dev)
+        ny = c["n"] + c["nh"] - 1
+        yc_d = torch.empty(c["batch"], ny, dtype=torch.float32, device=dev)
+        plans = []
+
+        def step(events=None):
+            if events is not None:
+                events[0].record(stream)
+            rc = fg.fft_convolve(xc_d.data_ptr(), c["n"], hc_d.data_ptr(), c["nh"],
+                                 yc_d.data_ptr(), c["batch"], 0, fg.FFT_CONV_REAL,
+                                 fg.FFT_C2C_F32, sh)
+            if events is not None:
+                events[1].record(stream)
+            assert rc == 0, fg.fft_status_string(rc)
+        kernels_per_step = fg.fft_convolve_num_kernels(c["n"], c["nh"], c["batch"], 0,
+                                                       fg.FFT_CONV_REAL, fg.FFT_C2C_F32)
+    elif info["kind"] == "polymul":
         a_h, b_h = workloads.poly_coeffs((c["batch"], c["n"]), c["seed"])
         a_d, b_d = torch.from_numpy(a_h).to(dev), torch.from_numpy(b_h).to(dev)
         c_d = torch.empty(c["batch"], 2 * c["n"] - 1, dtype=torch.int64, device=dev)
@@ -399,13 +438,13 @@ def run_gpu(args):
     # Per-launch durations of the dominant kernel (the forward transform;
     # for 1-kernel plans that is one launch per exec).
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    inv_ms = [e[1].elapsed_time(e[2]) for e in ev] if info["kind"] != "polymul" and \
+    inv_ms = [e[1].elapsed_time(e[2]) for e in ev] if info["kind"] in ("fft1d", "fft2d") and \
         info["directions"] == 2 else []
 
     # End-to-end through the host-buffer entry point: pinned host input ->
     # device, transforms, device -> pinned host output, every step.
     e2e = None
-    if info["kind"] != "polymul" and not args.no_e2e:
+    if info["kind"] in ("fft1d", "fft2d") and not args.no_e2e:
         h_in = torch.from_numpy(x_h).pin_memory()
         h_out = torch.empty_like(h_in).pin_memory()
         e2e_steps = max(1, min(args.steps, 5))
@@ -428,6 +467,28 @@ def run_gpu(args):
         e2e = {"value": info["bytes_per_step"] * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": info["h2d"], "d2h_bytes_per_step": info["d2h"],
                "ms_per_step": round(e2e_ms, 4), "chunk_transforms": chunk}
+    elif info["kind"] == "conv" and not args.no_e2e:
+        hx = torch.from_numpy(xc_h).pin_memory()
+        hy = torch.empty(yc_d.shape, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                xc_d.copy_(hx, non_blocking=True)
+                step()
+                hy.copy_(yc_d, non_blocking=True)
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(max(1, min(args.steps, 5))):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = s0.elapsed_time(s1) / max(1, min(args.steps, 5))
+        e2e = {"value": info["bytes_per_step"] * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": info["h2d"], "d2h_bytes_per_step": info["d2h"],
+               "ms_per_step": round(e2e_ms, 4)}
     elif info["kind"] == "polymul" and not args.no_e2e:
         ha, hb = torch.from_numpy(a_h).pin_memory(), torch.from_numpy(b_h).pin_memory()
         hc = torch.empty(c_d.shape, dtype=torch.int64).pin_memory()
@@ -457,7 +518,11 @@ def run_gpu(args):
     peak, peak_kind = measured_peaks()
     value = whole_job_value(info["bytes_per_step"], world, ms_step)
 
-    if info["kind"] == "polymul":
+    if info["kind"] == "conv":
+        dom_ms = statistics.mean(fwd_ms)
+        per_launch_bytes = info["bytes_per_step"]
+        dom_name = "fft_convolve (filter spectrum + fused convolution, %d kernels)" % kernels_per_step
+    elif info["kind"] == "polymul":
         dom_ms = statistics.mean(fwd_ms)
         per_launch_bytes = info["bytes_per_step"]
         dom_name = "polymul (whole fused pipeline, %d kernels)" % kernels_per_step
@@ -476,7 +541,8 @@ def run_gpu(args):
                 "inverse_launch_ms": round(statistics.mean(inv_ms), 4) if inv_ms else None}
 
     line = {
-        "metric": "batched C2C FFT effective GB/s",
+        "metric": "batched C2C FFT effective GB/s" if info["kind"] != "conv"
+                  else "batched FFT convolution effective GB/s",
         "value": round(value, 2),
         "unit": "GB/s",
         "n_gpus": world,
@@ -533,6 +599,9 @@ def workload_label(name: str) -> str:
         return "1D C2C forward, N=2^26, batch 1, fp32 (512 MiB), multi-pass"
     if name == "c4":
         return "2D C2C forward+inverse, 2048x2048, batch 8, fp32"
+    if name == "conv1":
+        return ("real fp32 convolution, 32768 signals x 3072 samples with one 1025-tap filter "
+                "(transform length 4096)")
     return f"polymul, {c['batch']} pairs of 2^20 int64 coefficients, fp64 transforms of 2^21"
 
 
@@ -562,7 +631,8 @@ def run_reference(args):
     ms_step = 1e3 * info["bytes_per_step"] / (value * 1e9)
     line = {
         "impl": "reference",
-        "metric": "batched C2C FFT effective GB/s",
+        "metric": "batched C2C FFT effective GB/s" if info["kind"] != "conv"
+                  else "batched FFT convolution effective GB/s",
         "value": round(value, 4),
         "unit": "GB/s",
         "n_gpus": world,

@@ -32,6 +32,9 @@ FFT_INVERSE = +1
 FFT_C2C_F32 = 0
 FFT_C2C_F64 = 1
 
+FFT_CONV_COMPLEX = 0
+FFT_CONV_REAL = 1
+
 # Every symbol the header declares, with its ctypes signature.
 _VP, _I64, _INT, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
@@ -46,6 +49,8 @@ SIGNATURES = {
     "polymul_batched": (_INT, [_VP, _I64, _VP, _I64, _VP, _I64, _VP]),
     "polymul_noalloc": (_INT, [_VP, _I64, _VP, _I64, _VP, _VP]),
     "polymul_num_kernels": (_INT, [_I64, _I64]),
+    "fft_convolve": (_INT, [_VP, _I64, _VP, _I64, _VP, _I64, _INT, _INT, _INT, _VP]),
+    "fft_convolve_num_kernels": (_INT, [_I64, _I64, _I64, _INT, _INT, _INT]),
     "fft_debug_radix2_pass": (_INT, [_VP, _VP, _I64, _I64, _INT, _VP]),
     "fft_device_status": (_INT, [_VP]),
     "fft_debug_wait_timeout": (_INT, [_I64, _VP]),
@@ -143,6 +148,16 @@ POLYMUL_NOALLOC_MAX_LEN = 65536
 
 def polymul_num_kernels(na: int, nb: int) -> int:
     return int(_lib.polymul_num_kernels(na, nb))
+
+
+def fft_convolve(x_ptr: int, nx: int, h_ptr: int, nh: int, y_ptr: int, batch: int,
+                 h_per_row: int, kind: int, dtype: int, stream: int) -> int:
+    return _lib.fft_convolve(x_ptr, nx, h_ptr, nh, y_ptr, batch, h_per_row, kind, dtype, stream)
+
+
+def fft_convolve_num_kernels(nx: int, nh: int, batch: int, h_per_row: int, kind: int,
+                             dtype: int) -> int:
+    return int(_lib.fft_convolve_num_kernels(nx, nh, batch, h_per_row, kind, dtype))
 
 
 def fft_debug_radix2_pass(in_ptr: int, out_ptr: int, n: int, half: int, dtype: int,
@@ -298,4 +313,30 @@ def polymul_tensors(a, b, out=None, stream=None):
     a2, b2 = a2.contiguous(), b2.contiguous()
     _check(polymul_batched(a2.data_ptr(), na, b2.data_ptr(), nb, out.data_ptr(), batch,
                            _stream_handle(stream)), "polymul_batched")
+    return out.reshape(-1) if squeeze else out
+
+
+def convolve(x, h, out=None, stream=None):
+    """Linear convolution of every row of x (CUDA tensor [batch, nx] or
+    [nx]; float32 / float64 / complex64 / complex128) with h ([nh] shared,
+    or [batch, nh] per row, same dtype); returns [batch, nx + nh - 1]."""
+    torch = _torch()
+    kinds = {torch.float32: (FFT_CONV_REAL, FFT_C2C_F32), torch.float64: (FFT_CONV_REAL, FFT_C2C_F64),
+             torch.complex64: (FFT_CONV_COMPLEX, FFT_C2C_F32),
+             torch.complex128: (FFT_CONV_COMPLEX, FFT_C2C_F64)}
+    if x.dtype not in kinds or h.dtype != x.dtype:
+        raise TypeError("x and h must share one of float32/64, complex64/128")
+    kind, dtype = kinds[x.dtype]
+    squeeze = x.dim() == 1
+    x2 = (x.reshape(1, -1) if squeeze else x).contiguous()
+    batch, nx = x2.shape
+    h_per_row = 1 if h.dim() == 2 else 0
+    h2 = h.contiguous()
+    nh = h2.shape[-1]
+    if h_per_row and h2.shape[0] != batch:
+        raise ValueError("a per-row filter needs one row per signal")
+    if out is None:
+        out = torch.empty(batch, nx + nh - 1, dtype=x.dtype, device=x.device)
+    _check(fft_convolve(x2.data_ptr(), nx, h2.data_ptr(), nh, out.data_ptr(), batch, h_per_row,
+                        kind, dtype, _stream_handle(stream)), "fft_convolve")
     return out.reshape(-1) if squeeze else out

@@ -553,6 +553,51 @@ int polymul(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, int64_t 
   return polymul_batched(a, na, b, nb, c, 1, stream);
 }
 
+// Maps the public (kind, h_per_row) to the internal variant and checks the
+// lengths; returns FFT_OK and the transform length, or an error.
+static int convolve_setup(int64_t nx, int64_t nh, int64_t batch, int h_per_row, int kind,
+                          int dtype, int *ikind, int *log_len) {
+  if (nx <= 0 || nh <= 0 || batch <= 0 || (h_per_row != 0 && h_per_row != 1) ||
+      (kind != FFT_CONV_COMPLEX && kind != FFT_CONV_REAL) ||
+      (dtype != FFT_C2C_F32 && dtype != FFT_C2C_F64))
+    return FFT_ERR_INVALID_ARG;
+  const int64_t ny = nx + nh - 1;
+  const int l = ny > 2 ? ilog2_exact(ny) : 1;
+  const int max_log = dtype == FFT_C2C_F32 ? 27 : 26;
+  if (l > max_log || batch > ((int64_t)1 << 40) / ((int64_t)1 << l)) return FFT_ERR_UNSUPPORTED;
+  *ikind = kind == FFT_CONV_COMPLEX ? 0 : (h_per_row ? 2 : 1);
+  *log_len = l;
+  return FFT_OK;
+}
+
+int fft_convolve(const void *x, int64_t nx, const void *h, int64_t nh, void *y, int64_t batch,
+                 int h_per_row, int kind, int dtype, void *stream) {
+  if (!x || !h || !y) return FFT_ERR_INVALID_ARG;
+  int ikind = 0, log_len = 0;
+  const int rc = convolve_setup(nx, nh, batch, h_per_row, kind, dtype, &ikind, &log_len);
+  if (rc != FFT_OK) return rc;
+  const uintptr_t align = (kind == FFT_CONV_COMPLEX ? 8u : 4u) * (dtype == FFT_C2C_F32 ? 1u : 2u);
+  if (((uintptr_t)x | (uintptr_t)h | (uintptr_t)y) & (align - 1)) return FFT_ERR_MISALIGNED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void *scratch = nullptr;
+  cudaError_t e = cudaMallocAsync(
+      &scratch, convolve_scratch_bytes(batch, h_per_row, ikind, dtype, log_len), st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = launch_convolve(x, nx, h, nh, y, batch, h_per_row, ikind, dtype, log_len, scratch, st);
+  cudaError_t f = cudaFreeAsync(scratch, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (f != cudaSuccess) return cuda_fail(f);
+  return FFT_OK;
+}
+
+int fft_convolve_num_kernels(int64_t nx, int64_t nh, int64_t batch, int h_per_row, int kind,
+                             int dtype) {
+  int ikind = 0, log_len = 0;
+  if (convolve_setup(nx, nh, batch, h_per_row, kind, dtype, &ikind, &log_len) != FFT_OK)
+    return 0;
+  return convolve_num_kernels(ikind, dtype, log_len);
+}
+
 int fft_debug_radix2_pass(const void *in, void *out, int64_t n, int64_t half, int dtype,
                           void *stream) {
   if (!in || !out || n <= 0 || half <= 0 || n % (2 * half) != 0 ||

@@ -77,4 +77,18 @@ cudaError_t launch_polymul(const long long *a, long long na, const long long *b,
                            long long *c, long long batch, int log_len, void *scratch,
                            cudaStream_t st);
 
+// Linear convolution of signals (conv.cu).  kind: 0 complex, 1 real rows in
+// pairs (shared real filter), 2 real rows one at a time.
+size_t convolve_scratch_bytes(long long batch, int h_per_row, int kind, int dtype, int log_len);
+int convolve_num_kernels(int kind, int dtype, int log_len);
+cudaError_t launch_convolve(const void *x, long long nx, const void *h, long long nh, void *y,
+                            long long batch, int h_per_row, int kind, int dtype, int log_len,
+                            void *scratch, cudaStream_t st);
+cudaError_t launch_convolve_f32(const void *x, long long nx, const void *h, long long nh, void *y,
+                                long long batch, int h_per_row, int kind, int log_len,
+                                void *scratch, cudaStream_t st);
+cudaError_t launch_convolve_f64(const void *x, long long nx, const void *h, long long nh, void *y,
+                                long long batch, int h_per_row, int kind, int log_len,
+                                void *scratch, cudaStream_t st);
+
 }  // namespace fftgb

@@ -189,6 +189,39 @@ int polymul_batched(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, 
 int polymul_noalloc(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, int64_t *c,
                     void *stream);
 
+/* Sample types of fft_convolve. */
+#define FFT_CONV_COMPLEX 0 /* interleaved complex samples of dtype */
+#define FFT_CONV_REAL 1    /* real samples: float (FFT_C2C_F32) or double (FFT_C2C_F64) */
+
+/*
+ * fft_convolve -- linear convolution of every row of x with a filter:
+ *   y[b][k] = sum_i x[b][i] h[k-i],  k < nx + nh - 1
+ * (the coefficient convolution of "FFT on GPU", polynomial-multiplication
+ * section, for complex or real samples), computed as the inverse transform
+ * of the pointwise product of the zero-padded forward transforms, length
+ * L = the smallest power of two >= nx + nh - 1.
+ *   x         device pointer, batch rows of nx samples (row-major).
+ *   h         device pointer: nh samples (h_per_row = 0, one filter for every
+ *             row) or batch rows of nh samples (h_per_row = 1).
+ *   y         device pointer, batch rows of nx + nh - 1 samples (written).
+ *   kind      FFT_CONV_COMPLEX or FFT_CONV_REAL; dtype FFT_C2C_F32 / _F64.
+ *             Pointers aligned to their sample size (else MISALIGNED).
+ * L <= 2^14 (fp32) / 2^13 (fp64): each row is read once and written once
+ * by one kernel (transform, product, inverse on chip).  Longer: 2-4 HBM
+ * passes per transform.  Real rows with one shared filter are transformed
+ * two at a time (as the real and imaginary parts of one complex signal).
+ * L <= 2^27 (fp32) / 2^26 (fp64).  Scratch (the filter spectra, and for long
+ * transforms two work arrays) is allocated with cudaMallocAsync on `stream`
+ * and freed the same way.  Asynchronous on `stream`.
+ */
+int fft_convolve(const void *x, int64_t nx, const void *h, int64_t nh, void *y, int64_t batch,
+                 int h_per_row, int kind, int dtype, void *stream);
+
+/* Kernels one fft_convolve call with these arguments launches (0 if the
+ * arguments are invalid). */
+int fft_convolve_num_kernels(int64_t nx, int64_t nh, int64_t batch, int h_per_row, int kind,
+                             int dtype);
+
 /*
  * fft_debug_radix2_pass -- test hook (not part of the transform API): one
  * gather-shaped radix-2 butterfly pass, "The Butterfly: One Thread, One

@@ -14,6 +14,8 @@ compute one by one, plus properties that hold at any size.
 * 64 polynomial pairs of 2^20 coefficients: 4096 sampled coefficients (64 per
   pair) exact against the schoolbook sum; C(t) = A(t) B(t) mod 2^61 - 1 at two
   points for every pair (covers every coefficient).
+* 32768 real signals x 3072 samples convolved with one 1025-tap filter: 16
+  sampled rows against the direct sum.
 
 All floating-point bounds are the relative-L2 tolerance 1e-5 * log2(N).
 """
@@ -163,3 +165,20 @@ def test_c5_polymul_64_pairs(fg):
             lhs = oracle.poly_eval_mod(out[p], t)
             rhs = oracle.poly_eval_mod(a[p], t) * oracle.poly_eval_mod(b[p], t) % oracle.MOD_P
             assert lhs == rhs, p
+
+
+def test_conv1_real_signals(fg):
+    # 32768 real fp32 signals x 3072 samples, one 1025-tap real filter: 16
+    # sampled rows (including the last) against the direct sum.
+    c = workloads.CONFIGS["conv1"]
+    x, h = workloads.config_input("conv1")
+    y = fg.convolve(torch.from_numpy(x).cuda(), torch.from_numpy(h).cuda())
+    torch.cuda.synchronize()
+    ny = c["n"] + c["nh"] - 1
+    assert tuple(y.shape) == (c["batch"], ny)
+    rows = np.unique(np.concatenate([workloads.sample_indices(15, c["batch"], 61),
+                                     [c["batch"] - 1]]))
+    got = y[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.complex128)
+    ref = oracle.convolve(x[rows].astype(np.complex128), h.astype(np.complex128))
+    err = np.linalg.norm(got - ref, axis=1) / np.linalg.norm(ref, axis=1)
+    assert err.max() <= TOL32 * 12

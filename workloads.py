@@ -20,6 +20,9 @@ Workloads (sizes and distributions):
   normal; forward 2D, then the inverse round trip.
 * ``c5``: 64 pairs of polynomials with 2^20 integer coefficients each,
   uniform on {0, ..., 9}; products have 2^21 - 1 coefficients.
+* ``conv1``: 32768 real fp32 signals of 3072 samples, i.i.d. standard
+  normal, convolved with one shared 1025-tap real filter (standard normal);
+  outputs have 4096 samples (transform length 4096).
 """
 from __future__ import annotations
 
@@ -31,6 +34,7 @@ CONFIGS = {
     "c3": dict(kind="fft1d", n=1 << 26, batch=1, dtype="f32", seed=3),
     "c4": dict(kind="fft2d", n=2048, batch=8, dtype="f32", seed=4),
     "c5": dict(kind="polymul", n=1 << 20, batch=64, dtype="f64", seed=5),
+    "conv1": dict(kind="conv", n=3072, nh=1025, batch=32768, dtype="f32", seed=6),
 }
 
 
@@ -134,4 +138,15 @@ def config_input(name: str, scale_batch: int | None = None):
         return normal_complex((batch, c["n"], c["n"]), c["seed"])
     if name == "c5":
         return poly_coeffs((batch, c["n"]), c["seed"])
+    if name == "conv1":
+        return conv_signals(batch, c["n"], c["nh"], c["seed"])
     raise KeyError(name)
+
+
+def conv_signals(batch: int, n: int, nh: int, seed: int):
+    """Real fp32 signals [batch, n] and one real fp32 filter [nh], i.i.d.
+    standard normal."""
+    g = generator(seed)
+    x = g.standard_normal(size=(batch, n), dtype=np.float32)
+    h = g.standard_normal(size=nh, dtype=np.float32)
+    return x, h
