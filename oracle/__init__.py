@@ -64,36 +64,49 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def bind(lib):
+    """Set the ctypes signatures of every oracle entry point on `lib` (a
+    CDLL of fft_oracle.c, or of a deliberately mutated copy in the pin
+    tests)."""
+    i64, c_int = ctypes.c_int64, ctypes.c_int
+    sig = {
+        "oracle_root_of_unity": [i64, i64, c_int, _D],
+        "oracle_dft": [_D, i64, c_int, _D],
+        "oracle_dft_bins": [_D, i64, c_int, _I64, i64, _D],
+        "oracle_fft": [_D, i64, c_int, _D],
+        "oracle_ifft": [_D, i64, _D],
+        "oracle_idft": [_D, i64, _D],
+        "oracle_fft_batch": [_D, i64, i64, c_int, _D],
+        "oracle_fft2d": [_D, i64, i64, c_int, _D],
+        "oracle_radix2_pass": [_D, i64, i64, _D],
+        "oracle_bit_reverse": [_D, i64, _D],
+        "oracle_bit_reverse_index": [i64, i64, _I64],
+        "oracle_stockham_stage": [_D, i64, c_int, _D],
+        "oracle_polymul_schoolbook_at": [_I64, i64, _I64, i64, _I64, i64, _I64],
+        "oracle_polymul_fft": [_I64, i64, _I64, i64, _I64],
+        "oracle_poly_eval_mod": [_I64, i64, ctypes.c_uint64, _U64],
+        "oracle_convolve": [_D, i64, _D, i64, _D],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB_PATH)
-            i64, c_int = ctypes.c_int64, ctypes.c_int
-            sig = {
-                "oracle_root_of_unity": [i64, i64, c_int, _D],
-                "oracle_dft": [_D, i64, c_int, _D],
-                "oracle_dft_bins": [_D, i64, c_int, _I64, i64, _D],
-                "oracle_fft": [_D, i64, c_int, _D],
-                "oracle_ifft": [_D, i64, _D],
-                "oracle_idft": [_D, i64, _D],
-                "oracle_fft_batch": [_D, i64, i64, c_int, _D],
-                "oracle_fft2d": [_D, i64, i64, c_int, _D],
-                "oracle_radix2_pass": [_D, i64, i64, _D],
-                "oracle_bit_reverse": [_D, i64, _D],
-                "oracle_bit_reverse_index": [i64, i64, _I64],
-                "oracle_stockham_stage": [_D, i64, c_int, _D],
-                "oracle_polymul_schoolbook_at": [_I64, i64, _I64, i64, _I64, i64, _I64],
-                "oracle_polymul_fft": [_I64, i64, _I64, i64, _I64],
-                "oracle_poly_eval_mod": [_I64, i64, ctypes.c_uint64, _U64],
-                "oracle_convolve": [_D, i64, _D, i64, _D],
-            }
-            for name, args in sig.items():
-                fn = getattr(lib, name)
-                fn.argtypes = args
-                fn.restype = ctypes.c_int
-            _lib = lib
+            # ORACLE_LIB_OVERRIDE: a library built from a deliberately mutated
+            # copy of fft_oracle.c, used by the pin-strength tests to show that
+            # the pins catch planted mistakes.
+            override = os.environ.get("ORACLE_LIB_OVERRIDE")
+            if override:
+                _lib = bind(ctypes.CDLL(override))
+            else:
+                build()
+                _lib = bind(ctypes.CDLL(_LIB_PATH))
     return _lib
 
 
