@@ -39,6 +39,7 @@ FFT_CONV_REAL = 1
 _VP, _I64, _INT, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
     "fft_plan_create": (_VP, [_I64, _I64, _INT, _INT, _INT]),
+    "fft_plan_create_nd": (_VP, [_INT, _VP, _I64, _INT, _INT]),
     "fft_plan_destroy": (None, [_VP]),
     "fft_plan_workspace_bytes": (_SZ, [_VP]),
     "fft_plan_num_kernels": (_INT, [_VP]),
@@ -97,6 +98,15 @@ def fft_plan_create(n: int, batch: int, dims: int, direction: int, dtype: int) -
     h = _lib.fft_plan_create(n, batch, dims, direction, dtype)
     if not h:
         raise FFTError(_lib.fft_last_status(), "fft_plan_create")
+    return h
+
+
+def fft_plan_create_nd(rank: int, shape, batch: int, direction: int, dtype: int) -> int:
+    """shape: a sequence of `rank` sides (marshalled to an int64 array)."""
+    arr = (ctypes.c_int64 * rank)(*shape)
+    h = _lib.fft_plan_create_nd(rank, arr, batch, direction, dtype)
+    if not h:
+        raise FFTError(_lib.fft_last_status(), "fft_plan_create_nd")
     return h
 
 
@@ -212,10 +222,17 @@ class Plan:
     or of n x n images (dims=2)."""
 
     def __init__(self, n: int, batch: int = 1, dims: int = 1, direction: int = FFT_FORWARD,
-                 dtype: int = FFT_C2C_F32):
-        self.n, self.batch, self.dims = n, batch, dims
-        self.direction, self.dtype = direction, dtype
-        self.handle = fft_plan_create(n, batch, dims, direction, dtype)
+                 dtype: int = FFT_C2C_F32, shape=None):
+        """n / dims as fft_plan_create; or shape=(H, W) / (D, H, W) for
+        fft_plan_create_nd."""
+        self.batch, self.direction, self.dtype = batch, direction, dtype
+        if shape is not None:
+            self.shape = tuple(int(v) for v in shape)
+            self.handle = fft_plan_create_nd(len(self.shape), self.shape, batch, direction, dtype)
+        else:
+            self.shape = (n,) if dims == 1 else (n, n)
+            self.handle = fft_plan_create(n, batch, dims, direction, dtype)
+        self.n, self.dims = self.shape[-1], len(self.shape)
 
     @property
     def workspace_bytes(self) -> int:
@@ -226,7 +243,10 @@ class Plan:
         return fft_plan_num_kernels(self.handle)
 
     def numel(self) -> int:
-        return self.batch * self.n * (self.n if self.dims == 2 else 1)
+        total = self.batch
+        for v in self.shape:
+            total *= v
+        return total
 
     def exec(self, inp, out=None, stream=None):
         """Run on device tensors (complex64 / complex128, contiguous)."""
@@ -340,3 +360,19 @@ def convolve(x, h, out=None, stream=None):
     _check(fft_convolve(x2.data_ptr(), nx, h2.data_ptr(), nh, out.data_ptr(), batch, h_per_row,
                         kind, dtype, _stream_handle(stream)), "fft_convolve")
     return out.reshape(-1) if squeeze else out
+
+
+def fftn(x, ndim: int, direction: int = FFT_FORWARD, out=None, stream=None):
+    """Transforms over the last `ndim` (1-3) axes of a contiguous CUDA
+    tensor, power-of-two sides."""
+    shape = tuple(x.shape[-ndim:])
+    batch = x.numel()
+    for v in shape:
+        batch //= v
+    p = Plan(0, batch, direction=direction, dtype=_dtype_code(x), shape=shape)
+    try:
+        return p.exec(x, out, stream)
+    finally:
+        if stream is None:
+            _torch().cuda.current_stream().synchronize()
+        p.close()

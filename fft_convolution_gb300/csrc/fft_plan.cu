@@ -41,7 +41,7 @@ namespace {
 thread_local int g_status = FFT_OK;
 thread_local cudaError_t g_cuda_error = cudaSuccess;
 
-enum Kind { KIND_ROWS = 0, KIND_MULTI = 1, KIND_2D = 2 };
+enum Kind { KIND_ROWS = 0, KIND_MULTI = 1, KIND_ND = 2 };
 
 constexpr int kMaxPasses = 8;
 
@@ -106,8 +106,11 @@ cudaError_t launch_pass(int dtype, int dir, const PassArgs &a, const void *in, v
 }  // namespace
 
 struct fft_plan {
-  int64_t n;
+  int64_t n;      // 1D: the length; ND: the innermost (contiguous) side
   int64_t batch;
+  int64_t elems;  // elements per transform (n, or the product of the sides)
+  int rank;       // 1, 2 or 3
+  int shape_log[3];  // log2 of the sides, outermost first (ND)
   int dims;
   int direction;
   int dtype;
@@ -123,8 +126,11 @@ extern "C" {
 
 fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int dtype) {
   g_status = FFT_OK;
-  if (n <= 0 || batch <= 0 || (dims != 1 && dims != 2) ||
-      (direction != FFT_FORWARD && direction != FFT_INVERSE) ||
+  if (dims == 2) {
+    const int64_t shape[2] = {n, n};
+    return fft_plan_create_nd(2, shape, batch, direction, dtype);
+  }
+  if (n <= 0 || batch <= 0 || dims != 1 || (direction != FFT_FORWARD && direction != FFT_INVERSE) ||
       (dtype != FFT_C2C_F32 && dtype != FFT_C2C_F64)) {
     g_status = FFT_ERR_INVALID_ARG;
     return nullptr;
@@ -145,20 +151,13 @@ fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int
   memset(p, 0, sizeof(*p));
   p->n = n;
   p->batch = batch;
-  p->dims = dims;
+  p->elems = n;
+  p->rank = 1;
+  p->dims = 1;
   p->direction = direction;
   p->dtype = dtype;
   p->logn = logn;
 
-  if (dims == 2) {
-    if (logn > on_chip_max || batch > ((int64_t)1 << 40) / (n * n)) {
-      delete p;
-      g_status = FFT_ERR_UNSUPPORTED;
-      return nullptr;
-    }
-    p->kind = KIND_2D;
-    return p;
-  }
   if (logn <= on_chip_max) {
     p->kind = KIND_ROWS;
     return p;
@@ -193,6 +192,60 @@ fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int
   return p;
 }
 
+fft_plan *fft_plan_create_nd(int rank, const int64_t *shape, int64_t batch, int direction,
+                             int dtype) {
+  g_status = FFT_OK;
+  if (rank == 1 && shape) return fft_plan_create(shape[0], batch, 1, direction, dtype);
+  if ((rank != 2 && rank != 3) || !shape || batch <= 0 ||
+      (direction != FFT_FORWARD && direction != FFT_INVERSE) ||
+      (dtype != FFT_C2C_F32 && dtype != FFT_C2C_F64)) {
+    g_status = FFT_ERR_INVALID_ARG;
+    return nullptr;
+  }
+  const int on_chip_max = dtype == FFT_C2C_F32 ? RowsMaxLog<float>::value : RowsMaxLog<double>::value;
+  const int pass_max = dtype == FFT_C2C_F32 ? kPassMaxLogF32 : kPassMaxLogF64;
+  int logs[3] = {0, 0, 0};
+  int total_log = 0;
+  for (int k = 0; k < rank; ++k) {
+    if (shape[k] <= 0) {
+      g_status = FFT_ERR_INVALID_ARG;
+      return nullptr;
+    }
+    if (!is_pow2(shape[k])) {
+      g_status = FFT_ERR_NOT_POW2;
+      return nullptr;
+    }
+    logs[k] = ilog2_exact(shape[k]);
+    total_log += logs[k];
+    // The innermost side runs on chip; the others as in-place column passes.
+    if (logs[k] > (k == rank - 1 ? on_chip_max : pass_max)) {
+      g_status = FFT_ERR_UNSUPPORTED;
+      return nullptr;
+    }
+  }
+  if (total_log > 34 || batch > ((int64_t)1 << 40) / ((int64_t)1 << total_log)) {
+    g_status = FFT_ERR_UNSUPPORTED;
+    return nullptr;
+  }
+  fft_plan *p = new (std::nothrow) fft_plan;
+  if (!p) {
+    g_status = FFT_ERR_ALLOC;
+    return nullptr;
+  }
+  memset(p, 0, sizeof(*p));
+  p->kind = KIND_ND;
+  p->rank = rank;
+  p->dims = rank;
+  for (int k = 0; k < rank; ++k) p->shape_log[k] = logs[k];
+  p->n = shape[rank - 1];
+  p->logn = logs[rank - 1];
+  p->elems = (int64_t)1 << total_log;
+  p->batch = batch;
+  p->direction = direction;
+  p->dtype = dtype;
+  return p;
+}
+
 void fft_plan_destroy(fft_plan *plan) {
   if (!plan) return;
   if (plan->workspace) cudaFree(plan->workspace);
@@ -216,9 +269,9 @@ struct Schedule {
 
   size_t elem() const { return p->dtype == FFT_C2C_F32 ? 8 : 16; }
 
-  cudaError_t rows(const void *in, void *out, long long batch) {
+  cudaError_t rows(const void *in, void *out, long long nrows) {
     ++count;
-    return dry ? cudaSuccess : launch_rows(p->dtype, p->logn, p->direction, in, out, batch, st);
+    return dry ? cudaSuccess : launch_rows(p->dtype, p->logn, p->direction, in, out, nrows, st);
   }
   cudaError_t pass(const PassArgs &a, const void *in, void *out) {
     ++count;
@@ -228,26 +281,31 @@ struct Schedule {
     return p->dtype == FFT_C2C_F32 ? pass_tile_cols_f32(log_l) : pass_tile_cols_f64(log_l);
   }
 
-  // 2D: rows (contiguous axis), then the columns in place, one L2-sized
-  // group of images at a time so the column pass reads the row pass's
-  // output from L2.
-  cudaError_t run_2d(const char *in, char *out) {
-    const long long n = p->n;
-    const size_t img = (size_t)n * (size_t)n * elem();
+  // 2D / 3D: rows (the contiguous side) on chip, then every other axis as
+  // an in-place column pass (stride = the product of the inner sides), from
+  // the inner axes outward.  With an L2 budget set, one L2-sized group of
+  // transforms at a time so the column passes read the rows' output from L2.
+  cudaError_t run_nd(const char *in, char *out) {
+    const size_t tbytes = (size_t)p->elems * elem();
     const size_t budget = l2_group_bytes();
-    long long g = budget ? (long long)(budget / img) : batch;
+    long long g = budget ? (long long)(budget / tbytes) : batch;
     if (g < 1) g = 1;
     for (long long b0 = 0; b0 < batch; b0 += g) {
       const long long nb = batch - b0 < g ? batch - b0 : g;
-      const size_t off = (size_t)b0 * img;
-      cudaError_t e = rows(in + off, out + off, nb * n);
-      if (e != cudaSuccess || p->logn == 0) {  // 1 x 1: rows already did it
-        if (e != cudaSuccess) return e;
-        continue;
-      }
-      PassArgs a{2 * p->logn, p->logn, p->logn, 0, nb, {}};
-      e = pass(a, out + off, out + off);
+      const size_t off = (size_t)b0 * tbytes;
+      cudaError_t e = rows(in + off, out + off, nb * (p->elems >> p->logn));
       if (e != cudaSuccess) return e;
+      int inner = p->logn;  // log2 of the stride of the next axis
+      for (int k = p->rank - 2; k >= 0; --k) {
+        const int l = p->shape_log[k];
+        if (l > 0) {
+          const int log_block = l + inner;  // one column block: L * stride elements
+          PassArgs a{log_block, l, inner, 0, nb * (p->elems >> log_block), {}};
+          e = pass(a, out + off, out + off);
+          if (e != cudaSuccess) return e;
+        }
+        inner += l;
+      }
     }
     return cudaSuccess;
   }
@@ -336,8 +394,8 @@ struct Schedule {
     switch (p->kind) {
       case KIND_ROWS:
         return rows(in, out, batch);
-      case KIND_2D:
-        return run_2d(i, o);
+      case KIND_ND:
+        return run_nd(i, o);
       case KIND_MULTI:
         return run_multi(i, o);
       default:
@@ -374,7 +432,7 @@ int fft_exec_host(const fft_plan *p, const void *host_in, void *host_out, void *
   if (misaligned(dev_in) || misaligned(dev_out)) return FFT_ERR_MISALIGNED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t elem = p->dtype == FFT_C2C_F32 ? 8 : 16;
-  const size_t count = (size_t)p->batch * (size_t)p->n * (p->dims == 2 ? (size_t)p->n : 1);
+  const size_t count = (size_t)p->batch * (size_t)p->elems;
   const size_t bytes = count * elem;
   cudaError_t e;
   if (host_in) {
@@ -461,8 +519,8 @@ int fft_exec_host_chain(const fft_plan *const *plans, int nplans, const void *ho
   const fft_plan *p0 = plans[0];
   for (int k = 0; k < nplans; ++k) {
     const fft_plan *q = plans[k];
-    if (!q || q->n != p0->n || q->dims != p0->dims || q->dtype != p0->dtype ||
-        q->batch != p0->batch)
+    if (!q || q->elems != p0->elems || q->rank != p0->rank || q->n != p0->n ||
+        q->dtype != p0->dtype || q->batch != p0->batch)
       return FFT_ERR_INVALID_ARG;
   }
   if (misaligned(dev_a) || misaligned(dev_b)) return FFT_ERR_MISALIGNED;
@@ -471,7 +529,7 @@ int fft_exec_host_chain(const fft_plan *const *plans, int nplans, const void *ho
   const long long nchunks = (batch + chunk - 1) / chunk;
   if (nchunks > 4096) return FFT_ERR_INVALID_ARG;
   const size_t elem = p0->dtype == FFT_C2C_F32 ? 8 : 16;
-  const size_t tbytes = (size_t)p0->n * (p0->dims == 2 ? (size_t)p0->n : 1) * elem;
+  const size_t tbytes = (size_t)p0->elems * elem;
 
   std::lock_guard<std::mutex> lock(g_pipe_mutex);
   HostPipe *hp = nullptr;

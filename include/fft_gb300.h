@@ -74,7 +74,8 @@ typedef struct fft_plan fft_plan;
  *             and batch * n * element size must fit the device.  dims = 2:
  *             n <= 2^14 (fp32) / 2^13 (fp64).
  *   batch     number of independent transforms, >= 1.
- *   dims      1 or 2.
+ *   dims      1, or 2 for an n x n transform (= fft_plan_create_nd with
+ *             shape {n, n}).
  *   direction FFT_FORWARD or FFT_INVERSE.
  *   dtype     FFT_C2C_F32 or FFT_C2C_F64.
  * Lengths up to 2^14 (fp32) / 2^13 (fp64) run as one kernel in which one
@@ -85,6 +86,20 @@ typedef struct fft_plan fft_plan;
  * (fft_last_status(): INVALID_ARG, NOT_POW2, UNSUPPORTED, ALLOC).
  */
 fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int dtype);
+
+/*
+ * fft_plan_create_nd -- plan `batch` multi-dimensional transforms of shape
+ * shape[0] x ... x shape[rank-1] (row-major: the last side is contiguous),
+ * rank 1, 2 or 3 ("Stockham FFT Butterfly Algorithm in Parallel GLSL",
+ * section Multi-Dimensional Transforms: the 1D transform along each axis in
+ * turn, rows first).  Every side a power of two; the last side at most
+ * 2^14 (fp32) / 2^13 (fp64), the others at most the same.  The inverse
+ * scales by 1/(product of the sides).  Runs as one on-chip row kernel plus
+ * one in-place column pass per other axis; no workspace.  rank 1 is
+ * fft_plan_create(shape[0], batch, 1, ...).  Errors as fft_plan_create.
+ */
+fft_plan *fft_plan_create_nd(int rank, const int64_t *shape, int64_t batch, int direction,
+                             int dtype);
 
 /* Frees the plan and its workspace.  NULL is ignored.  The caller must make
  * sure no fft_exec of this plan is still running on the GPU. */

@@ -15,8 +15,9 @@ arrays.  Every function states the passage it follows:
 * ``fft`` / ``ifft`` -- the recursive even/odd Cooley-Tukey derivation,
   "FFT on GPU", section Fast Fourier Transform; the inverse with the conjugate
   root and 1/N, section "polynomial multiplication and FFT".
-* ``fft2d`` -- separable 2D: rows, then columns, "Stockham FFT Butterfly
-  Algorithm in Parallel GLSL", section Multi-Dimensional Transforms.
+* ``fft2d`` / ``fftn`` -- separable 2D / nD: rows, then columns (then depth),
+  "Stockham FFT Butterfly Algorithm in Parallel GLSL", section
+  Multi-Dimensional Transforms.
 * ``radix2_pass`` -- one gather-shaped pass, "The Butterfly: One Thread, One
   Output" (gpu.rocks), the j / base / r recipe.
 * ``stockham_stage`` -- one Stockham stage, "Stockham FFT Butterfly Algorithm
@@ -281,3 +282,16 @@ def convolve(x, h) -> np.ndarray:
         hr = h if h.ndim == 1 else np.ascontiguousarray(h.reshape(-1, h.shape[-1])[r])
         rows.append(convolve(np.ascontiguousarray(x2[r]), hr))
     return np.stack(rows)
+
+
+def fftn(x, ndim: int, direction: int = -1) -> np.ndarray:
+    """The recursive CT along each of the last `ndim` axes in turn, the
+    contiguous axis first (separable transform); the inverse scales by
+    1/(product of the sides).  numpy only moves axes; the arithmetic is the
+    oracle's."""
+    y = _c128(x)
+    for k in range(1, ndim + 1):
+        axis = y.ndim - k
+        moved = np.ascontiguousarray(np.moveaxis(y, axis, -1))
+        y = np.moveaxis(fft(moved, direction), -1, axis)
+    return np.ascontiguousarray(y)

@@ -209,6 +209,44 @@ def test_2d_large_sides(fg, dtype, logn):
         assert rel_rows(y, oracle.fft2d(x.astype(np.complex128))).max() <= tol(dtype, n * n)
 
 
+@pytest.mark.parametrize("dtype", [F32, F64])
+@pytest.mark.parametrize("shape", [(2, 8), (64, 32), (16, 1024), (1024, 16), (4, 8, 16),
+                                   (32, 16, 64), (2, 2, 2), (1, 16, 16), (128, 1, 4), (8, 4, 1)])
+def test_nd_forward_inverse(fg, dtype, shape):
+    batch = 3
+    x = workloads.normal_complex((batch,) + shape, 3500 + sum(shape), NP[dtype])
+    npts = int(np.prod(shape))
+    p = fg.Plan(0, batch, direction=fg.FFT_FORWARD, dtype=dtype, shape=shape)
+    pi = fg.Plan(0, batch, direction=fg.FFT_INVERSE, dtype=dtype, shape=shape)
+    d = torch.from_numpy(x).cuda()
+    y = p.exec(d)
+    z = pi.exec(y)
+    torch.cuda.synchronize()
+    ref = oracle.fftn(x.astype(np.complex128), len(shape))
+    assert rel_rows(y.cpu().numpy(), ref).max() <= tol(dtype, npts)
+    assert rel_rows(z.cpu().numpy(), x).max() <= 2 * tol(dtype, npts)
+    p.close()
+    pi.close()
+
+
+def test_nd_large_3d(fg):
+    shape = (256, 512, 64)        # 8 Mi points: rows of 64, columns of 512 and 256
+    x = workloads.uniform_complex((1,) + shape, 3600, np.complex64)
+    y = fg.fftn(torch.from_numpy(x).cuda(), 3)
+    torch.cuda.synchronize()
+    ref = np.fft.fftn(x.astype(np.complex128), axes=(1, 2, 3))
+    assert rel_rows(y.cpu().numpy(), ref).max() <= tol(F32, int(np.prod(shape)))
+
+
+def test_nd_rejects(fg):
+    with pytest.raises(fg.FFTError):
+        fg.Plan(0, 1, shape=(6, 8))                 # not a power of two
+    with pytest.raises(fg.FFTError):
+        fg.Plan(0, 1, shape=(2, 2, 1 << 15))        # contiguous side beyond on chip
+    with pytest.raises(fg.FFTError):
+        fg.fft_plan_create_nd(4, (2, 2, 2, 2), 1, -1, 0)
+
+
 # --- polynomial multiplication ----------------------------------------------
 
 @pytest.mark.parametrize("na,nb,batch", [(1, 1, 1), (1, 5, 2), (5, 7, 3), (16, 16, 4),

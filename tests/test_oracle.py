@@ -400,3 +400,17 @@ def test_convolve_rows():
         assert rel_l2(y[r], np.convolve(x[r], h[r])) < 1e-14
     y1 = oracle.convolve(x, h[0])
     assert rel_l2(y1[2], np.convolve(x[2], h[0])) < 1e-14
+
+
+@pytest.mark.parametrize("shape", [(2, 8), (16, 4), (4, 8, 16), (2, 1, 32), (8, 8, 8)])
+def test_fftn_matches_numpy(shape):
+    x = workloads.normal_complex((2,) + shape, 900 + len(shape), np.complex128)
+    nd = len(shape)
+    X = oracle.fftn(x, nd)
+    assert rel_l2(X, np.fft.fftn(x, axes=tuple(range(-nd, 0)))) < 1e-14
+    assert rel_l2(oracle.fftn(X, nd, +1), x) < 1e-14
+    d = np.zeros(shape, complex)
+    d[(0,) * nd] = 1
+    assert np.array_equal(oracle.fftn(d, nd), np.ones(shape))
+    if nd == 2:
+        assert rel_l2(X, oracle.fft2d(x)) < 1e-15
