@@ -86,11 +86,11 @@ template <typename T, int LOGN> struct ConvRowsBounds {
   static constexpr int MIN_BLOCKS = THREADS >= 1024 ? 1 : 1024 / THREADS;
 };
 
-template <typename T, int LOGN, int KIND, int MODE>
+// Src: (row, idx) -> sample (zero beyond the data); Snk: (row, idx, value).
+template <typename T, int LOGN, int MODE, class Src, class Snk>
 __global__ void __launch_bounds__(ConvRowsBounds<T, LOGN>::THREADS,
                                   ConvRowsBounds<T, LOGN>::MIN_BLOCKS)
-    conv_rows_kernel(ConvSource<T, KIND> src, ConvSink<T, KIND> dst, vec2_t<T> *H,
-                     int h_per_row, long long trows) {
+    conv_rows_kernel(Src src, Snk dst, vec2_t<T> *H, int h_per_row, long long trows) {
   using V = vec2_t<T>;
   using P = StagePlan<LOGN>;
   constexpr int F = RowsConfig<T, LOGN>::F;
@@ -127,16 +127,17 @@ __global__ void __launch_bounds__(ConvRowsBounds<T, LOGN>::THREADS,
   }
 }
 
-template <typename T, int KIND, int MODE, int LOGN = 1>
-cudaError_t launch_conv_rows(int logn, ConvSource<T, KIND> src, ConvSink<T, KIND> dst,
-                             vec2_t<T> *H, int h_per_row, long long trows, cudaStream_t st) {
+template <typename T, int MODE, class Src, class Snk, int LOGN = 1>
+cudaError_t launch_conv_rows(int logn, Src src, Snk dst, vec2_t<T> *H, int h_per_row,
+                             long long trows, cudaStream_t st) {
   if constexpr (LOGN > RowsMaxLog<T>::value) {
     return cudaErrorInvalidValue;
   } else {
     if (logn != LOGN)
-      return launch_conv_rows<T, KIND, MODE, LOGN + 1>(logn, src, dst, H, h_per_row, trows, st);
+      return launch_conv_rows<T, MODE, Src, Snk, LOGN + 1>(logn, src, dst, H, h_per_row, trows,
+                                                           st);
     using C = RowsConfig<T, LOGN>;
-    auto kern = conv_rows_kernel<T, LOGN, KIND, MODE>;
+    auto kern = conv_rows_kernel<T, LOGN, MODE, Src, Snk>;
     if (C::SMEM > 48 * 1024) {
       static cudaError_t attr = cudaFuncSetAttribute(
           kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
@@ -241,10 +242,9 @@ cudaError_t convolve_t(const void *x, long long nx, const void *h, long long nh,
   ConvSink<T, KIND> ysink{y, ny, batch};
   cudaError_t e;
   if (log_len <= RowsMaxLog<T>::value) {
-    e = launch_conv_rows<T, HK, 0>(log_len, hsrc, ConvSink<T, HK>{nullptr, 0, 0}, H, 0, nfilt,
-                                   st);
+    e = launch_conv_rows<T, 0>(log_len, hsrc, ConvSink<T, HK>{nullptr, 0, 0}, H, 0, nfilt, st);
     if (e != cudaSuccess) return e;
-    return launch_conv_rows<T, KIND, 1>(log_len, xsrc, ysink, H, h_per_row, trows, st);
+    return launch_conv_rows<T, 1>(log_len, xsrc, ysink, H, h_per_row, trows, st);
   }
   V *bufs[2] = {H + nfilt * L, H + nfilt * L + trows * L};
   // H = FFT(h padded), written straight into H by the last pass.

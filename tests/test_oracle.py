@@ -414,3 +414,20 @@ def test_fftn_matches_numpy(shape):
     assert np.array_equal(oracle.fftn(d, nd), np.ones(shape))
     if nd == 2:
         assert rel_l2(X, oracle.fft2d(x)) < 1e-15
+
+
+# --- lengths that are not powers of two (direct DFT) ------------------------
+
+@pytest.mark.parametrize("n", [3, 5, 6, 12, 97, 1000])
+def test_direct_dft_any_length_matches_numpy(n):
+    x = workloads.normal_complex(n, 1100 + n, np.complex128)
+    assert rel_l2(oracle.dft(x), np.fft.fft(x)) < 1e-13
+    assert rel_l2(oracle.dft(x, +1), np.fft.ifft(x)) < 1e-13
+
+
+def test_direct_dft_closed_form_n3():
+    # omega_3 = e^{-2 pi i / 3} = -1/2 - i sqrt(3)/2; X_k = sum_n x_n omega^{kn}.
+    a = workloads.uniform_complex(3, 13, np.complex128)
+    w = -0.5 - 0.5j * np.sqrt(3.0)
+    expect = [a[0] + a[1] + a[2], a[0] + w * a[1] + w * w * a[2], a[0] + w * w * a[1] + w * a[2]]
+    assert np.allclose(oracle.dft(a), expect, atol=1e-14)
