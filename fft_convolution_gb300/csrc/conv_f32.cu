@@ -24,6 +24,11 @@ int convolve_num_kernels(int kind, int dtype, int log_len) {
   return 3 * P;
 }
 
+int convolve_passes(int dtype, int log_len) {
+  int logs[8];
+  return conv_split(log_len, dtype == 0 ? conv_pass_log<float>() : conv_pass_log<double>(), logs);
+}
+
 cudaError_t launch_convolve_f32(const void *x, long long nx, const void *h, long long nh, void *y,
                                 long long batch, int h_per_row, int kind, int log_len,
                                 void *scratch, cudaStream_t st) {

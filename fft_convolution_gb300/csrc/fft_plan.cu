@@ -41,7 +41,11 @@ namespace {
 thread_local int g_status = FFT_OK;
 thread_local cudaError_t g_cuda_error = cudaSuccess;
 
-enum Kind { KIND_ROWS = 0, KIND_MULTI = 1, KIND_ND = 2 };
+enum Kind { KIND_ROWS = 0, KIND_MULTI = 1, KIND_ND = 2, KIND_DFT = 3, KIND_BLUESTEIN = 4 };
+
+// Lengths that are not powers of two: the direct DFT up to this length,
+// Bluestein beyond.
+constexpr int64_t kDirectDftMax = 64;
 
 constexpr int kMaxPasses = 8;
 
@@ -120,7 +124,71 @@ struct fft_plan {
   int pass_log[kMaxPasses];
   void *workspace;
   size_t workspace_bytes;
+  // Bluestein: convolution length 2^log_m; chirp (n values) and the filter
+  // spectrum (2^log_m values) in one allocation.
+  int log_m;
+  void *chirp;
+  void *filter;
+  size_t aux_bytes;
 };
+
+// Plans a 1D length that is not a power of two (the caller validated the
+// other arguments): the direct DFT for n <= kDirectDftMax, else Bluestein,
+// whose chirp and filter spectrum are computed here (on the legacy default
+// stream, waited for before returning).
+static fft_plan *plan_any_length(int64_t n, int64_t batch, int direction, int dtype) {
+  const size_t elem = dtype == FFT_C2C_F32 ? 8 : 16;
+  const int on_chip_max = dtype == FFT_C2C_F32 ? RowsMaxLog<float>::value : RowsMaxLog<double>::value;
+  fft_plan *p = new (std::nothrow) fft_plan;
+  if (!p) {
+    g_status = FFT_ERR_ALLOC;
+    return nullptr;
+  }
+  memset(p, 0, sizeof(*p));
+  p->n = n;
+  p->batch = batch;
+  p->elems = n;
+  p->rank = 1;
+  p->dims = 1;
+  p->direction = direction;
+  p->dtype = dtype;
+  if (n <= kDirectDftMax) {
+    p->kind = KIND_DFT;
+    return p;
+  }
+  const int log_m = ilog2_exact(2 * n - 1);
+  if (log_m > (dtype == FFT_C2C_F32 ? 27 : 26) || batch > ((int64_t)1 << 40) / ((int64_t)1 << log_m)) {
+    delete p;
+    g_status = FFT_ERR_UNSUPPORTED;
+    return nullptr;
+  }
+  p->kind = KIND_BLUESTEIN;
+  p->log_m = log_m;
+  const size_t M = (size_t)1 << log_m;
+  const size_t chirp_bytes = (((size_t)n * elem + 255) / 256) * 256;
+  p->aux_bytes = chirp_bytes + M * elem;
+  cudaError_t e = cudaMalloc(&p->chirp, p->aux_bytes);
+  if (e == cudaSuccess && log_m > on_chip_max) {
+    p->workspace_bytes = 2 * (size_t)batch * M * elem;
+    e = cudaMalloc(&p->workspace, p->workspace_bytes);
+  }
+  if (e == cudaSuccess) {
+    p->filter = static_cast<char *>(p->chirp) + chirp_bytes;
+    e = dtype == FFT_C2C_F32
+            ? bluestein_prepare_f32(n, log_m, direction, p->chirp, p->filter, p->workspace, 0)
+            : bluestein_prepare_f64(n, log_m, direction, p->chirp, p->filter, p->workspace, 0);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+  }
+  if (e != cudaSuccess) {
+    g_cuda_error = e;
+    if (p->workspace) cudaFree(p->workspace);
+    if (p->chirp) cudaFree(p->chirp);
+    delete p;
+    g_status = e == cudaErrorMemoryAllocation ? FFT_ERR_ALLOC : FFT_ERR_CUDA;
+    return nullptr;
+  }
+  return p;
+}
 
 extern "C" {
 
@@ -135,10 +203,7 @@ fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int
     g_status = FFT_ERR_INVALID_ARG;
     return nullptr;
   }
-  if (!is_pow2(n)) {
-    g_status = FFT_ERR_NOT_POW2;
-    return nullptr;
-  }
+  if (!is_pow2(n)) return plan_any_length(n, batch, direction, dtype);
   const int logn = ilog2_exact(n);
   const int on_chip_max = dtype == FFT_C2C_F32 ? RowsMaxLog<float>::value : RowsMaxLog<double>::value;
   const size_t elem = dtype == FFT_C2C_F32 ? 8 : 16;
@@ -249,10 +314,13 @@ fft_plan *fft_plan_create_nd(int rank, const int64_t *shape, int64_t batch, int 
 void fft_plan_destroy(fft_plan *plan) {
   if (!plan) return;
   if (plan->workspace) cudaFree(plan->workspace);
+  if (plan->chirp) cudaFree(plan->chirp);
   delete plan;
 }
 
-size_t fft_plan_workspace_bytes(const fft_plan *plan) { return plan ? plan->workspace_bytes : 0; }
+size_t fft_plan_workspace_bytes(const fft_plan *plan) {
+  return plan ? plan->workspace_bytes + plan->aux_bytes : 0;
+}
 
 }  // extern "C"
 
@@ -396,6 +464,30 @@ struct Schedule {
         return rows(in, out, batch);
       case KIND_ND:
         return run_nd(i, o);
+      case KIND_DFT: {
+        ++count;
+        if (dry) return cudaSuccess;
+        const double scale = p->direction > 0 ? 1.0 / (double)p->n : 1.0;
+        return p->dtype == FFT_C2C_F32
+                   ? dft_small_f32(in, out, (int)p->n, batch, p->direction, scale, st)
+                   : dft_small_f64(in, out, (int)p->n, batch, p->direction, scale, st);
+      }
+      case KIND_BLUESTEIN: {
+        const int on_chip = p->dtype == FFT_C2C_F32 ? RowsMaxLog<float>::value
+                                                    : RowsMaxLog<double>::value;
+        // Fused: one kernel.  Multi-pass: the forward and inverse passes of
+        // the convolution (its filter spectrum was computed at planning).
+        count += p->log_m <= on_chip ? 1 : 2 * convolve_passes(p->dtype, p->log_m);
+        if (dry) return cudaSuccess;
+        const double scale = p->direction > 0 ? 1.0 / (double)p->n : 1.0;
+        // The work arrays are reused chunk after chunk (one stream), so the
+        // plan's own base is used for any batch range.
+        return p->dtype == FFT_C2C_F32
+                   ? bluestein_exec_f32(in, out, p->n, batch, p->log_m, scale, p->chirp, p->filter,
+                                        p->workspace, st)
+                   : bluestein_exec_f64(in, out, p->n, batch, p->log_m, scale, p->chirp, p->filter,
+                                        p->workspace, st);
+      }
       case KIND_MULTI:
         return run_multi(i, o);
       default:

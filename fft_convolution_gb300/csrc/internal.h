@@ -81,6 +81,7 @@ cudaError_t launch_polymul(const long long *a, long long na, const long long *b,
 // pairs (shared real filter), 2 real rows one at a time.
 size_t convolve_scratch_bytes(long long batch, int h_per_row, int kind, int dtype, int log_len);
 int convolve_num_kernels(int kind, int dtype, int log_len);
+int convolve_passes(int dtype, int log_len);  // HBM passes per multi-pass transform
 cudaError_t launch_convolve(const void *x, long long nx, const void *h, long long nh, void *y,
                             long long batch, int h_per_row, int kind, int dtype, int log_len,
                             void *scratch, cudaStream_t st);
@@ -90,5 +91,20 @@ cudaError_t launch_convolve_f32(const void *x, long long nx, const void *h, long
 cudaError_t launch_convolve_f64(const void *x, long long nx, const void *h, long long nh, void *y,
                                 long long batch, int h_per_row, int kind, int log_len,
                                 void *scratch, cudaStream_t st);
+
+// Transforms of any length (anylen_*.cu): direct DFT (N <= 64) and
+// Bluestein through a power-of-two convolution of length 2^log_m.
+cudaError_t bluestein_prepare_f32(long long N, int log_m, int dir, void *w, void *B, void *ws,
+                                  cudaStream_t st);
+cudaError_t bluestein_prepare_f64(long long N, int log_m, int dir, void *w, void *B, void *ws,
+                                  cudaStream_t st);
+cudaError_t bluestein_exec_f32(const void *in, void *out, long long N, long long batch, int log_m,
+                               double scale, void *w, void *B, void *ws, cudaStream_t st);
+cudaError_t bluestein_exec_f64(const void *in, void *out, long long N, long long batch, int log_m,
+                               double scale, void *w, void *B, void *ws, cudaStream_t st);
+cudaError_t dft_small_f32(const void *in, void *out, int N, long long batch, int dir, double scale,
+                          cudaStream_t st);
+cudaError_t dft_small_f64(const void *in, void *out, int N, long long batch, int dir, double scale,
+                          cudaStream_t st);
 
 }  // namespace fftgb

@@ -50,7 +50,7 @@ extern "C" {
 /* Status codes. */
 #define FFT_OK 0
 #define FFT_ERR_INVALID_ARG 1 /* null pointer, size <= 0, bad enum value       */
-#define FFT_ERR_NOT_POW2 2    /* transform length is not a power of two         */
+#define FFT_ERR_NOT_POW2 2    /* a 2D / 3D side is not a power of two           */
 #define FFT_ERR_UNSUPPORTED 3 /* valid but not implemented (size / dtype / dims) */
 #define FFT_ERR_CUDA 4        /* CUDA runtime error or launch failure           */
 #define FFT_ERR_ALLOC 5       /* device allocation failed                       */
@@ -70,9 +70,10 @@ typedef struct fft_plan fft_plan;
 /*
  * fft_plan_create -- plan `batch` transforms of length n (dims = 1) or of
  * n x n images (dims = 2) in the given direction and element type.
- *   n         power of two, 1 <= n.  dims = 1: n <= 2^30 (fp32) / 2^29 (fp64)
- *             and batch * n * element size must fit the device.  dims = 2:
- *             n <= 2^14 (fp32) / 2^13 (fp64).
+ *   n         1 <= n.  dims = 1: a power of two up to 2^30 (fp32) / 2^29
+ *             (fp64), or any other length up to 2^26 (fp32) / 2^25 (fp64);
+ *             batch * n * element size must fit the device.  dims = 2: a
+ *             power of two up to 2^14 (fp32) / 2^13 (fp64).
  *   batch     number of independent transforms, >= 1.
  *   dims      1, or 2 for an n x n transform (= fft_plan_create_nd with
  *             shape {n, n}).
@@ -82,8 +83,15 @@ typedef struct fft_plan fft_plan;
  * thread block holds a whole transform on chip (one HBM read, one HBM write).
  * Longer 1D transforms run as 2-4 passes over HBM (a Stockham decomposition
  * into factors of at most 2^9) and need a workspace of batch * n elements,
- * allocated here on the current device.  Returns NULL on error
- * (fft_last_status(): INVALID_ARG, NOT_POW2, UNSUPPORTED, ALLOC).
+ * allocated here on the current device.  Lengths that are not powers of two
+ * ("FFT on GPU", sections FFT on GPU and Algorithm per signal Length): up to
+ * 64 the direct DFT, one kernel; beyond, Bluestein's algorithm -- a
+ * power-of-two convolution of length M >= 2n - 1 with a chirp -- whose chirp
+ * and filter spectrum are computed here (small kernels on the legacy default
+ * stream, waited for) and kept by the plan, plus 2 * batch * M work elements
+ * when M exceeds the on-chip length.  Returns NULL on error
+ * (fft_last_status(): INVALID_ARG, NOT_POW2 (2D only), UNSUPPORTED, ALLOC,
+ * CUDA).
  */
 fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int dtype);
 
@@ -105,7 +113,8 @@ fft_plan *fft_plan_create_nd(int rank, const int64_t *shape, int64_t batch, int 
  * sure no fft_exec of this plan is still running on the GPU. */
 void fft_plan_destroy(fft_plan *plan);
 
-/* Bytes of device workspace the plan owns (0 for single-kernel plans). */
+/* Bytes of device memory the plan owns (0 for single-kernel power-of-two
+ * plans). */
 size_t fft_plan_workspace_bytes(const fft_plan *plan);
 
 /* Number of kernels one fft_exec of this plan launches. */

@@ -60,8 +60,7 @@ def test_status_strings(fg):
     ((8, 1, 3, -1, 0), 1),        # dims
     ((8, 1, 1, 0, 0), 1),         # direction
     ((8, 1, 1, -1, 7), 1),        # dtype
-    ((12, 1, 1, -1, 0), 2),       # not a power of two
-    ((1000, 4, 2, 1, 1), 2),
+    ((1000, 4, 2, 1, 1), 2),      # 2D side not a power of two
     ((1 << 15, 1, 2, -1, 0), 3),  # 2D side beyond the on-chip limit
     ((1 << 14, 1, 2, -1, 1), 3),
     ((1 << 31, 1, 1, -1, 0), 3),  # 1D beyond the supported length
@@ -74,6 +73,7 @@ def test_plan_create_rejects(fg, args, status):
 
 @pytest.mark.parametrize("n,dims,dtype,kernels", [
     (1, 1, 0, 1), (1024, 1, 0, 1), (1 << 14, 1, 0, 1), (1 << 13, 1, 1, 1),
+    (12, 1, 0, 1), (63, 1, 1, 1),  # short non-power-of-two lengths: the direct DFT
     (64, 2, 0, 2), (2048, 2, 0, 2), (1 << 13, 2, 1, 2), (1, 2, 0, 1)])
 def test_on_chip_plans_need_no_device(fg, n, dims, dtype, kernels):
     # Single-kernel and 2D plans own no workspace, so they are created

@@ -247,6 +247,69 @@ def test_nd_rejects(fg):
         fg.fft_plan_create_nd(4, (2, 2, 2, 2), 1, -1, 0)
 
 
+# --- lengths that are not powers of two ---------------------------------------
+
+def bluestein_len(n):
+    return 1 << (2 * n - 2).bit_length()
+
+
+@pytest.mark.parametrize("dtype", [F32, F64])
+@pytest.mark.parametrize("n", [3, 5, 6, 12, 17, 33, 63])
+def test_direct_dft_short_lengths(fg, dtype, n):
+    batch = 37
+    x = workloads.normal_complex((batch, n), 5200 + n, NP[dtype])
+    y = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, dtype)
+    ref = np.stack([oracle.dft(r) for r in x.astype(np.complex128)])
+    assert rel_rows(y, ref).max() <= tol(dtype, 64)
+    z = run_plan(fg, y, n, batch, 1, fg.FFT_INVERSE, dtype, inplace=True)
+    assert rel_rows(z, x).max() <= 2 * tol(dtype, 64)
+
+
+@pytest.mark.parametrize("dtype,n", [(F32, 65), (F32, 100), (F32, 1000), (F32, 3001), (F32, 8191),
+                                     (F64, 65), (F64, 1000), (F64, 4095),
+                                     (F32, 10000), (F64, 5000), (F64, 9999)])
+def test_bluestein(fg, dtype, n):
+    # n <= 8191 fp32 / 4095 fp64 fuse the whole convolution on chip; the rest
+    # take the multi-pass path.
+    batch = 3
+    x = workloads.normal_complex((batch, n), 5300 + n, NP[dtype])
+    y = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, dtype)
+    ref = np.stack([oracle.dft(r) for r in x.astype(np.complex128)])
+    t = tol(dtype, bluestein_len(n))
+    assert rel_rows(y, ref).max() <= t
+    z = run_plan(fg, y, n, batch, 1, fg.FFT_INVERSE, dtype, inplace=True)
+    assert rel_rows(z, x).max() <= 2 * t
+
+
+def test_bluestein_large_prime_sampled(fg):
+    n = 1000003                     # prime; convolution length 2^21 (3 passes)
+    x = workloads.normal_complex((1, n), 54, np.complex64)
+    y = run_plan(fg, x, n, 1, 1, fg.FFT_FORWARD, F32)[0].astype(np.complex128)
+    ks = workloads.sample_indices(12, n, 55)
+    ref = oracle.dft_bins(x[0].astype(np.complex128), ks)
+    rms = np.linalg.norm(y) / np.sqrt(n)
+    assert np.linalg.norm(y[ks] - ref) / (np.sqrt(ks.size) * rms) <= tol(F32, 1 << 21)
+    x64 = x[0].astype(np.complex128)
+    assert abs(np.sum(np.abs(x64) ** 2) - np.sum(np.abs(y) ** 2) / n) / np.sum(np.abs(x64) ** 2) \
+        <= tol(F32, 1 << 21)
+
+
+def test_bluestein_in_host_chain(fg):
+    n, batch = 1500, 6
+    x = workloads.normal_complex((batch, n), 56, np.complex64)
+    pf = fg.Plan(n, batch, 1, fg.FFT_FORWARD, F32)
+    pi = fg.Plan(n, batch, 1, fg.FFT_INVERSE, F32)
+    h_in = torch.from_numpy(x).pin_memory()
+    h_out = torch.empty_like(h_in).pin_memory()
+    da, db = torch.empty_like(h_in).cuda(), torch.empty_like(h_in).cuda()
+    pf.chain_host([pi], h_in, h_out, da, db, 4)
+    torch.cuda.synchronize()
+    assert rel_rows(h_out.numpy(), x).max() <= 2 * tol(F32, bluestein_len(n))
+    assert pf.num_kernels == 1 and pf.workspace_bytes > 0
+    pf.close()
+    pi.close()
+
+
 # --- polynomial multiplication ----------------------------------------------
 
 @pytest.mark.parametrize("na,nb,batch", [(1, 1, 1), (1, 5, 2), (5, 7, 3), (16, 16, 4),
