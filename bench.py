@@ -64,16 +64,33 @@ def workload_info(name: str, pass_log: int = 9):
     if c["kind"] == "fft1d":
         elem = 8
         arr = n * batch * elem
-        passes = 1 if log2i(n) <= 14 else max(2, math.ceil(log2i(n) / pass_log))
         directions = 1 if name in ("c1", "c3") else 2
+        info = dict(kind="fft1d", n=n, batch=batch, directions=directions, array_bytes=arr,
+                    transforms_per_step=directions * batch, h2d=arr, d2h=arr,
+                    flops_per_step=directions * 5.0 * n * math.log2(max(n, 2)) * batch)
+        if n & (n - 1) == 0:
+            passes = 1 if log2i(n) <= 14 else max(2, math.ceil(log2i(n) / pass_log))
+        else:
+            # Bluestein: a length-M cyclic convolution per row, M = 2^ceil(log2(2n - 1));
+            # fused on chip (one read, one write) while M <= 2^14.
+            M = 1 << (2 * n - 2).bit_length()
+            passes = 1 if M <= 1 << 14 else None
+            info.update(bluestein_m=M, alu_flops_per_row=2 * 5.0 * M * log2i(M) + 6.0 * M
+                        + 12.0 * n)
+        info.update(passes=passes, bytes_per_step=directions * (passes or 1) * 2 * arr,
+                    ideal_bytes_per_step=directions * 2 * arr)
+        return info
+    if c["kind"] == "fftnd":
+        npts = 1
+        for v in c["shape"]:
+            npts *= v
+        arr = npts * batch * 8
+        passes = sum(1 for v in c["shape"] if v > 1)
         return dict(
-            kind="fft1d", n=n, batch=batch, passes=passes, directions=directions,
-            array_bytes=arr,
-            bytes_per_step=directions * passes * 2 * arr,
-            ideal_bytes_per_step=directions * 2 * arr,
-            flops_per_step=directions * 5.0 * n * log2i(n) * batch,
-            transforms_per_step=directions * batch,
-            h2d=arr, d2h=arr)
+            kind="fftnd", n=n, batch=batch, passes=passes, directions=2, array_bytes=arr,
+            bytes_per_step=2 * passes * 2 * arr, ideal_bytes_per_step=2 * 2 * arr,
+            flops_per_step=2 * 5.0 * npts * log2i(npts) * batch,
+            transforms_per_step=2 * batch, h2d=arr, d2h=arr)
     if c["kind"] == "fft2d":
         arr = n * n * batch * 8
         return dict(
@@ -181,6 +198,9 @@ KERNEL_SOURCES = {
     "c5": ["fft_device.cuh", "fft_pass.cuh", "fft_pass_tma.cuh", "fft_pass_f64.cu",
            "polymul.cu"],
     "conv1": ["fft_device.cuh", "fft_rows.cuh", "conv.cuh", "conv_f32.cu"],
+    "any1": ["fft_device.cuh", "fft_rows.cuh", "conv.cuh", "anylen.cuh", "anylen_f32.cu"],
+    "nd1": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_f32.cu", "fft_pass.cuh",
+            "fft_pass_tma.cuh", "fft_pass_f32.cu", "fft_plan.cu"],
 }
 
 
@@ -234,12 +254,14 @@ def cpu_oracle_sample(name: str, budget_s: float = 12.0):
         n = c["n"]
         if n <= 1 << 16:
             x = workloads.config_input(name, scale_batch=min(c["batch"], 64)).astype(np.complex128)
+            pow2 = n & (n - 1) == 0
+            fwd = oracle.fft if pow2 else oracle.dft          # any length: the direct DFT
             k = 0
             while time.perf_counter() - t0 < budget_s and k < x.shape[0] * 64:
                 r = x[k % x.shape[0]]
-                y = oracle.fft(r)
+                y = fwd(r)
                 if info["directions"] == 2:
-                    oracle.ifft(y)
+                    oracle.ifft(y) if pow2 else oracle.dft(y, +1)
                 k += 1
             done_units = k / c["batch"]
             sample = f"{k} of {c['batch']} transforms of N={n}" + \
@@ -264,6 +286,15 @@ def cpu_oracle_sample(name: str, budget_s: float = 12.0):
             k += 1
         done_units = k / c["batch"]
         sample = f"{k} of {c['batch']} images {n}x{n} (forward+inverse)"
+    elif info["kind"] == "fftnd":
+        vol = workloads.normal_complex((1,) + tuple(c["shape"]), c["seed"], np.complex128)
+        k = 0
+        while time.perf_counter() - t0 < budget_s and k < 4:
+            Y = oracle.fftn(vol, len(c["shape"]))
+            oracle.fftn(Y, len(c["shape"]), +1)
+            k += 1
+        done_units = k / c["batch"]
+        sample = f"{k} of {c['batch']} volumes {c['shape']} (forward+inverse)"
     elif info["kind"] == "conv":
         x, h = workloads.conv_signals(64, c["n"], c["nh"], c["seed"])
         k = 0
@@ -377,10 +408,11 @@ def run_gpu(args):
         z_d = torch.empty_like(x_d)
         dims = 2 if info["kind"] == "fft2d" else 1
         n, batch = c["n"], c["batch"]
-        pf = fg.Plan(n, batch, dims, fg.FFT_FORWARD, fg.FFT_C2C_F32)
+        shape = tuple(c["shape"]) if info["kind"] == "fftnd" else None
+        pf = fg.Plan(n, batch, dims, fg.FFT_FORWARD, fg.FFT_C2C_F32, shape=shape)
         plans = [pf]
         if info["directions"] == 2:
-            pi = fg.Plan(n, batch, dims, fg.FFT_INVERSE, fg.FFT_C2C_F32)
+            pi = fg.Plan(n, batch, dims, fg.FFT_INVERSE, fg.FFT_C2C_F32, shape=shape)
             plans.append(pi)
 
         def step(events=None):
@@ -438,13 +470,13 @@ def run_gpu(args):
     # Per-launch durations of the dominant kernel (the forward transform;
     # for 1-kernel plans that is one launch per exec).
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    inv_ms = [e[1].elapsed_time(e[2]) for e in ev] if info["kind"] in ("fft1d", "fft2d") and \
+    inv_ms = [e[1].elapsed_time(e[2]) for e in ev] if info["kind"] in ("fft1d", "fft2d", "fftnd") and \
         info["directions"] == 2 else []
 
     # End-to-end through the host-buffer entry point: pinned host input ->
     # device, transforms, device -> pinned host output, every step.
     e2e = None
-    if info["kind"] in ("fft1d", "fft2d") and not args.no_e2e:
+    if info["kind"] in ("fft1d", "fft2d", "fftnd") and not args.no_e2e:
         h_in = torch.from_numpy(x_h).pin_memory()
         h_out = torch.empty_like(h_in).pin_memory()
         e2e_steps = max(1, min(args.steps, 5))
@@ -539,6 +571,19 @@ def run_gpu(args):
                 "kernel": dom_name, "peak_source": peak_kind,
                 "launch_ms": round(dom_ms, 4),
                 "inverse_launch_ms": round(statistics.mean(inv_ms), 4) if inv_ms else None}
+    if info.get("bluestein_m") and info["passes"] == 1:
+        # Two length-M transforms per row of n points: the fused Bluestein kernel is bound by
+        # on-chip arithmetic, not HBM.  Peak: 152 SMs x 128 fp32 lanes x 2 flop (FMA) x 2070 MHz.
+        alu_peak = 152 * 128 * 2 * 2.070e9 / 1e12
+        flops = info["alu_flops_per_row"] * c["batch"]
+        alu = flops / (dom_ms * 1e-3) / 1e12
+        roofline.update(bound="alu", achieved=round(alu, 2), peak=round(alu_peak, 1),
+                        unit="TFLOP/s", frac=round(alu / alu_peak, 4),
+                        peak_source="derived (152 SM x 128 fp32 lanes x 2 x 2070 MHz)",
+                        kernel="conv_rows_kernel<float,%d,COMPLEX,1> (Bluestein, M=%d)"
+                        % (log2i(info["bluestein_m"]), info["bluestein_m"]),
+                        hbm_achieved_gbs=round(achieved, 1),
+                        flops_per_launch=flops)
 
     line = {
         "metric": "batched C2C FFT effective GB/s" if info["kind"] != "conv"
@@ -579,6 +624,17 @@ def run_gpu(args):
 def sized_input(name: str, c: dict):
     if not SIZE_OVERRIDE:
         return workloads.config_input(name)
+    if c["kind"] == "fftnd":
+        npts = 1
+        for v in c["shape"]:
+            npts *= v
+        arr = npts * batch * 8
+        passes = sum(1 for v in c["shape"] if v > 1)
+        return dict(
+            kind="fftnd", n=n, batch=batch, passes=passes, directions=2, array_bytes=arr,
+            bytes_per_step=2 * passes * 2 * arr, ideal_bytes_per_step=2 * 2 * arr,
+            flops_per_step=2 * 5.0 * npts * log2i(npts) * batch,
+            transforms_per_step=2 * batch, h2d=arr, d2h=arr)
     if c["kind"] == "fft2d":
         return workloads.normal_complex((c["batch"], c["n"], c["n"]), c["seed"])
     if name == "c3":
@@ -602,6 +658,10 @@ def workload_label(name: str) -> str:
     if name == "conv1":
         return ("real fp32 convolution, 32768 signals x 3072 samples with one 1025-tap filter "
                 "(transform length 4096)")
+    if name == "any1":
+        return "1D C2C forward+inverse, N=3000 (Bluestein, M=8192 on chip), batch 16384, fp32"
+    if name == "nd1":
+        return "3D C2C forward+inverse, 128x256x256, batch 4, fp32 (256 MiB)"
     return f"polymul, {c['batch']} pairs of 2^20 int64 coefficients, fp64 transforms of 2^21"
 
 
