@@ -87,6 +87,8 @@ def bind(lib):
         "oracle_polymul_fft": [_I64, i64, _I64, i64, _I64],
         "oracle_poly_eval_mod": [_I64, i64, ctypes.c_uint64, _U64],
         "oracle_convolve": [_D, i64, _D, i64, _D],
+        "oracle_rfft": [_D, i64, _D],
+        "oracle_irfft": [_D, i64, _D],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -295,3 +297,36 @@ def fftn(x, ndim: int, direction: int = -1) -> np.ndarray:
         moved = np.ascontiguousarray(np.moveaxis(y, axis, -1))
         y = np.moveaxis(fft(moved, direction), -1, axis)
     return np.ascontiguousarray(y)
+
+
+def rfft(x) -> np.ndarray:
+    """Half spectrum X_k, k = 0 .. n//2, of each real row (last axis) of x:
+    the first n//2 + 1 bins of its DFT (forward, unscaled)."""
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    n = x.shape[-1]
+    x2 = x.reshape(-1, n)
+    out = np.empty((x2.shape[0], n // 2 + 1), dtype=np.complex128)
+    lib = _load()
+    for r in range(x2.shape[0]):
+        row = np.ascontiguousarray(x2[r])
+        res = np.empty(n // 2 + 1, dtype=np.complex128)
+        _check(lib.oracle_rfft(_dp(row), n, _dp(res)), "rfft")
+        out[r] = res
+    return out.reshape(x.shape[:-1] + (n // 2 + 1,))
+
+
+def irfft(X, n: int) -> np.ndarray:
+    """Real rows of length n from half spectra X[..., n//2 + 1]: the inverse
+    transform (1/n) of the Hermitian extension, real part."""
+    X = _c128(X)
+    if X.shape[-1] != n // 2 + 1:
+        raise ValueError("half spectrum must have n//2 + 1 bins")
+    X2 = X.reshape(-1, X.shape[-1])
+    out = np.empty((X2.shape[0], n), dtype=np.float64)
+    lib = _load()
+    for r in range(X2.shape[0]):
+        row = np.ascontiguousarray(X2[r])
+        res = np.empty(n, dtype=np.float64)
+        _check(lib.oracle_irfft(_dp(row), n, _dp(res)), "irfft")
+        out[r] = res
+    return out.reshape(X.shape[:-1] + (n,))

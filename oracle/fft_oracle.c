@@ -395,3 +395,58 @@ int oracle_convolve(const double *x, int64_t nx, const double *h, int64_t nh, do
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------------------
+ * Transforms of real sequences.  For real x the DFT X_k = sum_n x_n omega^{kn}
+ * satisfies X_{N-k} = conj(X_k), so the bins k = 0 .. floor(N/2) hold all of
+ * it (the half spectrum).
+ *
+ *   oracle_rfft:  X_k, k = 0 .. floor(N/2), of the DFT of x_n + 0i
+ *                 (forward, unscaled).  x: n doubles; X: floor(n/2)+1 complex.
+ *   oracle_irfft: the inverse of a half spectrum: the full spectrum
+ *                 Y_k = X_k (k <= N/2), Y_k = conj(X_{N-k}) (k > N/2), its
+ *                 inverse transform with 1/N, and the real part of that.  The
+ *                 imaginary parts of X_0 and (even N) X_{N/2} add only
+ *                 imaginary terms to the result and so drop out.
+ *                 X: floor(n/2)+1 complex; x: n doubles.
+ * Power-of-two N goes through the recursive Cooley-Tukey, every other N
+ * through the direct DFT.
+ * ------------------------------------------------------------------------- */
+static int full_transform(const cplx *x, int64_t n, int sign, cplx *X) {
+    return is_pow2(n) ? oracle_fft((const double *)x, n, sign, (double *)X)
+                      : oracle_dft((const double *)x, n, sign, (double *)X);
+}
+
+int oracle_rfft(const double *x, int64_t n, double *X) {
+    if (n <= 0 || x == NULL || X == NULL) return -1;
+    cplx *z = (cplx *)malloc(sizeof(cplx) * (size_t)n);
+    cplx *Z = (cplx *)malloc(sizeof(cplx) * (size_t)n);
+    if (!z || !Z) {
+        free(z); free(Z);
+        return -2;
+    }
+    for (int64_t i = 0; i < n; ++i) z[i] = x[i] + 0.0 * I;
+    int rc = full_transform(z, n, -1, Z);
+    if (rc == 0) memcpy(X, Z, sizeof(cplx) * (size_t)(n / 2 + 1));
+    free(z);
+    free(Z);
+    return rc;
+}
+
+int oracle_irfft(const double *X, int64_t n, double *x) {
+    if (n <= 0 || x == NULL || X == NULL) return -1;
+    const cplx *half = (const cplx *)X;
+    cplx *Y = (cplx *)malloc(sizeof(cplx) * (size_t)n);
+    cplx *y = (cplx *)malloc(sizeof(cplx) * (size_t)n);
+    if (!Y || !y) {
+        free(Y); free(y);
+        return -2;
+    }
+    for (int64_t k = 0; k < n; ++k) Y[k] = 2 * k <= n ? half[k] : conj(half[n - k]);
+    int rc = full_transform(Y, n, +1, y);
+    if (rc == 0)
+        for (int64_t i = 0; i < n; ++i) x[i] = creal(y[i]) / (double)n;
+    free(Y);
+    free(y);
+    return rc;
+}

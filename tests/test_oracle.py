@@ -431,3 +431,83 @@ def test_direct_dft_closed_form_n3():
     w = -0.5 - 0.5j * np.sqrt(3.0)
     expect = [a[0] + a[1] + a[2], a[0] + w * a[1] + w * w * a[2], a[0] + w * w * a[1] + w * a[2]]
     assert np.allclose(oracle.dft(a), expect, atol=1e-14)
+
+
+# --- transforms of real sequences (half spectrum) ---------------------------
+# Derived from the DFT definition ("FFT on GPU", Discrete Fourier Transform)
+# for real samples, which the page's polynomial section uses (real
+# coefficients): X_{N-k} = conj(X_k).
+
+RLEN = [1, 2, 3, 4, 7, 8, 64, 100, 1024]
+
+
+@pytest.mark.parametrize("n", RLEN)
+def test_rfft_matches_numpy(n):
+    x = workloads.generator(1200 + n).standard_normal(size=(3, n))
+    X = oracle.rfft(x)
+    assert X.shape == (3, n // 2 + 1)
+    assert rel_l2(X, np.fft.rfft(x, axis=-1)) < 1e-13
+
+
+@pytest.mark.parametrize("n", RLEN)
+def test_irfft_matches_numpy(n):
+    g = workloads.generator(1300 + n)
+    X = g.standard_normal(size=(3, n // 2 + 1)) + 1j * g.standard_normal(size=(3, n // 2 + 1))
+    x = oracle.irfft(X, n)
+    assert x.shape == (3, n) and x.dtype == np.float64
+    assert rel_l2(x, np.fft.irfft(X, n, axis=-1)) < 1e-13
+
+
+def test_rfft_closed_forms():
+    a = np.array([0.75, -2.5])
+    assert np.allclose(oracle.rfft(a), [a[0] + a[1], a[0] - a[1]], atol=0)
+    x = np.array([1.0, 2.0, -3.0, 0.5])
+    # X_1 = x0 - i x1 - x2 + i x3, X_2 = x0 - x1 + x2 - x3.
+    expect = [x.sum(), x[0] - x[2] - 1j * (x[1] - x[3]), x[0] - x[1] + x[2] - x[3]]
+    assert np.allclose(oracle.rfft(x), expect, atol=1e-15)
+    d = np.zeros(16)
+    d[0] = 1.0
+    assert np.array_equal(oracle.rfft(d), np.ones(9))
+    c = np.full(16, -1.25)
+    expect = np.zeros(9, complex)
+    expect[0] = 16 * -1.25
+    assert np.allclose(oracle.rfft(c), expect, atol=1e-14)
+
+
+@pytest.mark.parametrize("n,f", [(64, 5), (1024, 300), (100, 7)])
+def test_rfft_of_cosine_is_one_bin(n, f):
+    # cos(2 pi f k / N) = (w^{-fk} + w^{fk}) / 2: N/2 at bin f, nothing else.
+    k = np.arange(n)
+    x = np.cos(2 * np.pi * ((f * k) % n) / n)
+    expect = np.zeros(n // 2 + 1, complex)
+    expect[f] = n / 2
+    assert np.abs(oracle.rfft(x) - expect).max() < 1e-11
+
+
+@pytest.mark.parametrize("n", [2, 8, 1024, 100, 63])
+def test_real_round_trip_and_parseval(n):
+    x = workloads.generator(1400 + n).standard_normal(size=n)
+    X = oracle.rfft(x)
+    assert rel_l2(oracle.irfft(X, n), x) < 1e-14
+    # Parseval with the mirrored bins counted twice.
+    w = np.full(X.size, 2.0)
+    w[0] = 1.0
+    if n % 2 == 0:
+        w[-1] = 1.0
+    assert abs(np.sum(w * np.abs(X) ** 2) / n - np.sum(x ** 2)) < 1e-11 * np.sum(x ** 2)
+
+
+@pytest.mark.parametrize("n", [8, 9, 1024])
+def test_irfft_drops_imaginary_dc_and_nyquist(n):
+    g = workloads.generator(1500 + n)
+    X = g.standard_normal(size=n // 2 + 1) + 1j * g.standard_normal(size=n // 2 + 1)
+    clean = X.copy()
+    clean[0] = clean[0].real
+    if n % 2 == 0:
+        clean[-1] = clean[-1].real
+    assert rel_l2(oracle.irfft(X, n), oracle.irfft(clean, n)) < 1e-15
+    if n % 2 == 1:
+        # Odd n has no Nyquist bin: the last bin's imaginary part counts.
+        bumped = clean.copy()
+        bumped[-1] += 1j
+        assert rel_l2(oracle.irfft(bumped, n), oracle.irfft(clean, n)) > 1e-3

@@ -56,6 +56,12 @@ MUTANTS = [
      "acc = (acc * tt + ar) % p;", "acc = (acc * tt + ar + 1) % p;"),
     ("convolution: filter index shifted",
      "cplx term = xc[i] * hc[k - i];", "cplx term = xc[i] * hc[k - i > 0 ? k - i - 1 : 0];"),
+    ("real transform: the last half-spectrum bin not written",
+     "memcpy(X, Z, sizeof(cplx) * (size_t)(n / 2 + 1));", "memcpy(X, Z, sizeof(cplx) * (size_t)(n / 2));"),
+    ("real inverse: mirrored bins not conjugated",
+     "Y[k] = 2 * k <= n ? half[k] : conj(half[n - k]);", "Y[k] = 2 * k <= n ? half[k] : half[n - k];"),
+    ("real inverse: 1/N dropped",
+     "x[i] = creal(y[i]) / (double)n;", "x[i] = creal(y[i]);"),
 ]
 
 
