@@ -80,6 +80,18 @@ def workload_info(name: str, pass_log: int = 9):
         info.update(passes=passes, bytes_per_step=directions * (passes or 1) * 2 * arr,
                     ideal_bytes_per_step=directions * 2 * arr)
         return info
+    if c["kind"] == "real":
+        # R2C then C2R: samples (4 B) read and bins (8 B, n/2 + 1 per row)
+        # written, then the reverse.
+        H = n // 2
+        pw2 = H > 0 and H & (H - 1) == 0 and n % 2 == 0
+        passes = 1 if pw2 and log2i(H) <= 14 else None
+        rb, cb = n * 4 * batch, (H + 1) * 8 * batch
+        return dict(
+            kind="real", n=n, batch=batch, passes=passes, directions=2, array_bytes=rb,
+            bytes_per_step=2 * (rb + cb), ideal_bytes_per_step=2 * (rb + cb),
+            flops_per_step=2 * 2.5 * n * math.log2(max(n, 2)) * batch,
+            transforms_per_step=2 * batch, h2d=rb, d2h=rb)
     if c["kind"] == "fftnd":
         npts = 1
         for v in c["shape"]:
@@ -199,6 +211,7 @@ KERNEL_SOURCES = {
            "polymul.cu"],
     "conv1": ["fft_device.cuh", "fft_rows.cuh", "conv.cuh", "conv_f32.cu"],
     "any1": ["fft_device.cuh", "fft_rows.cuh", "conv.cuh", "anylen.cuh", "anylen_f32.cu"],
+    "real1": ["fft_device.cuh", "fft_rows.cuh", "real.cuh", "real_f32.cu"],
     "nd1": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_f32.cu", "fft_pass.cuh",
             "fft_pass_tma.cuh", "fft_pass_f32.cu", "fft_plan.cu"],
 }
@@ -295,6 +308,14 @@ def cpu_oracle_sample(name: str, budget_s: float = 12.0):
             k += 1
         done_units = k / c["batch"]
         sample = f"{k} of {c['batch']} volumes {c['shape']} (forward+inverse)"
+    elif info["kind"] == "real":
+        x = workloads.normal_real((64, c["n"]), c["seed"], np.float64)
+        k = 0
+        while time.perf_counter() - t0 < budget_s and k < 64 * 64:
+            oracle.irfft(oracle.rfft(x[k % 64]), c["n"])
+            k += 1
+        done_units = k / c["batch"]
+        sample = f"{k} of {c['batch']} real rows of N={c['n']} (forward+inverse)"
     elif info["kind"] == "conv":
         x, h = workloads.conv_signals(64, c["n"], c["nh"], c["seed"])
         k = 0
@@ -401,6 +422,27 @@ def run_gpu(args):
                     events[1].record(stream)
             assert rc == 0, fg.fft_status_string(rc)
         kernels_per_step = fg.polymul_num_kernels(c["n"], c["n"])
+    elif info["kind"] == "real":
+        x_h = sized_input(name, c)
+        x_d = torch.from_numpy(x_h).to(dev)
+        n, batch = c["n"], c["batch"]
+        X_d = torch.empty(batch, n // 2 + 1, dtype=torch.complex64, device=dev)
+        y_d = torch.empty_like(x_d)
+        pf = fg.Plan(n, batch, 1, fg.FFT_FORWARD, fg.FFT_REAL_F32)
+        pi = fg.Plan(n, batch, 1, fg.FFT_INVERSE, fg.FFT_REAL_F32)
+        plans = [pf, pi]
+
+        def step(events=None):
+            if events is not None:
+                events[0].record(stream)
+            r0 = fg.fft_exec(pf.handle, x_d.data_ptr(), X_d.data_ptr(), sh)
+            if events is not None:
+                events[1].record(stream)
+            r1 = fg.fft_exec(pi.handle, X_d.data_ptr(), y_d.data_ptr(), sh)
+            if events is not None:
+                events[2].record(stream)
+            assert r0 == 0 and r1 == 0, (fg.fft_status_string(r0), fg.fft_status_string(r1))
+        kernels_per_step = pf.num_kernels + pi.num_kernels
     else:
         x_h = sized_input(name, c)
         x_d = torch.from_numpy(x_h).to(dev)
@@ -470,22 +512,25 @@ def run_gpu(args):
     # Per-launch durations of the dominant kernel (the forward transform;
     # for 1-kernel plans that is one launch per exec).
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    inv_ms = [e[1].elapsed_time(e[2]) for e in ev] if info["kind"] in ("fft1d", "fft2d", "fftnd") and \
+    inv_ms = [e[1].elapsed_time(e[2]) for e in ev] if info["kind"] in ("fft1d", "fft2d", "fftnd",
+                                                                        "real") and \
         info["directions"] == 2 else []
 
     # End-to-end through the host-buffer entry point: pinned host input ->
     # device, transforms, device -> pinned host output, every step.
     e2e = None
-    if info["kind"] in ("fft1d", "fft2d", "fftnd") and not args.no_e2e:
+    if info["kind"] in ("fft1d", "fft2d", "fftnd", "real") and not args.no_e2e:
         h_in = torch.from_numpy(x_h).pin_memory()
         h_out = torch.empty_like(h_in).pin_memory()
         e2e_steps = max(1, min(args.steps, 5))
         # Chunks of the batch stream through the device: uploads, transforms
         # and downloads of different chunks overlap (fft_exec_host_chain).
         chunk = max(1, c["batch"] // 16)
+        # Samples in x_d, spectra in X_d for the real round trip.
+        dev_b = X_d if info["kind"] == "real" else y_d
 
         def e2e_step():
-            plans[0].chain_host(plans[1:], h_in, h_out, x_d, y_d, chunk, stream)
+            plans[0].chain_host(plans[1:], h_in, h_out, x_d, dev_b, chunk, stream)
         e2e_step()
         torch.cuda.synchronize(dev)
         s0 = torch.cuda.Event(enable_timing=True)
@@ -558,6 +603,11 @@ def run_gpu(args):
         dom_ms = statistics.mean(fwd_ms)
         per_launch_bytes = info["bytes_per_step"]
         dom_name = "polymul (whole fused pipeline, %d kernels)" % kernels_per_step
+    elif info["kind"] == "real":
+        dom_ms = statistics.mean(fwd_ms)
+        per_launch_bytes = info["bytes_per_step"] / 2
+        dom_name = ("r2c_rows_kernel<float,%d>" % log2i(c["n"] // 2)) if info["passes"] == 1 \
+            else "forward real plan (%d kernels)" % plans[0].num_kernels
     else:
         dom_ms = statistics.mean(fwd_ms)
         per_launch_bytes = info["bytes_per_step"] / info["directions"]
@@ -586,8 +636,7 @@ def run_gpu(args):
                         flops_per_launch=flops)
 
     line = {
-        "metric": "batched C2C FFT effective GB/s" if info["kind"] != "conv"
-                  else "batched FFT convolution effective GB/s",
+        "metric": metric_name(info["kind"]),
         "value": round(value, 2),
         "unit": "GB/s",
         "n_gpus": world,
@@ -625,21 +674,22 @@ def sized_input(name: str, c: dict):
     if not SIZE_OVERRIDE:
         return workloads.config_input(name)
     if c["kind"] == "fftnd":
-        npts = 1
-        for v in c["shape"]:
-            npts *= v
-        arr = npts * batch * 8
-        passes = sum(1 for v in c["shape"] if v > 1)
-        return dict(
-            kind="fftnd", n=n, batch=batch, passes=passes, directions=2, array_bytes=arr,
-            bytes_per_step=2 * passes * 2 * arr, ideal_bytes_per_step=2 * 2 * arr,
-            flops_per_step=2 * 5.0 * npts * log2i(npts) * batch,
-            transforms_per_step=2 * batch, h2d=arr, d2h=arr)
+        return workloads.normal_complex((c["batch"],) + tuple(c["shape"]), c["seed"])
+    if c["kind"] == "real":
+        return workloads.normal_real((c["batch"], c["n"]), c["seed"])
     if c["kind"] == "fft2d":
         return workloads.normal_complex((c["batch"], c["n"], c["n"]), c["seed"])
     if name == "c3":
         return workloads.tones_plus_noise(c["n"], c["seed"]).reshape(1, -1)
     return workloads.normal_complex((c["batch"], c["n"]), c["seed"])
+
+
+def metric_name(kind: str) -> str:
+    if kind == "conv":
+        return "batched FFT convolution effective GB/s"
+    if kind == "real":
+        return "batched real FFT (R2C + C2R) effective GB/s"
+    return "batched C2C FFT effective GB/s"
 
 
 def workload_label(name: str) -> str:
@@ -658,6 +708,8 @@ def workload_label(name: str) -> str:
     if name == "conv1":
         return ("real fp32 convolution, 32768 signals x 3072 samples with one 1025-tap filter "
                 "(transform length 4096)")
+    if name == "real1":
+        return "1D real R2C+C2R, N=8192, batch 32768, fp32 (1 GiB of samples)"
     if name == "any1":
         return "1D C2C forward+inverse, N=3000 (Bluestein, M=8192 on chip), batch 16384, fp32"
     if name == "nd1":
@@ -691,8 +743,7 @@ def run_reference(args):
     ms_step = 1e3 * info["bytes_per_step"] / (value * 1e9)
     line = {
         "impl": "reference",
-        "metric": "batched C2C FFT effective GB/s" if info["kind"] != "conv"
-                  else "batched FFT convolution effective GB/s",
+        "metric": metric_name(info["kind"]),
         "value": round(value, 4),
         "unit": "GB/s",
         "n_gpus": world,

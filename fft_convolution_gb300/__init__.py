@@ -31,6 +31,8 @@ FFT_INVERSE = +1
 
 FFT_C2C_F32 = 0
 FFT_C2C_F64 = 1
+FFT_REAL_F32 = 2
+FFT_REAL_F64 = 3
 
 FFT_CONV_COMPLEX = 0
 FFT_CONV_REAL = 1
@@ -248,16 +250,39 @@ class Plan:
             total *= v
         return total
 
-    def exec(self, inp, out=None, stream=None):
-        """Run on device tensors (complex64 / complex128, contiguous)."""
+    @property
+    def real(self) -> bool:
+        return self.dtype in (FFT_REAL_F32, FFT_REAL_F64)
+
+    def io_spec(self):
+        """((input torch dtype, elements), (output torch dtype, elements))."""
         torch = _torch()
+        if not self.real:
+            t = torch.complex64 if self.dtype == FFT_C2C_F32 else torch.complex128
+            return (t, self.numel()), (t, self.numel())
+        rt, ct = ((torch.float32, torch.complex64) if self.dtype == FFT_REAL_F32
+                  else (torch.float64, torch.complex128))
+        samples = (rt, self.batch * self.n)
+        bins = (ct, self.batch * (self.n // 2 + 1))
+        return (samples, bins) if self.direction == FFT_FORWARD else (bins, samples)
+
+    def exec(self, inp, out=None, stream=None):
+        """Run on contiguous device tensors: complex64 / complex128 for
+        complex plans; float samples and complex half spectra (n // 2 + 1
+        bins per row) for real plans."""
+        torch = _torch()
+        (it, ni), (ot, no) = self.io_spec()
         if out is None:
-            out = torch.empty_like(inp)
+            if self.real:
+                shape = (self.batch, no // self.batch)
+                out = torch.empty(shape, dtype=ot, device=inp.device)
+            else:
+                out = torch.empty_like(inp)
         if not (inp.is_cuda and out.is_cuda and inp.is_contiguous() and out.is_contiguous()):
             raise ValueError("exec needs contiguous CUDA tensors")
-        if inp.numel() != self.numel() or out.numel() != self.numel():
-            raise ValueError(f"tensors must hold {self.numel()} elements")
-        if _dtype_code(inp) != self.dtype or _dtype_code(out) != self.dtype:
+        if inp.numel() != ni or out.numel() != no:
+            raise ValueError(f"tensors must hold {ni} and {no} elements")
+        if inp.dtype != it or out.dtype != ot:
             raise TypeError("tensor dtype does not match the plan")
         _check(fft_exec(self.handle, inp.data_ptr(), out.data_ptr(), _stream_handle(stream)),
                "fft_exec")
@@ -360,6 +385,42 @@ def convolve(x, h, out=None, stream=None):
     _check(fft_convolve(x2.data_ptr(), nx, h2.data_ptr(), nh, out.data_ptr(), batch, h_per_row,
                         kind, dtype, _stream_handle(stream)), "fft_convolve")
     return out.reshape(-1) if squeeze else out
+
+
+def rfft(x, out=None, stream=None):
+    """Half spectra (n // 2 + 1 bins) of the real rows along the last axis of
+    a contiguous float32 / float64 CUDA tensor."""
+    torch = _torch()
+    if x.dtype not in (torch.float32, torch.float64):
+        raise TypeError("rfft takes float32 or float64 samples")
+    n = x.shape[-1]
+    p = Plan(n, x.numel() // n, 1, FFT_FORWARD,
+             FFT_REAL_F32 if x.dtype == torch.float32 else FFT_REAL_F64)
+    try:
+        y = p.exec(x, out, stream)
+        return y.reshape(tuple(x.shape[:-1]) + (n // 2 + 1,))
+    finally:
+        if stream is None:
+            torch.cuda.current_stream().synchronize()
+        p.close()
+
+
+def irfft(X, n: int, out=None, stream=None):
+    """Real rows of length n from half spectra (n // 2 + 1 bins, complex64 /
+    complex128 CUDA tensor, last axis), scaled by 1/n."""
+    torch = _torch()
+    if X.shape[-1] != n // 2 + 1:
+        raise ValueError("the last axis must hold n // 2 + 1 bins")
+    dt = _dtype_code(X)
+    p = Plan(n, X.numel() // X.shape[-1], 1, FFT_INVERSE,
+             FFT_REAL_F32 if dt == FFT_C2C_F32 else FFT_REAL_F64)
+    try:
+        y = p.exec(X, out, stream)
+        return y.reshape(tuple(X.shape[:-1]) + (n,))
+    finally:
+        if stream is None:
+            torch.cuda.current_stream().synchronize()
+        p.close()
 
 
 def fftn(x, ndim: int, direction: int = FFT_FORWARD, out=None, stream=None):

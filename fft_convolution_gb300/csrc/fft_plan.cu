@@ -41,7 +41,16 @@ namespace {
 thread_local int g_status = FFT_OK;
 thread_local cudaError_t g_cuda_error = cudaSuccess;
 
-enum Kind { KIND_ROWS = 0, KIND_MULTI = 1, KIND_ND = 2, KIND_DFT = 3, KIND_BLUESTEIN = 4 };
+enum Kind {
+  KIND_ROWS = 0,
+  KIND_MULTI = 1,
+  KIND_ND = 2,
+  KIND_DFT = 3,
+  KIND_BLUESTEIN = 4,
+  KIND_REAL_ROWS = 5,  // real, N = 2H with H a power of two on chip: one kernel
+  KIND_REAL_EVEN = 6,  // real, other even N: complex plan of length N/2 + pre/post kernel
+  KIND_REAL_ODD = 7    // real, odd N: complex plan of length N + widen/narrow kernels
+};
 
 // Lengths that are not powers of two: the direct DFT up to this length,
 // Bluestein beyond.
@@ -130,7 +139,116 @@ struct fft_plan {
   void *chirp;
   void *filter;
   size_t aux_bytes;
+  // Real sequences (FFT_REAL_*; dtype then holds the matching complex type).
+  int real;
+  fft_plan *inner;     // the complex plan of KIND_REAL_EVEN / KIND_REAL_ODD
+  size_t ws_stride;    // workspace bytes per transform (batch ranges slice it)
+  void *rtw;           // split twiddle table of W_N (KIND_REAL_EVEN), in aux
+  int rtw_log_s;
+  int64_t rtw_nhi;
 };
+
+namespace {
+
+size_t complex_bytes(const fft_plan *p) { return p->dtype == FFT_C2C_F32 ? 8 : 16; }
+
+// Bytes of one transform's input and output.
+size_t in_tbytes(const fft_plan *p) {
+  if (!p->real) return (size_t)p->elems * complex_bytes(p);
+  return p->direction < 0 ? (size_t)p->n * (complex_bytes(p) / 2)
+                          : (size_t)(p->n / 2 + 1) * complex_bytes(p);
+}
+size_t out_tbytes(const fft_plan *p) {
+  if (!p->real) return (size_t)p->elems * complex_bytes(p);
+  return p->direction < 0 ? (size_t)(p->n / 2 + 1) * complex_bytes(p)
+                          : (size_t)p->n * (complex_bytes(p) / 2);
+}
+
+// Workspace bytes that belong to one transform (0: the plan's workspace is
+// reused whole by every batch range on one stream, as Bluestein's is).
+size_t ws_tbytes(const fft_plan *p) {
+  if (p->kind == KIND_MULTI) return (size_t)p->n * complex_bytes(p);
+  if (p->kind == KIND_REAL_EVEN || p->kind == KIND_REAL_ODD) return p->ws_stride;
+  return 0;
+}
+
+cudaError_t launch_real_rows(int dtype, int logh, int dir, const void *in, void *out,
+                             long long batch, cudaStream_t st) {
+  return dtype == FFT_C2C_F32 ? launch_real_rows_f32(logh, dir, in, out, batch, st)
+                              : launch_real_rows_f64(logh, dir, in, out, batch, st);
+}
+
+cudaError_t real_aux(int dtype, int op, const RealAuxArgs &a, cudaStream_t st) {
+  return dtype == FFT_C2C_F32 ? real_aux_f32(op, a, st) : real_aux_f64(op, a, st);
+}
+
+}  // namespace
+
+extern "C" void fft_plan_destroy(fft_plan *plan);
+
+// Plans `batch` transforms of real sequences of length n (the caller
+// validated the arguments; cdtype is the complex type of the samples'
+// precision).  N = 2H with H a power of two that fits on chip: one kernel per
+// direction.  Other even N: a complex plan of length H and a pre/post
+// kernel with a split twiddle table of W_N (computed here on the legacy
+// default stream, waited for).  Odd N: a complex plan of length N.
+static fft_plan *plan_real(int64_t n, int64_t batch, int direction, int cdtype) {
+  const size_t elem = cdtype == FFT_C2C_F32 ? 8 : 16;
+  const int on_chip_max = cdtype == FFT_C2C_F32 ? RowsMaxLog<float>::value : RowsMaxLog<double>::value;
+  fft_plan *p = new (std::nothrow) fft_plan;
+  if (!p) {
+    g_status = FFT_ERR_ALLOC;
+    return nullptr;
+  }
+  memset(p, 0, sizeof(*p));
+  p->n = n;
+  p->batch = batch;
+  p->elems = n;
+  p->rank = 1;
+  p->dims = 1;
+  p->direction = direction;
+  p->dtype = cdtype;
+  p->real = 1;
+  if (n % 2 == 0 && is_pow2(n) && ilog2_exact(n) - 1 <= on_chip_max) {
+    p->kind = KIND_REAL_ROWS;
+    p->logn = ilog2_exact(n) - 1;
+    return p;
+  }
+  const bool even = n % 2 == 0;
+  const int64_t inner_n = even ? n / 2 : n;
+  p->kind = even ? KIND_REAL_EVEN : KIND_REAL_ODD;
+  p->inner = fft_plan_create(inner_n, batch, 1, direction, cdtype);
+  if (!p->inner) {  // g_status says why
+    delete p;
+    return nullptr;
+  }
+  g_status = FFT_OK;
+  p->ws_stride = (size_t)inner_n * elem;
+  p->workspace_bytes = (size_t)batch * p->ws_stride;
+  cudaError_t e = cudaMalloc(&p->workspace, p->workspace_bytes);
+  if (e == cudaSuccess && even) {
+    const int64_t H = n / 2;
+    int log_s = 0;
+    while (((int64_t)1 << (2 * log_s)) < H + 1) ++log_s;
+    p->rtw_log_s = log_s;
+    p->rtw_nhi = (H >> log_s) + 1;
+    p->aux_bytes = (((size_t)1 << log_s) + (size_t)p->rtw_nhi) * elem;
+    e = cudaMalloc(&p->rtw, p->aux_bytes);
+    if (e == cudaSuccess) {
+      char *lo = static_cast<char *>(p->rtw);
+      RealAuxArgs a{nullptr, nullptr, n, 0, lo, lo + ((size_t)1 << log_s) * elem, log_s, p->rtw_nhi};
+      e = real_aux(cdtype, REAL_TABLES, a, 0);
+      if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+    }
+  }
+  if (e != cudaSuccess) {
+    g_cuda_error = e;
+    fft_plan_destroy(p);
+    g_status = e == cudaErrorMemoryAllocation ? FFT_ERR_ALLOC : FFT_ERR_CUDA;
+    return nullptr;
+  }
+  return p;
+}
 
 // Plans a 1D length that is not a power of two (the caller validated the
 // other arguments): the direct DFT for n <= kDirectDftMax, else Bluestein,
@@ -195,14 +313,20 @@ extern "C" {
 fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int dtype) {
   g_status = FFT_OK;
   if (dims == 2) {
+    if (dtype == FFT_REAL_F32 || dtype == FFT_REAL_F64) {
+      g_status = FFT_ERR_UNSUPPORTED;  // real transforms are 1D
+      return nullptr;
+    }
     const int64_t shape[2] = {n, n};
     return fft_plan_create_nd(2, shape, batch, direction, dtype);
   }
+  const bool real = dtype == FFT_REAL_F32 || dtype == FFT_REAL_F64;
   if (n <= 0 || batch <= 0 || dims != 1 || (direction != FFT_FORWARD && direction != FFT_INVERSE) ||
-      (dtype != FFT_C2C_F32 && dtype != FFT_C2C_F64)) {
+      (dtype != FFT_C2C_F32 && dtype != FFT_C2C_F64 && !real)) {
     g_status = FFT_ERR_INVALID_ARG;
     return nullptr;
   }
+  if (real) return plan_real(n, batch, direction, dtype == FFT_REAL_F32 ? FFT_C2C_F32 : FFT_C2C_F64);
   if (!is_pow2(n)) return plan_any_length(n, batch, direction, dtype);
   const int logn = ilog2_exact(n);
   const int on_chip_max = dtype == FFT_C2C_F32 ? RowsMaxLog<float>::value : RowsMaxLog<double>::value;
@@ -315,11 +439,14 @@ void fft_plan_destroy(fft_plan *plan) {
   if (!plan) return;
   if (plan->workspace) cudaFree(plan->workspace);
   if (plan->chirp) cudaFree(plan->chirp);
+  if (plan->rtw) cudaFree(plan->rtw);
+  if (plan->inner) fft_plan_destroy(plan->inner);
   delete plan;
 }
 
 size_t fft_plan_workspace_bytes(const fft_plan *plan) {
-  return plan ? plan->workspace_bytes + plan->aux_bytes : 0;
+  if (!plan) return 0;
+  return plan->workspace_bytes + plan->aux_bytes + fft_plan_workspace_bytes(plan->inner);
 }
 
 }  // extern "C"
@@ -331,9 +458,15 @@ struct Schedule {
   const fft_plan *p;
   cudaStream_t st;
   bool dry;
-  long long batch;  // transforms this run covers (a range of the plan's batch)
-  char *ws;         // the workspace slice of that range
+  long long batch;  // transforms this run covers: b0 .. b0 + batch - 1 of the plan's
+  long long b0;
   int count = 0;
+  char *ws = nullptr;  // the workspace slice of that range
+
+  Schedule(const fft_plan *p_, cudaStream_t st_, bool dry_, long long batch_, long long b0_)
+      : p(p_), st(st_), dry(dry_), batch(batch_), b0(b0_) {
+    if (p->workspace) ws = static_cast<char *>(p->workspace) + (size_t)b0 * ws_tbytes(p);
+  }
 
   size_t elem() const { return p->dtype == FFT_C2C_F32 ? 8 : 16; }
 
@@ -490,9 +623,54 @@ struct Schedule {
       }
       case KIND_MULTI:
         return run_multi(i, o);
+      case KIND_REAL_ROWS:
+        ++count;
+        return dry ? cudaSuccess : launch_real_rows(p->dtype, p->logn, p->direction, in, out, batch, st);
+      case KIND_REAL_EVEN:
+      case KIND_REAL_ODD:
+        return run_real(in, out);
       default:
         return cudaErrorInvalidValue;
     }
+  }
+
+  // Real sequences around the inner complex plan (same batch range).  Even
+  // N: forward = complex transform of the samples read as N/2 complex values
+  // into the workspace, then the post kernel; inverse = pre kernel into the
+  // workspace, then the complex inverse into `out`.  Odd N: samples widened
+  // into the workspace, transformed there in place, bins 0 .. N/2 copied out
+  // (forward); spectrum extended into the workspace, inverse in place, real
+  // parts copied out (inverse).
+  cudaError_t run_real(const void *in, void *out) {
+    Schedule inner(p->inner, st, dry, batch, b0);
+    const bool even = p->kind == KIND_REAL_EVEN;
+    const size_t elem = complex_bytes(p);
+    const char *lo = static_cast<const char *>(p->rtw);
+    const char *hi = lo ? lo + ((size_t)1 << p->rtw_log_s) * elem : nullptr;
+    const long long len = even ? p->n / 2 : p->n;
+    auto aux = [&](int op, const void *a_in, void *a_out) -> cudaError_t {
+      ++count;
+      if (dry) return cudaSuccess;
+      RealAuxArgs a{a_in, a_out, len, batch, lo, hi, p->rtw_log_s, p->rtw_nhi};
+      return real_aux(p->dtype, op, a, st);
+    };
+    cudaError_t e;
+    if (p->direction < 0) {
+      if (even) {
+        e = inner.run(in, ws);
+      } else {
+        if ((e = aux(REAL_WIDEN, in, ws)) != cudaSuccess) return e;
+        e = inner.run(ws, ws);
+      }
+      count += inner.count;
+      if (e != cudaSuccess) return e;
+      return aux(even ? REAL_POST : REAL_NARROW, ws, out);
+    }
+    if ((e = aux(even ? REAL_PRE : REAL_EXTEND, in, ws)) != cudaSuccess) return e;
+    e = even ? inner.run(ws, out) : inner.run(ws, ws);
+    count += inner.count;
+    if (e != cudaSuccess || even) return e;
+    return aux(REAL_PART, ws, out);
   }
 };
 
@@ -503,16 +681,16 @@ extern "C" {
 int fft_plan_num_kernels(const fft_plan *plan) {
   if (!plan) return 0;
   // Count an out-of-place execution (distinct dummy addresses).
-  Schedule s{plan, nullptr, true, plan->batch, static_cast<char *>(plan->workspace)};
+  Schedule s(plan, nullptr, true, plan->batch, 0);
   s.run(reinterpret_cast<const void *>(16), reinterpret_cast<void *>(32));
   return s.count;
 }
 
 int fft_exec(const fft_plan *p, const void *in, void *out, void *stream) {
   if (!p || !in || !out) return FFT_ERR_INVALID_ARG;
+  if (p->real && in == out) return FFT_ERR_INVALID_ARG;  // sizes differ: out of place only
   if (misaligned(in) || misaligned(out)) return FFT_ERR_MISALIGNED;
-  Schedule s{p, static_cast<cudaStream_t>(stream), false, p->batch,
-             static_cast<char *>(p->workspace)};
+  Schedule s(p, static_cast<cudaStream_t>(stream), false, p->batch, 0);
   cudaError_t e = s.run(in, out);
   if (e != cudaSuccess) return cuda_fail(e);
   return FFT_OK;
@@ -523,18 +701,16 @@ int fft_exec_host(const fft_plan *p, const void *host_in, void *host_out, void *
   if (!p || !dev_in || !dev_out) return FFT_ERR_INVALID_ARG;
   if (misaligned(dev_in) || misaligned(dev_out)) return FFT_ERR_MISALIGNED;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t elem = p->dtype == FFT_C2C_F32 ? 8 : 16;
-  const size_t count = (size_t)p->batch * (size_t)p->elems;
-  const size_t bytes = count * elem;
   cudaError_t e;
   if (host_in) {
-    e = cudaMemcpyAsync(dev_in, host_in, bytes, cudaMemcpyHostToDevice, st);
+    e = cudaMemcpyAsync(dev_in, host_in, (size_t)p->batch * in_tbytes(p), cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   int rc = fft_exec(p, dev_in, dev_out, stream);
   if (rc != FFT_OK) return rc;
   if (host_out) {
-    e = cudaMemcpyAsync(host_out, dev_out, bytes, cudaMemcpyDeviceToHost, st);
+    e = cudaMemcpyAsync(host_out, dev_out, (size_t)p->batch * out_tbytes(p), cudaMemcpyDeviceToHost,
+                        st);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return FFT_OK;
@@ -611,8 +787,8 @@ int fft_exec_host_chain(const fft_plan *const *plans, int nplans, const void *ho
   const fft_plan *p0 = plans[0];
   for (int k = 0; k < nplans; ++k) {
     const fft_plan *q = plans[k];
-    if (!q || q->elems != p0->elems || q->rank != p0->rank || q->n != p0->n ||
-        q->dtype != p0->dtype || q->batch != p0->batch)
+    // One batch; each plan takes what the previous one produces.
+    if (!q || q->batch != p0->batch || (k > 0 && in_tbytes(q) != out_tbytes(plans[k - 1])))
       return FFT_ERR_INVALID_ARG;
   }
   if (misaligned(dev_a) || misaligned(dev_b)) return FFT_ERR_MISALIGNED;
@@ -620,8 +796,14 @@ int fft_exec_host_chain(const fft_plan *const *plans, int nplans, const void *ho
   if (chunk > batch) chunk = batch;
   const long long nchunks = (batch + chunk - 1) / chunk;
   if (nchunks > 4096) return FFT_ERR_INVALID_ARG;
-  const size_t elem = p0->dtype == FFT_C2C_F32 ? 8 : 16;
-  const size_t tbytes = (size_t)p0->elems * elem;
+  // Every chunk's slices must start 16-byte aligned, like whole buffers.
+  for (int k = 0; k < nplans; ++k)
+    if (((size_t)chunk * in_tbytes(plans[k])) % 16 || ((size_t)chunk * out_tbytes(plans[k])) % 16 ||
+        ((size_t)chunk * ws_tbytes(plans[k])) % 16)
+      return FFT_ERR_MISALIGNED;
+  for (int k = 0; k < nplans; ++k)
+    if (plans[k]->real && dev_a == dev_b) return FFT_ERR_INVALID_ARG;  // real: out of place only
+  const size_t in_bytes0 = in_tbytes(p0), out_bytes_last = out_tbytes(plans[nplans - 1]);
 
   std::lock_guard<std::mutex> lock(g_pipe_mutex);
   HostPipe *hp = nullptr;
@@ -639,22 +821,22 @@ int fft_exec_host_chain(const fft_plan *const *plans, int nplans, const void *ho
   for (long long k = 0; k < nchunks; ++k) {
     const long long b0 = k * chunk;
     const long long cnt = batch - b0 < chunk ? batch - b0 : chunk;
-    const size_t off = (size_t)b0 * tbytes, bytes = (size_t)cnt * tbytes;
-    e = cudaMemcpyAsync(bufs[0] + off, static_cast<const char *>(host_in) + off, bytes,
-                        cudaMemcpyHostToDevice, hp->in);
+    e = cudaMemcpyAsync(bufs[0] + (size_t)b0 * in_bytes0,
+                        static_cast<const char *>(host_in) + (size_t)b0 * in_bytes0,
+                        (size_t)cnt * in_bytes0, cudaMemcpyHostToDevice, hp->in);
     if (e != cudaSuccess) return cuda_fail(e);
     cudaEventRecord(hp->loaded[k], hp->in);
     cudaStreamWaitEvent(hp->comp, hp->loaded[k], 0);
     for (int j = 0; j < nplans; ++j) {
       const fft_plan *q = plans[j];
-      char *ws = q->workspace ? static_cast<char *>(q->workspace) + off : nullptr;
-      Schedule s{q, hp->comp, false, cnt, ws};
-      e = s.run(bufs[j % 2] + off, bufs[(j + 1) % 2] + off);
+      Schedule s(q, hp->comp, false, cnt, b0);
+      e = s.run(bufs[j % 2] + (size_t)b0 * in_tbytes(q), bufs[(j + 1) % 2] + (size_t)b0 * out_tbytes(q));
       if (e != cudaSuccess) return cuda_fail(e);
     }
     cudaEventRecord(hp->done[k], hp->comp);
     cudaStreamWaitEvent(hp->out, hp->done[k], 0);
-    e = cudaMemcpyAsync(static_cast<char *>(host_out) + off, bufs[nplans % 2] + off, bytes,
+    e = cudaMemcpyAsync(static_cast<char *>(host_out) + (size_t)b0 * out_bytes_last,
+                        bufs[nplans % 2] + (size_t)b0 * out_bytes_last, (size_t)cnt * out_bytes_last,
                         cudaMemcpyDeviceToHost, hp->out);
     if (e != cudaSuccess) return cuda_fail(e);
   }

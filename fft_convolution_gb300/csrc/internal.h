@@ -107,4 +107,36 @@ cudaError_t dft_small_f32(const void *in, void *out, int N, long long batch, int
 cudaError_t dft_small_f64(const void *in, void *out, int N, long long batch, int dir, double scale,
                           cudaStream_t st);
 
+// Transforms of real sequences (real_*.cu).  On chip: N = 2H, H = 2^logh,
+// forward (dir < 0) batch x 2H reals -> batch x (H + 1) bins, inverse the
+// reverse with 1/N.
+cudaError_t launch_real_rows_f32(int logh, int dir, const void *in, void *out, long long batch,
+                                 cudaStream_t st);
+cudaError_t launch_real_rows_f64(int logh, int dir, const void *in, void *out, long long batch,
+                                 cudaStream_t st);
+// Kernels around a complex plan.  `len` is H for REAL_POST / REAL_PRE and
+// the real length N for the others; lo / hi / log_s / nhi describe the
+// split twiddle table of W_N (REAL_TABLES fills it).
+enum RealAuxOp {
+  REAL_TABLES = 0,  // lo[j] = W_N^j (j < 2^log_s), hi[i] = W_N^{i 2^log_s} (i < nhi)
+  REAL_POST = 1,    // Z (batch x H) -> X (batch x (H + 1))
+  REAL_PRE = 2,     // X (batch x (H + 1)) -> Z (batch x H)
+  REAL_WIDEN = 3,   // odd N: reals -> complex with imaginary part 0
+  REAL_NARROW = 4,  // odd N: bins 0 .. N/2 of each row
+  REAL_EXTEND = 5,  // odd N: half spectrum -> full Hermitian spectrum
+  REAL_PART = 6     // odd N: complex -> real parts
+};
+struct RealAuxArgs {
+  const void *in;
+  void *out;
+  long long len;
+  long long batch;
+  const void *lo;
+  const void *hi;
+  int log_s;
+  long long nhi;
+};
+cudaError_t real_aux_f32(int op, const RealAuxArgs &a, cudaStream_t st);
+cudaError_t real_aux_f64(int op, const RealAuxArgs &a, cudaStream_t st);
+
 }  // namespace fftgb

@@ -64,6 +64,22 @@ extern "C" {
 /* Element type. */
 #define FFT_C2C_F32 0 /* interleaved float  (re, im), 8 bytes  */
 #define FFT_C2C_F64 1 /* interleaved double (re, im), 16 bytes */
+/* Transforms of real sequences (1D).  A real row of n samples has the
+ * spectrum X_k = sum_j x_j e^{-2 pi i jk/n} with X_{n-k} = conj(X_k) ("FFT on
+ * GPU", section Discrete Fourier Transform, for real x), so the half
+ * spectrum X_0 .. X_{n/2} (n/2 + 1 bins, integer division) carries it all.
+ *   FFT_FORWARD (R2C): in  = batch rows of n reals (float / double),
+ *                      out = batch rows of n/2 + 1 interleaved complex bins.
+ *   FFT_INVERSE (C2R): in  = batch rows of n/2 + 1 bins,
+ *                      out = batch rows of n reals,
+ *                      x_j = (1/n) sum_{k<n} Y_k e^{+2 pi i jk/n} with Y the
+ *                      Hermitian extension (Y_k = X_k for k <= n/2,
+ *                      conj(X_{n-k}) above); the imaginary parts of X_0 and
+ *                      (even n) X_{n/2} are ignored.
+ * Rows are contiguous with no padding (a row of bins starts every
+ * (n/2 + 1) complex values).  Out of place only. */
+#define FFT_REAL_F32 2 /* float samples, interleaved float bins   */
+#define FFT_REAL_F64 3 /* double samples, interleaved double bins */
 
 typedef struct fft_plan fft_plan;
 
@@ -78,7 +94,16 @@ typedef struct fft_plan fft_plan;
  *   dims      1, or 2 for an n x n transform (= fft_plan_create_nd with
  *             shape {n, n}).
  *   direction FFT_FORWARD or FFT_INVERSE.
- *   dtype     FFT_C2C_F32 or FFT_C2C_F64.
+ *   dtype     FFT_C2C_F32 or FFT_C2C_F64; or FFT_REAL_F32 / FFT_REAL_F64
+ *             (dims = 1 only, else UNSUPPORTED) for real sequences, any
+ *             n >= 1: n = 2H with H a power of two up to 2^14 (fp32) /
+ *             2^13 (fp64) runs as one kernel per direction (the samples
+ *             read as H complex values, a length-H transform on chip and
+ *             the split into the half spectrum in the same block); other
+ *             even n as a complex plan of length n/2 plus one kernel that
+ *             splits or merges the spectrum over HBM (workspace batch * n/2
+ *             complex); odd n as a complex plan of length n (workspace
+ *             batch * n complex).
  * Lengths up to 2^14 (fp32) / 2^13 (fp64) run as one kernel in which one
  * thread block holds a whole transform on chip (one HBM read, one HBM write).
  * Longer 1D transforms run as 2-4 passes over HBM (a Stockham decomposition
@@ -123,9 +148,11 @@ int fft_plan_num_kernels(const fft_plan *plan);
 /*
  * fft_exec -- run the planned transforms.
  *   in, out   device pointers to batch-contiguous interleaved complex data
- *             of the plan's type, 16-byte aligned (else FFT_ERR_MISALIGNED).
- *             in == out (in place) is allowed; other overlaps are not.
- *             `in` is only read unless in == out.
+ *             of the plan's type (for FFT_REAL_* plans: reals and half
+ *             spectra as described there), 16-byte aligned (else
+ *             FFT_ERR_MISALIGNED).  in == out (in place) is allowed for
+ *             complex plans (FFT_ERR_INVALID_ARG for real ones); other
+ *             overlaps are not.  `in` is only read unless in == out.
  *   stream    a cudaStream_t (NULL = the legacy default stream).
  * Enqueues the kernels and returns; no synchronisation.
  */
@@ -137,7 +164,8 @@ int fft_exec(const fft_plan *plan, const void *in, void *out, void *stream);
  * transform dev_in -> dev_out; if host_out is not NULL, copy
  * dev_out -> host_out.  Host buffers should be pinned for the copies to be
  * asynchronous.  dev_in / dev_out are caller-owned device buffers of the
- * plan's full size (they may be equal).  Allocates nothing.
+ * plan's full input / output size (they may be equal for complex plans).
+ * Allocates nothing.
  */
 int fft_exec_host(const fft_plan *plan, const void *host_in, void *host_out, void *dev_in,
                   void *dev_out, void *stream);
@@ -149,12 +177,18 @@ int fft_exec_host(const fft_plan *plan, const void *host_in, void *host_out, voi
  * different chunks overlap.  For each chunk: copy host_in -> dev_a, run
  * plans[0] dev_a -> dev_b, plans[1] dev_b -> dev_a, ..., copy the last
  * result (dev_a if nplans is even, dev_b if odd) -> host_out.
- *   plans     nplans >= 1 plans with the same n, dims, dtype and batch.
+ *   plans     nplans >= 1 plans with the same batch, each taking as input
+ *             what the previous one produces (same bytes per transform:
+ *             e.g. an R2C plan followed by the C2R plan of the same n).
  *   host_in, host_out  host buffers of the full batch (pinned for the copies
  *             to overlap); host_in is only read.
- *   dev_a, dev_b       caller-owned device buffers of the full batch,
- *             16-byte aligned; both are overwritten.
- *   chunk     transforms per chunk (>= 1; at most 4096 chunks).
+ *   dev_a, dev_b       caller-owned device buffers, each large enough for
+ *             the full batch of every input or output placed in it,
+ *             16-byte aligned; both are overwritten; distinct when a real
+ *             plan is in the chain (else FFT_ERR_INVALID_ARG).
+ *   chunk     transforms per chunk (>= 1; at most 4096 chunks); every
+ *             chunk's slice of every buffer must start 16-byte aligned
+ *             (else FFT_ERR_MISALIGNED).
  * Ordered after the work already on `stream`; `stream` waits for the last
  * download, so the call is asynchronous on `stream` like fft_exec.  Uses
  * three internal non-blocking streams and per-chunk events, created on the

@@ -116,3 +116,24 @@ def test_polymul_and_debug_argument_checks(fg):
     assert fg.fft_debug_radix2_pass(16, 32, 8, 0, 0, None) == fg.FFT_ERR_INVALID_ARG
     assert fg.fft_debug_radix2_pass(16, 32, 8, 2, 5, None) == fg.FFT_ERR_INVALID_ARG
     assert fg.fft_debug_radix2_pass(24, 32, 8, 2, 0, None) == fg.FFT_ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("n,dtype", [(2, 2), (8, 2), (4096, 2), (1 << 15, 2), (1 << 14, 3), (2, 3)])
+def test_on_chip_real_plans_need_no_device(fg, n, dtype):
+    # n = 2H with H a power of two on chip: one kernel each way, no workspace.
+    for direction in (-1, 1):
+        h = fg._lib.fft_plan_create(n, 5, 1, direction, dtype)
+        assert h, fg.fft_last_status()
+        assert fg.fft_plan_num_kernels(h) == 1
+        assert fg.fft_plan_workspace_bytes(h) == 0
+        fg.fft_plan_destroy(h)
+
+
+def test_real_plan_argument_checks(fg):
+    assert not fg._lib.fft_plan_create(64, 1, 2, -1, fg.FFT_REAL_F32)
+    assert fg.fft_last_status() == fg.FFT_ERR_UNSUPPORTED
+    h = fg._lib.fft_plan_create(64, 1, 1, -1, fg.FFT_REAL_F32)
+    assert h
+    assert fg.fft_exec(h, 16, 16, None) == fg.FFT_ERR_INVALID_ARG  # in place
+    assert fg.fft_exec(h, 16 + 8, 32, None) == fg.FFT_ERR_MISALIGNED
+    fg.fft_plan_destroy(h)

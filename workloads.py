@@ -27,6 +27,8 @@ Workloads (sizes and distributions):
   and im i.i.d. standard normal; forward then inverse.
 * ``nd1``: 4 volumes of 128 x 256 x 256 fp32 complex (256 MiB), standard
   normal; 3D forward then inverse.
+* ``real1``: 32768 real fp32 rows of 8192 samples (1 GiB), standard normal;
+  half spectrum (R2C) then back (C2R).
 """
 from __future__ import annotations
 
@@ -41,6 +43,7 @@ CONFIGS = {
     "conv1": dict(kind="conv", n=3072, nh=1025, batch=32768, dtype="f32", seed=6),
     "any1": dict(kind="fft1d", n=3000, batch=16384, dtype="f32", seed=7),
     "nd1": dict(kind="fftnd", n=256, shape=(128, 256, 256), batch=4, dtype="f32", seed=8),
+    "real1": dict(kind="real", n=8192, batch=32768, dtype="f32", seed=9),
 }
 
 
@@ -74,6 +77,14 @@ def normal_complex(shape, seed: int, dtype=np.complex64) -> np.ndarray:
         re = g.standard_normal(size=shape)
         im = g.standard_normal(size=shape)
     return _complex(re, im, dtype)
+
+
+def normal_real(shape, seed: int, dtype=np.float32) -> np.ndarray:
+    """i.i.d. standard normal real samples (drawn in the target precision)."""
+    g = generator(seed)
+    if np.dtype(dtype) == np.float32:
+        return g.standard_normal(size=shape, dtype=np.float32)
+    return g.standard_normal(size=shape).astype(dtype)
 
 
 def tone_params(n: int, seed: int, ntones: int = 16):
@@ -150,6 +161,8 @@ def config_input(name: str, scale_batch: int | None = None):
         return normal_complex((batch, c["n"]), c["seed"])
     if name == "nd1":
         return normal_complex((batch,) + tuple(c["shape"]), c["seed"])
+    if name == "real1":
+        return normal_real((batch, c["n"]), c["seed"])
     raise KeyError(name)
 
 
