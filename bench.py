@@ -58,6 +58,13 @@ def config_of(name: str) -> dict:
     return c
 
 
+def smooth_2357(n: int) -> bool:
+    for f in (2, 3, 5, 7):
+        while n % f == 0:
+            n //= f
+    return n == 1
+
+
 def workload_info(name: str, pass_log: int = 9):
     c = config_of(name)
     n, batch = c["n"], c["batch"]
@@ -70,6 +77,9 @@ def workload_info(name: str, pass_log: int = 9):
                     flops_per_step=directions * 5.0 * n * math.log2(max(n, 2)) * batch)
         if n & (n - 1) == 0:
             passes = 1 if log2i(n) <= 14 else max(2, math.ceil(log2i(n) / pass_log))
+        elif smooth_2357(n) and 64 < n <= 12288:
+            passes = 1    # mixed radix on chip: one read, one write
+            info.update(mixed=True)
         else:
             # Bluestein: a length-M cyclic convolution per row, M = 2^ceil(log2(2n - 1));
             # fused on chip (one read, one write) while M <= 2^14.
@@ -210,7 +220,8 @@ KERNEL_SOURCES = {
     "c5": ["fft_device.cuh", "fft_pass.cuh", "fft_pass_tma.cuh", "fft_pass_f64.cu",
            "polymul.cu"],
     "conv1": ["fft_device.cuh", "fft_rows.cuh", "conv.cuh", "conv_f32.cu"],
-    "any1": ["fft_device.cuh", "fft_rows.cuh", "conv.cuh", "anylen.cuh", "anylen_f32.cu"],
+    "any1": ["fft_device.cuh", "mixed.cuh", "mixed_f32.cu", "fft_plan.cu"],
+    "any2": ["fft_device.cuh", "fft_rows.cuh", "conv.cuh", "anylen.cuh", "anylen_f32.cu"],
     "real1": ["fft_device.cuh", "fft_rows.cuh", "real.cuh", "real_f32.cu"],
     "nd1": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_f32.cu", "fft_pass.cuh",
             "fft_pass_tma.cuh", "fft_pass_f32.cu", "fft_plan.cu"],
@@ -613,6 +624,8 @@ def run_gpu(args):
         per_launch_bytes = info["bytes_per_step"] / info["directions"]
         dom_name = ("fft_rows_kernel<float,%d,-1>" % log2i(c["n"])) if info["passes"] == 1 and \
             info["kind"] == "fft1d" else "forward plan (%d kernels)" % plans[0].num_kernels
+        if info.get("mixed"):
+            dom_name = "mixed_rows_kernel<float,-1> (N=%d)" % c["n"]
     achieved = per_launch_bytes / (dom_ms * 1e-3) / 1e9
     tr = committed_traffic(name)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -711,7 +724,9 @@ def workload_label(name: str) -> str:
     if name == "real1":
         return "1D real R2C+C2R, N=8192, batch 32768, fp32 (1 GiB of samples)"
     if name == "any1":
-        return "1D C2C forward+inverse, N=3000 (Bluestein, M=8192 on chip), batch 16384, fp32"
+        return "1D C2C forward+inverse, N=3000 = 2^3 3 5^3 (mixed radix on chip), batch 16384, fp32"
+    if name == "any2":
+        return "1D C2C forward+inverse, N=3001 prime (Bluestein, M=8192 on chip), batch 16384, fp32"
     if name == "nd1":
         return "3D C2C forward+inverse, 128x256x256, batch 4, fp32 (256 MiB)"
     return f"polymul, {c['batch']} pairs of 2^20 int64 coefficients, fp64 transforms of 2^21"

@@ -8,6 +8,7 @@
 // the caller's stream (1 kernel for on-chip lengths, 2 for 2D, 2-4 for long
 // 1D transforms) and never synchronises.
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -49,7 +50,8 @@ enum Kind {
   KIND_BLUESTEIN = 4,
   KIND_REAL_ROWS = 5,  // real, N = 2H with H a power of two on chip: one kernel
   KIND_REAL_EVEN = 6,  // real, other even N: complex plan of length N/2 + pre/post kernel
-  KIND_REAL_ODD = 7    // real, odd N: complex plan of length N + widen/narrow kernels
+  KIND_REAL_ODD = 7,   // real, odd N: complex plan of length N + widen/narrow kernels
+  KIND_MIXED = 8       // N = 2^a 3^b 5^c 7^d (not a power of two) on chip
 };
 
 // Lengths that are not powers of two: the direct DFT up to this length,
@@ -146,6 +148,9 @@ struct fft_plan {
   void *rtw;           // split twiddle table of W_N (KIND_REAL_EVEN), in aux
   int rtw_log_s;
   int64_t rtw_nhi;
+  // Mixed radix: the stages and their forward twiddle table (in aux).
+  MixedStages ms;
+  void *mtw;
 };
 
 namespace {
@@ -250,10 +255,75 @@ static fft_plan *plan_real(int64_t n, int64_t batch, int direction, int cdtype) 
   return p;
 }
 
+// The stages of a mixed-radix plan of length n: the odd factors first (3s,
+// then 5s, then 7s: short blocks m while the stride N/R is odd), then the
+// power of two as one 2, 4 or 8 and radix-16 stages.  False if n has a prime
+// factor above 7 or needs more than 16 stages.
+static bool mixed_stages(int64_t n, int elem, MixedStages *ms) {
+  int radix[64], k = 0, a = 0;
+  int64_t r = n;
+  while (r % 2 == 0) {
+    r /= 2;
+    ++a;
+  }
+  const int odd[3] = {3, 5, 7};
+  for (int f : odd)
+    while (r % f == 0 && k < 64) {
+      r /= f;
+      radix[k++] = f;
+    }
+  if (r != 1) return false;
+  if (a % 4) radix[k++] = 1 << (a % 4);
+  for (int j = 0; j < a / 4; ++j) radix[k++] = 16;
+  if (k > 16) return false;
+  memset(ms, 0, sizeof(*ms));
+  ms->N = (int)n;
+  ms->nstages = k;
+  int m = 1, off = 0;
+  for (int j = 0; j < k; ++j) {
+    ms->radix[j] = radix[j];
+    ms->m[j] = m;
+    ms->tw_off[j] = off;
+    off += (radix[j] - 1) * m;
+    m *= radix[j];
+  }
+  // Transforms per block: about 2048 values, both buffers within 48 KB.
+  int F = n < 2048 ? (int)(2048 / n) : 1;
+  while (F > 1 && 2 * (size_t)F * n * elem > 48 * 1024) --F;
+  ms->F = F;
+  return true;
+}
+
+// Forward twiddles of every mixed-radix stage, W_{R m}^{p u} at
+// tw_off + (u - 1) m + p, computed in double precision with the exponent
+// reduced mod R m, rounded once to the element type.
+static void mixed_twiddles(const MixedStages &ms, bool f64, void *host) {
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int k = 0; k < ms.nstages; ++k) {
+    const int R = ms.radix[k], m = ms.m[k];
+    const int64_t RM = (int64_t)R * m;
+    for (int u = 1; u < R; ++u)
+      for (int p = 0; p < m; ++p) {
+        const int64_t e = ((int64_t)p * u) % RM;
+        const double ang = two_pi * (double)e / (double)RM;
+        const size_t at = (size_t)ms.tw_off[k] + (size_t)(u - 1) * m + p;
+        if (f64) {
+          static_cast<double *>(host)[2 * at] = cos(ang);
+          static_cast<double *>(host)[2 * at + 1] = -sin(ang);
+        } else {
+          static_cast<float *>(host)[2 * at] = (float)cos(ang);
+          static_cast<float *>(host)[2 * at + 1] = (float)-sin(ang);
+        }
+      }
+  }
+}
+
 // Plans a 1D length that is not a power of two (the caller validated the
-// other arguments): the direct DFT for n <= kDirectDftMax, else Bluestein,
-// whose chirp and filter spectrum are computed here (on the legacy default
-// stream, waited for before returning).
+// other arguments): the direct DFT for n <= kDirectDftMax; mixed radix on
+// chip for longer lengths whose prime factors are 2, 3, 5, 7 (up to
+// kMixedMaxF32 / kMixedMaxF64); Bluestein for the rest, whose chirp and
+// filter spectrum are computed here (on the legacy default stream, waited
+// for before returning).
 static fft_plan *plan_any_length(int64_t n, int64_t batch, int direction, int dtype) {
   const size_t elem = dtype == FFT_C2C_F32 ? 8 : 16;
   const int on_chip_max = dtype == FFT_C2C_F32 ? RowsMaxLog<float>::value : RowsMaxLog<double>::value;
@@ -272,6 +342,29 @@ static fft_plan *plan_any_length(int64_t n, int64_t batch, int direction, int dt
   p->dtype = dtype;
   if (n <= kDirectDftMax) {
     p->kind = KIND_DFT;
+    return p;
+  }
+  if (n <= (dtype == FFT_C2C_F32 ? kMixedMaxF32 : kMixedMaxF64) &&
+      mixed_stages(n, (int)elem, &p->ms)) {
+    p->kind = KIND_MIXED;
+    const MixedStages &ms = p->ms;
+    const int last = ms.nstages - 1;
+    const size_t entries = (size_t)ms.tw_off[last] + (size_t)(ms.radix[last] - 1) * ms.m[last];
+    p->aux_bytes = (entries > 0 ? entries : 1) * elem;
+    void *host = malloc(p->aux_bytes);
+    cudaError_t e = host ? cudaMalloc(&p->mtw, p->aux_bytes) : cudaErrorMemoryAllocation;
+    if (e == cudaSuccess) {
+      mixed_twiddles(ms, dtype == FFT_C2C_F64, host);
+      e = cudaMemcpy(p->mtw, host, entries * elem, cudaMemcpyHostToDevice);
+    }
+    free(host);
+    if (e != cudaSuccess) {
+      g_cuda_error = e;
+      if (p->mtw) cudaFree(p->mtw);
+      delete p;
+      g_status = e == cudaErrorMemoryAllocation ? FFT_ERR_ALLOC : FFT_ERR_CUDA;
+      return nullptr;
+    }
     return p;
   }
   const int log_m = ilog2_exact(2 * n - 1);
@@ -440,6 +533,7 @@ void fft_plan_destroy(fft_plan *plan) {
   if (plan->workspace) cudaFree(plan->workspace);
   if (plan->chirp) cudaFree(plan->chirp);
   if (plan->rtw) cudaFree(plan->rtw);
+  if (plan->mtw) cudaFree(plan->mtw);
   if (plan->inner) fft_plan_destroy(plan->inner);
   delete plan;
 }
@@ -623,6 +717,12 @@ struct Schedule {
       }
       case KIND_MULTI:
         return run_multi(i, o);
+      case KIND_MIXED:
+        ++count;
+        if (dry) return cudaSuccess;
+        return p->dtype == FFT_C2C_F32
+                   ? mixed_exec_f32(in, out, batch, p->ms, p->mtw, p->direction, st)
+                   : mixed_exec_f64(in, out, batch, p->ms, p->mtw, p->direction, st);
       case KIND_REAL_ROWS:
         ++count;
         return dry ? cudaSuccess : launch_real_rows(p->dtype, p->logn, p->direction, in, out, batch, st);

@@ -107,6 +107,25 @@ cudaError_t dft_small_f32(const void *in, void *out, int N, long long batch, int
 cudaError_t dft_small_f64(const void *in, void *out, int N, long long batch, int dir, double scale,
                           cudaStream_t st);
 
+// Mixed-radix on-chip transforms (mixed_*.cu): stage k has radix radix[k]
+// (2, 3, 4, 5, 7, 8 or 16) and block length m[k] (the product of the
+// radices before it); its forward twiddles W_{R m}^{p u} sit at
+// tw_off[k] + (u - 1) m + p of the plan's table.  A block holds F transforms.
+struct MixedStages {
+  int N;
+  int nstages;
+  int F;
+  int radix[16];
+  int m[16];
+  int tw_off[16];
+};
+constexpr int kMixedMaxF32 = 12288;  // 2 buffers of N values within 192 KB of shared memory
+constexpr int kMixedMaxF64 = 6144;
+cudaError_t mixed_exec_f32(const void *in, void *out, long long batch, const MixedStages &ms,
+                           const void *tw, int dir, cudaStream_t st);
+cudaError_t mixed_exec_f64(const void *in, void *out, long long batch, const MixedStages &ms,
+                           const void *tw, int dir, cudaStream_t st);
+
 // Transforms of real sequences (real_*.cu).  On chip: N = 2H, H = 2^logh,
 // forward (dir < 0) batch x 2H reals -> batch x (H + 1) bins, inverse the
 // reverse with 1/N.

@@ -1,0 +1,174 @@
+// mixed.cuh -- on-chip mixed-radix transforms for lengths N = 2^a 3^b 5^c 7^d.
+//
+// "FFT on GPU" (section Algorithm per signal Length) names the mixed-radix
+// FFT for lengths such as 12 = 3 * 4 beside the power-of-two one.  The
+// Stockham stage of "Stockham FFT Butterfly Algorithm in Parallel GLSL"
+// (section Stockham) holds for any radix R once the block length m is the
+// product of the radices before it:
+//   out[q R m + p + v m] = sum_{u<R} W_R^{u v} (W_{R m}^{p u} in[i + u N/R]),
+//   i = q m + p,  p < m,  q < N/(R m),
+// natural order in and out.  A block holds F whole transforms in shared
+// memory (two buffers, one barrier per stage); every stage is a loop of its
+// 256 threads over the F * N/R butterflies, each loading its R inputs,
+// applying the stage twiddles (read from a per-plan table of the forward
+// roots, conjugated for the inverse), running the radix-R DFT in registers
+// and storing the R outputs.  Radices 2, 4, 8, 16 use the power-of-two
+// register DFTs; 3, 5, 7 pair x_u with x_{R-u}:
+//   X_v = x_0 + sum_{u<=(R-1)/2} [(x_u + x_{R-u}) cos(2 pi uv/R)
+//                                 + DIR i (x_u - x_{R-u}) sin(2 pi uv/R)],
+// and X_{R-v} the same with the sine term negated.
+#pragma once
+
+#include "fft_device.cuh"
+#include "internal.h"
+
+namespace fftgb {
+namespace {
+
+constexpr int kMixedThreads = 256;
+
+// cos(2 pi k / R), sin(2 pi k / R) for R = 3, 5, 7, k <= (R-1)/2.
+__host__ __device__ constexpr double odd_cos(int R, int k) {
+  return R == 3   ? -0.5
+         : R == 5 ? (k == 1 ? 0.309016994374947424102293417182819059
+                            : -0.809016994374947424102293417182819059)
+                  : (k == 1   ? 0.623489801858733530525004884004239811
+                     : k == 2 ? -0.222520933956314404288902564496794759
+                              : -0.900968867902419126236102319507445051);
+}
+__host__ __device__ constexpr double odd_sin(int R, int k) {
+  return R == 3   ? 0.866025403784438646763723170752936183
+         : R == 5 ? (k == 1 ? 0.951056516295153572116439333379382143
+                            : 0.587785252292473129168705954639072769)
+                  : (k == 1   ? 0.781831482468029808708444526674057750
+                     : k == 2 ? 0.974927912181823607018131682993931217
+                              : 0.433883739117558120475768332848358755);
+}
+
+// In-register DFT of odd prime length R (3, 5, 7), natural order.
+template <int R, int DIR, typename V> __device__ __forceinline__ void dft_odd(V *x) {
+  using T = decltype(V::x);
+  constexpr int H = (R - 1) / 2;
+  V s[H], d[H];
+  V x0 = x[0];
+  V sum = x[0];
+#pragma unroll
+  for (int u = 1; u <= H; ++u) {
+    s[u - 1] = c_add(x[u], x[R - u]);
+    d[u - 1] = c_sub(x[u], x[R - u]);
+    sum = c_add(sum, s[u - 1]);
+  }
+  x[0] = sum;
+#pragma unroll
+  for (int v = 1; v <= H; ++v) {
+    V a = x0, b = make_c<V>((T)0, (T)0);
+#pragma unroll
+    for (int u = 1; u <= H; ++u) {
+      const int k = (u * v) % R;  // constant once the loops are unrolled
+      const int kk = k <= H ? k : R - k;
+      const T c = (T)odd_cos(R, kk);
+      const T sn = (T)(k <= H ? odd_sin(R, kk) : -odd_sin(R, kk));
+      a.x += s[u - 1].x * c;
+      a.y += s[u - 1].y * c;
+      b.x += d[u - 1].x * sn;
+      b.y += d[u - 1].y * sn;
+    }
+    // DIR i b
+    const V ib = DIR < 0 ? make_c<V>(b.y, -b.x) : make_c<V>(-b.y, b.x);
+    x[v] = c_add(a, ib);
+    x[R - v] = c_sub(a, ib);
+  }
+}
+
+template <int R, int DIR, typename V> __device__ __forceinline__ void dft_any(V *x) {
+  if constexpr (R == 3 || R == 5 || R == 7) dft_odd<R, DIR>(x);
+  else dft_reg<R, DIR>(x);
+}
+
+// One stage of radix R over the F transforms of a block: src and dst hold
+// F transforms of N values each (stride N).  tw: this stage's table,
+// W_{Rm}^{p u} (forward) at (u - 1) m + p.
+template <int R, int DIR, typename V>
+__device__ __forceinline__ void mixed_stage(const V *src, V *dst, int N, int m, const V *tw, int F) {
+  const int nb = N / R;
+  const int total = F * nb;
+  for (int b = threadIdx.x; b < total; b += kMixedThreads) {
+    const int f = b / nb, i = b - f * nb;
+    const int q = i / m, p = i - q * m;
+    const V *s = src + f * N;
+    V y[R];
+#pragma unroll
+    for (int u = 0; u < R; ++u) y[u] = s[i + u * nb];
+    if (m > 1) {
+#pragma unroll
+      for (int u = 1; u < R; ++u) {
+        const V w = __ldg(tw + (u - 1) * m + p);
+        y[u] = DIR < 0 ? c_mul(y[u], w) : make_c<V>(y[u].x * w.x + y[u].y * w.y,
+                                                      y[u].y * w.x - y[u].x * w.y);
+      }
+    }
+    dft_any<R, DIR>(y);
+    V *d = dst + f * N + q * R * m + p;
+#pragma unroll
+    for (int v = 0; v < R; ++v) d[v * m] = y[v];
+  }
+}
+
+template <typename T, int DIR>
+__global__ void __launch_bounds__(kMixedThreads)
+    mixed_rows_kernel(const vec2_t<T> *in, vec2_t<T> *out, long long batch, MixedStages ms,
+                      const vec2_t<T> *__restrict__ tw, T scale) {
+  using V = vec2_t<T>;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  V *cur = reinterpret_cast<V *>(smem_raw);
+  V *nxt = cur + ms.F * ms.N;
+  const long long row0 = (long long)blockIdx.x * ms.F;
+  const long long left = batch - row0;
+  const int rows = left < ms.F ? (int)left : ms.F;
+  const int count = rows * ms.N;  // valid values of this block
+  const V *src = in + row0 * ms.N;
+  for (int e = threadIdx.x; e < ms.F * ms.N; e += kMixedThreads)
+    cur[e] = e < count ? src[e] : make_c<V>((T)0, (T)0);
+  __syncthreads();
+  for (int k = 0; k < ms.nstages; ++k) {
+    const V *t = tw + ms.tw_off[k];
+    switch (ms.radix[k]) {
+      case 2: mixed_stage<2, DIR>(cur, nxt, ms.N, ms.m[k], t, ms.F); break;
+      case 3: mixed_stage<3, DIR>(cur, nxt, ms.N, ms.m[k], t, ms.F); break;
+      case 4: mixed_stage<4, DIR>(cur, nxt, ms.N, ms.m[k], t, ms.F); break;
+      case 5: mixed_stage<5, DIR>(cur, nxt, ms.N, ms.m[k], t, ms.F); break;
+      case 7: mixed_stage<7, DIR>(cur, nxt, ms.N, ms.m[k], t, ms.F); break;
+      case 8: mixed_stage<8, DIR>(cur, nxt, ms.N, ms.m[k], t, ms.F); break;
+      default: mixed_stage<16, DIR>(cur, nxt, ms.N, ms.m[k], t, ms.F); break;
+    }
+    __syncthreads();  // dst complete; src free for the next stage's output
+    V *tmp = cur;
+    cur = nxt;
+    nxt = tmp;
+  }
+  V *dst = out + row0 * ms.N;
+  for (int e = threadIdx.x; e < count; e += kMixedThreads) dst[e] = c_scale(cur[e], scale);
+}
+
+template <typename T>
+cudaError_t mixed_exec_t(const void *in, void *out, long long batch, const MixedStages &ms,
+                         const void *tw, int dir, cudaStream_t st) {
+  using V = vec2_t<T>;
+  const size_t smem = 2 * (size_t)ms.F * ms.N * sizeof(V);
+  auto kern = dir < 0 ? mixed_rows_kernel<T, -1> : mixed_rows_kernel<T, 1>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  const long long grid = (batch + ms.F - 1) / ms.F;
+  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const T scale = dir < 0 ? (T)1 : (T)(1.0 / ms.N);
+  kern<<<(unsigned)grid, kMixedThreads, smem, st>>>(static_cast<const V *>(in),
+                                                    static_cast<V *>(out), batch, ms,
+                                                    static_cast<const V *>(tw), scale);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace fftgb

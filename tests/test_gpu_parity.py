@@ -265,9 +265,9 @@ def test_direct_dft_short_lengths(fg, dtype, n):
     assert rel_rows(z, x).max() <= 2 * tol(dtype, 64)
 
 
-@pytest.mark.parametrize("dtype,n", [(F32, 65), (F32, 100), (F32, 1000), (F32, 3001), (F32, 8191),
-                                     (F64, 65), (F64, 1000), (F64, 4095),
-                                     (F32, 10000), (F64, 5000), (F64, 9999)])
+@pytest.mark.parametrize("dtype,n", [(F32, 65), (F32, 130), (F32, 1009), (F32, 3001), (F32, 8191),
+                                     (F64, 65), (F64, 1009), (F64, 4095),
+                                     (F32, 10007), (F64, 5003), (F64, 9999)])
 def test_bluestein(fg, dtype, n):
     # n <= 8191 fp32 / 4095 fp64 fuse the whole convolution on chip; the rest
     # take the multi-pass path.
@@ -279,6 +279,39 @@ def test_bluestein(fg, dtype, n):
     assert rel_rows(y, ref).max() <= t
     z = run_plan(fg, y, n, batch, 1, fg.FFT_INVERSE, dtype, inplace=True)
     assert rel_rows(z, x).max() <= 2 * t
+
+
+# Lengths whose prime factors are 2, 3, 5, 7 (above the direct-DFT range):
+# mixed-radix stages on chip, one kernel.
+@pytest.mark.parametrize("dtype,n", [(F32, 72), (F32, 96), (F32, 100), (F32, 120), (F32, 210),
+                                     (F32, 243), (F32, 343), (F32, 625), (F32, 1000), (F32, 3000),
+                                     (F32, 5040), (F32, 11025), (F32, 12288),
+                                     (F64, 72), (F64, 210), (F64, 1000), (F64, 3000), (F64, 6144)])
+def test_mixed_radix(fg, dtype, n):
+    batch = 3 if n > 2048 else 37   # ragged against the transforms per block
+    x = workloads.normal_complex((batch, n), 5400 + n, NP[dtype])
+    p = fg.Plan(n, batch, 1, fg.FFT_FORWARD, dtype)
+    assert p.num_kernels == 1
+    p.close()
+    y = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, dtype)
+    rows = range(batch) if n <= 3000 else range(2)
+    ref = np.stack([oracle.dft(x[r].astype(np.complex128)) for r in rows])
+    assert rel_rows(y[list(rows)], ref).max() <= tol(dtype, n)
+    z = run_plan(fg, y, n, batch, 1, fg.FFT_INVERSE, dtype, inplace=True)
+    assert rel_rows(z, x).max() <= 2 * tol(dtype, n)
+    refi = np.stack([oracle.dft(y[r].astype(np.complex128), +1) for r in rows])
+    assert rel_rows(z[list(rows)], refi).max() <= tol(dtype, n)
+
+
+def test_mixed_radix_limits_route_to_bluestein(fg):
+    # Beyond the on-chip mixed-radix length (fp32 12288) a smooth length takes
+    # Bluestein: 12800 = 2^9 5^2.
+    n = 12800
+    x = workloads.normal_complex((2, n), 5500, np.complex64)
+    y = run_plan(fg, x, n, 2, 1, fg.FFT_FORWARD, F32)
+    ks = workloads.sample_indices(16, n, 5501)
+    ref = oracle.dft_bins(x[0].astype(np.complex128), ks)
+    assert np.linalg.norm(y[0][ks] - ref) / np.linalg.norm(ref) <= tol(F32, bluestein_len(n))
 
 
 def test_bluestein_large_prime_sampled(fg):

@@ -23,8 +23,9 @@ Workloads (sizes and distributions):
 * ``conv1``: 32768 real fp32 signals of 3072 samples, i.i.d. standard
   normal, convolved with one shared 1025-tap real filter (standard normal);
   outputs have 4096 samples (transform length 4096).
-* ``any1``: 16384 transforms of 3000 points (not a power of two), fp32, re
-  and im i.i.d. standard normal; forward then inverse.
+* ``any1``: 16384 transforms of 3000 = 2^3 3 5^3 points, fp32, re and im
+  i.i.d. standard normal; forward then inverse.
+* ``any2``: the same with the prime length 3001.
 * ``nd1``: 4 volumes of 128 x 256 x 256 fp32 complex (256 MiB), standard
   normal; 3D forward then inverse.
 * ``real1``: 32768 real fp32 rows of 8192 samples (1 GiB), standard normal;
@@ -42,6 +43,7 @@ CONFIGS = {
     "c5": dict(kind="polymul", n=1 << 20, batch=64, dtype="f64", seed=5),
     "conv1": dict(kind="conv", n=3072, nh=1025, batch=32768, dtype="f32", seed=6),
     "any1": dict(kind="fft1d", n=3000, batch=16384, dtype="f32", seed=7),
+    "any2": dict(kind="fft1d", n=3001, batch=16384, dtype="f32", seed=10),
     "nd1": dict(kind="fftnd", n=256, shape=(128, 256, 256), batch=4, dtype="f32", seed=8),
     "real1": dict(kind="real", n=8192, batch=32768, dtype="f32", seed=9),
 }
@@ -157,7 +159,7 @@ def config_input(name: str, scale_batch: int | None = None):
         return poly_coeffs((batch, c["n"]), c["seed"])
     if name == "conv1":
         return conv_signals(batch, c["n"], c["nh"], c["seed"])
-    if name == "any1":
+    if name in ("any1", "any2"):
         return normal_complex((batch, c["n"]), c["seed"])
     if name == "nd1":
         return normal_complex((batch,) + tuple(c["shape"]), c["seed"])
