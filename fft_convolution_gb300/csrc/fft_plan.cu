@@ -279,11 +279,16 @@ static bool mixed_stages(int64_t n, int elem, MixedStages *ms) {
   memset(ms, 0, sizeof(*ms));
   ms->N = (int)n;
   ms->nstages = k;
+  auto magic = [](int64_t d) -> unsigned {
+    return d > 1 ? (unsigned)(((uint64_t)1 << 32) / (uint64_t)d + 1) : 0u;
+  };
   int m = 1, off = 0;
   for (int j = 0; j < k; ++j) {
     ms->radix[j] = radix[j];
     ms->m[j] = m;
     ms->tw_off[j] = off;
+    ms->nb_magic[j] = magic(n / radix[j]);
+    ms->m_magic[j] = magic(m);
     off += (radix[j] - 1) * m;
     m *= radix[j];
   }

@@ -118,6 +118,10 @@ struct MixedStages {
   int radix[16];
   int m[16];
   int tw_off[16];
+  // floor(2^32 / d) + 1 for d = N / radix[k] and d = m[k] (0 when d = 1):
+  // floor(x / d) = umulhi(x, magic) while x * d < 2^32.
+  unsigned nb_magic[16];
+  unsigned m_magic[16];
 };
 constexpr int kMixedMaxF32 = 12288;  // 2 buffers of N values within 192 KB of shared memory
 constexpr int kMixedMaxF64 = 6144;

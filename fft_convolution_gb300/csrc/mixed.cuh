@@ -8,8 +8,9 @@
 //   out[q R m + p + v m] = sum_{u<R} W_R^{u v} (W_{R m}^{p u} in[i + u N/R]),
 //   i = q m + p,  p < m,  q < N/(R m),
 // natural order in and out.  A block holds F whole transforms in shared
-// memory (two buffers, one barrier per stage); every stage is a loop of its
-// 256 threads over the F * N/R butterflies, each loading its R inputs,
+// memory (loaded with asynchronous copies; two buffers, one barrier per
+// stage; the last stage writes global memory); every stage is a loop of its 256 threads
+// over the F * N/R butterflies, each loading its R inputs,
 // applying the stage twiddles (read from a per-plan table of the forward
 // roots, conjugated for the inverse), running the radix-R DFT in registers
 // and storing the R outputs.  Radices 2, 4, 8, 16 use the power-of-two
@@ -85,16 +86,40 @@ template <int R, int DIR, typename V> __device__ __forceinline__ void dft_any(V 
   else dft_reg<R, DIR>(x);
 }
 
+// floor(x / d) from the host-computed magic of d (exact while x * d < 2^32;
+// x < F N / 2 and d <= N keep every use far below that).
+__device__ __forceinline__ int div_magic(int x, int d, unsigned magic) {
+  return d == 1 ? x : (int)__umulhi((unsigned)x, magic);
+}
+
+// Asynchronous global -> shared copy of one element (8 or 16 bytes), and
+// the wait for all of this thread's copies.
+template <typename V> __device__ __forceinline__ void cp_async_elem(V *dst, const V *src) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+  if constexpr (sizeof(V) == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;\n" ::: "memory");
+}
+
 // One stage of radix R over the F transforms of a block: src and dst hold
 // F transforms of N values each (stride N).  tw: this stage's table,
-// W_{Rm}^{p u} (forward) at (u - 1) m + p.
-template <int R, int DIR, typename V>
-__device__ __forceinline__ void mixed_stage(const V *src, V *dst, int N, int m, const V *tw, int F) {
+// W_{Rm}^{p u} (forward) at (u - 1) m + p.  The last stage writes the
+// block's valid rows (`rows` of them) straight to global memory with the
+// scale; the others go from one shared buffer to the other.
+template <int R, int DIR, bool LAST, typename V>
+__device__ __forceinline__ void mixed_stage(const V *src, V *dst, const MixedStages &ms, int k,
+                                            const V *tw, int rows, decltype(V::x) scale) {
+  using T = decltype(V::x);
+  const int N = ms.N, m = ms.m[k];
   const int nb = N / R;
-  const int total = F * nb;
+  const int total = ms.F * nb;
   for (int b = threadIdx.x; b < total; b += kMixedThreads) {
-    const int f = b / nb, i = b - f * nb;
-    const int q = i / m, p = i - q * m;
+    const int f = div_magic(b, nb, ms.nb_magic[k]), i = b - f * nb;
+    const int q = div_magic(i, m, ms.m_magic[k]), p = i - q * m;
     const V *s = src + f * N;
     V y[R];
 #pragma unroll
@@ -109,8 +134,31 @@ __device__ __forceinline__ void mixed_stage(const V *src, V *dst, int N, int m, 
     }
     dft_any<R, DIR>(y);
     V *d = dst + f * N + q * R * m + p;
+    if (LAST) {
+      if (f < rows) {
 #pragma unroll
-    for (int v = 0; v < R; ++v) d[v * m] = y[v];
+        for (int v = 0; v < R; ++v) d[v * m] = c_scale(y[v], scale);
+      }
+    } else {
+#pragma unroll
+      for (int v = 0; v < R; ++v) d[v * m] = y[v];
+    }
+  }
+}
+
+template <int DIR, bool LAST, typename V>
+__device__ __forceinline__ void mixed_stage_any(const V *src, V *dst, const MixedStages &ms,
+                                                int k, const V *tw, int rows,
+                                                decltype(V::x) scale) {
+  const V *t = tw + ms.tw_off[k];
+  switch (ms.radix[k]) {
+    case 2: mixed_stage<2, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
+    case 3: mixed_stage<3, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
+    case 4: mixed_stage<4, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
+    case 5: mixed_stage<5, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
+    case 7: mixed_stage<7, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
+    case 8: mixed_stage<8, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
+    default: mixed_stage<16, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
   }
 }
 
@@ -125,29 +173,29 @@ __global__ void __launch_bounds__(kMixedThreads)
   const long long row0 = (long long)blockIdx.x * ms.F;
   const long long left = batch - row0;
   const int rows = left < ms.F ? (int)left : ms.F;
-  const int count = rows * ms.N;  // valid values of this block
+  // The block's rows into shared memory with asynchronous copies (all in
+  // flight at once; rows beyond the batch as zeros), the stages between the
+  // two shared buffers (one barrier each: a stage's output is complete and
+  // its input buffer free for the next output), the last stage to global
+  // memory.  (Persistent blocks prefetching the next rows into a third
+  // buffer measured slower: one block fewer per SM.)
+  const int count = rows * ms.N;
   const V *src = in + row0 * ms.N;
-  for (int e = threadIdx.x; e < ms.F * ms.N; e += kMixedThreads)
-    cur[e] = e < count ? src[e] : make_c<V>((T)0, (T)0);
+  for (int e = threadIdx.x; e < ms.F * ms.N; e += kMixedThreads) {
+    if (e < count) cp_async_elem(cur + e, src + e);
+    else cur[e] = make_c<V>((T)0, (T)0);
+  }
+  cp_async_wait_all();
   __syncthreads();
-  for (int k = 0; k < ms.nstages; ++k) {
-    const V *t = tw + ms.tw_off[k];
-    switch (ms.radix[k]) {
-      case 2: mixed_stage<2, DIR>(cur, nxt, ms.N, ms.m[k], t, ms.F); break;
-      case 3: mixed_stage<3, DIR>(cur, nxt, ms.N, ms.m[k], t, ms.F); break;
-      case 4: mixed_stage<4, DIR>(cur, nxt, ms.N, ms.m[k], t, ms.F); break;
-      case 5: mixed_stage<5, DIR>(cur, nxt, ms.N, ms.m[k], t, ms.F); break;
-      case 7: mixed_stage<7, DIR>(cur, nxt, ms.N, ms.m[k], t, ms.F); break;
-      case 8: mixed_stage<8, DIR>(cur, nxt, ms.N, ms.m[k], t, ms.F); break;
-      default: mixed_stage<16, DIR>(cur, nxt, ms.N, ms.m[k], t, ms.F); break;
-    }
-    __syncthreads();  // dst complete; src free for the next stage's output
+  const int S = ms.nstages;  // >= 2 for every planned length (N > 64, R <= 16)
+  for (int k = 0; k < S - 1; ++k) {
+    mixed_stage_any<DIR, false>(cur, nxt, ms, k, tw, rows, (T)1);
+    __syncthreads();
     V *tmp = cur;
     cur = nxt;
     nxt = tmp;
   }
-  V *dst = out + row0 * ms.N;
-  for (int e = threadIdx.x; e < count; e += kMixedThreads) dst[e] = c_scale(cur[e], scale);
+  mixed_stage_any<DIR, true>(cur, out + row0 * ms.N, ms, S - 1, tw, rows, scale);
 }
 
 template <typename T>
