@@ -16,6 +16,12 @@ compute one by one, plus properties that hold at any size.
   points for every pair (covers every coefficient).
 * 32768 real signals x 3072 samples convolved with one 1025-tap filter: 16
   sampled rows against the direct sum.
+* 16384 x 3000 (mixed radix) and 16384 x 3001 (Bluestein): 6 sampled rows
+  against the direct DFT; the inverse round trip for every row.
+* 32768 real rows x 8192: 16 sampled half spectra against the oracle; C2R
+  round trip for every row.
+* 4 volumes of 128 x 256 x 256: one volume against the oracle's separable
+  3D transform; the inverse round trip for all four.
 
 All floating-point bounds are the relative-L2 tolerance 1e-5 * log2(N).
 """
@@ -182,3 +188,79 @@ def test_conv1_real_signals(fg):
     ref = oracle.convolve(x[rows].astype(np.complex128), h.astype(np.complex128))
     err = np.linalg.norm(got - ref, axis=1) / np.linalg.norm(ref, axis=1)
     assert err.max() <= TOL32 * 12
+
+
+def _any_length_full(fg, name, tol_len):
+    c = workloads.CONFIGS[name]
+    n, batch = c["n"], c["batch"]
+    x = workloads.config_input(name)
+    xd = torch.from_numpy(x).cuda()
+    yd, zd = torch.empty_like(xd), torch.empty_like(xd)
+    pf = fg.Plan(n, batch, 1, fg.FFT_FORWARD, fg.FFT_C2C_F32)
+    pi = fg.Plan(n, batch, 1, fg.FFT_INVERSE, fg.FFT_C2C_F32)
+    pf.exec(xd, yd)
+    pi.exec(yd, zd)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([workloads.sample_indices(5, batch, 71), [batch - 1]]))
+    y = yd[torch.from_numpy(rows).cuda()].cpu().numpy()
+    ref = np.stack([oracle.dft(x[r].astype(np.complex128)) for r in rows])
+    tol = TOL32 * int(np.log2(tol_len))
+    assert rel_rows(y, ref).max() <= tol
+    assert rel_rows(zd.cpu().numpy(), x).max() <= 2 * tol
+    pf.close()
+    pi.close()
+
+
+def test_any1_mixed_radix_3000(fg):
+    # 16384 x 3000 fp32 (mixed radix): 6 sampled rows (with the last) against
+    # the direct DFT; the inverse returns every row.
+    _any_length_full(fg, "any1", 3000)
+
+
+def test_any2_bluestein_3001(fg):
+    # 16384 x 3001 fp32 (prime: Bluestein, convolution length 8192).
+    _any_length_full(fg, "any2", 8192)
+
+
+def test_real1_r2c_c2r(fg):
+    # 32768 real rows x 8192: 16 sampled half spectra (with the last row)
+    # against the oracle; the C2R of the GPU spectra returns every row.
+    c = workloads.CONFIGS["real1"]
+    n, batch = c["n"], c["batch"]
+    x = workloads.config_input("real1")
+    xd = torch.from_numpy(x).cuda()
+    pf = fg.Plan(n, batch, 1, fg.FFT_FORWARD, fg.FFT_REAL_F32)
+    pi = fg.Plan(n, batch, 1, fg.FFT_INVERSE, fg.FFT_REAL_F32)
+    Xd = pf.exec(xd)
+    zd = pi.exec(Xd)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([workloads.sample_indices(15, batch, 81), [batch - 1]]))
+    X = Xd[torch.from_numpy(rows).cuda()].cpu().numpy()
+    ref = oracle.rfft(x[rows].astype(np.float64))
+    assert rel_rows(X, ref).max() <= TOL32 * 13
+    z = zd.cpu().numpy()
+    err = np.linalg.norm(z - x, axis=1) / np.linalg.norm(x, axis=1)
+    assert err.max() <= 2 * TOL32 * 13
+    pf.close()
+    pi.close()
+
+
+def test_nd1_3d_volumes(fg):
+    # 4 volumes of 128 x 256 x 256 fp32: volume 3 against the oracle's
+    # separable transform; the inverse round trip for all four.
+    c = workloads.CONFIGS["nd1"]
+    shape, batch = tuple(c["shape"]), c["batch"]
+    x = workloads.config_input("nd1")
+    xd = torch.from_numpy(x).cuda()
+    yd, zd = torch.empty_like(xd), torch.empty_like(xd)
+    pf = fg.Plan(0, batch, direction=fg.FFT_FORWARD, dtype=fg.FFT_C2C_F32, shape=shape)
+    pi = fg.Plan(0, batch, direction=fg.FFT_INVERSE, dtype=fg.FFT_C2C_F32, shape=shape)
+    pf.exec(xd, yd)
+    pi.exec(yd, zd)
+    torch.cuda.synchronize()
+    y3 = yd[3].cpu().numpy().reshape(1, -1)
+    ref = oracle.fftn(x[3].astype(np.complex128), 3).reshape(1, -1)
+    assert rel_rows(y3, ref).max() <= TOL32 * 23
+    assert rel_rows(zd.cpu().numpy().reshape(batch, -1), x.reshape(batch, -1)).max() <= 2 * TOL32 * 23
+    pf.close()
+    pi.close()
