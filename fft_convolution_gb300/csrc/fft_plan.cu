@@ -68,8 +68,12 @@ int ilog2_exact(int64_t n) {
 
 bool is_pow2(int64_t n) { return n > 0 && (n & (n - 1)) == 0; }
 
+// Records a failed CUDA call and consumes the runtime's last-error state it
+// left (a failed allocation would otherwise surface again at the next
+// launch check of an unrelated call).
 int cuda_fail(cudaError_t e) {
   g_cuda_error = e;
+  (void)cudaGetLastError();
   return e == cudaErrorMemoryAllocation ? FFT_ERR_ALLOC : FFT_ERR_CUDA;
 }
 
@@ -248,6 +252,7 @@ static fft_plan *plan_real(int64_t n, int64_t batch, int direction, int cdtype) 
   }
   if (e != cudaSuccess) {
     g_cuda_error = e;
+    (void)cudaGetLastError();
     fft_plan_destroy(p);
     g_status = e == cudaErrorMemoryAllocation ? FFT_ERR_ALLOC : FFT_ERR_CUDA;
     return nullptr;
@@ -365,6 +370,7 @@ static fft_plan *plan_any_length(int64_t n, int64_t batch, int direction, int dt
     free(host);
     if (e != cudaSuccess) {
       g_cuda_error = e;
+      (void)cudaGetLastError();
       if (p->mtw) cudaFree(p->mtw);
       delete p;
       g_status = e == cudaErrorMemoryAllocation ? FFT_ERR_ALLOC : FFT_ERR_CUDA;
@@ -397,6 +403,7 @@ static fft_plan *plan_any_length(int64_t n, int64_t batch, int direction, int dt
   }
   if (e != cudaSuccess) {
     g_cuda_error = e;
+    (void)cudaGetLastError();
     if (p->workspace) cudaFree(p->workspace);
     if (p->chirp) cudaFree(p->chirp);
     delete p;
@@ -472,6 +479,7 @@ fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int
   cudaError_t e = cudaMalloc(&p->workspace, p->workspace_bytes);
   if (e != cudaSuccess) {
     g_cuda_error = e;
+    (void)cudaGetLastError();
     delete p;
     g_status = FFT_ERR_ALLOC;
     return nullptr;
