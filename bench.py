@@ -141,6 +141,9 @@ def workload_info(name: str, pass_log: int = 9):
         bytes_per_step=batch * (2 * n * 8 + nc * 8),
         ideal_bytes_per_step=batch * (2 * n * 8 + nc * 8),
         flops_per_step=3 * 5.0 * L * log2i(L) * batch,
+        # the transforms the pipeline actually runs: one of length L (both
+        # inputs packed as a + ib) and one of length L/2 (the real product)
+        fp64_flops_per_step=(5.0 * L * log2i(L) + 5.0 * (L // 2) * log2i(L // 2)) * batch,
         transforms_per_step=3 * batch, h2d=batch * 2 * n * 8, d2h=batch * nc * 8)
 
 
@@ -634,6 +637,15 @@ def run_gpu(args):
                 "kernel": dom_name, "peak_source": peak_kind,
                 "launch_ms": round(dom_ms, 4),
                 "inverse_launch_ms": round(statistics.mean(inv_ms), 4) if inv_ms else None}
+    if info["kind"] == "polymul":
+        # Bound by the FP64 pipe: flops of the transforms run (5 M log2 M each) per pipeline
+        # launch against the GB300's nominal 1.25 TFLOP/s FP64 (an FMA probe measured 1.19).
+        fl = info["fp64_flops_per_step"]
+        tf = fl / (dom_ms * 1e-3) / 1e12
+        roofline.update(bound="alu", achieved=round(tf, 4), peak=1.25, unit="TFLOP/s",
+                        frac=round(tf / 1.25, 4), flops_per_launch=fl,
+                        peak_source="nominal FP64 (1.25 TFLOP/s); measured FMA probe 1.19",
+                        hbm_achieved_gbs=round(achieved, 1))
     if info.get("bluestein_m") and info["passes"] == 1:
         # Two length-M transforms per row of n points: the fused Bluestein kernel is bound by
         # on-chip arithmetic, not HBM.  Peak: 152 SMs x 128 fp32 lanes x 2 flop (FMA) x 2070 MHz.
