@@ -139,9 +139,9 @@ cudaError_t launch_conv_rows(int logn, Src src, Snk dst, vec2_t<T> *H, int h_per
     using C = RowsConfig<T, LOGN>;
     auto kern = conv_rows_kernel<T, LOGN, MODE, Src, Snk>;
     if (C::SMEM > 48 * 1024) {
-      static cudaError_t attr = cudaFuncSetAttribute(
-          kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
-      if (attr != cudaSuccess) return attr;
+      static std::atomic<unsigned long long> attr_set{0};
+      const cudaError_t e = smem_limit_once((const void *)kern, C::SMEM, attr_set);
+      if (e != cudaSuccess) return e;
     }
     const long long grid = (trows + C::F - 1) / C::F;
     if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

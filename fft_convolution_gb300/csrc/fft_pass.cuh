@@ -194,9 +194,9 @@ cudaError_t launch_pass_t(Load load, Store store, int log_n, int log_m, int twid
   using C = PassConfig<T, LOGL>;
   auto kern = fft_pass_kernel<T, LOGL, DIR, Load, Store>;
   if (C::SMEM > 48 * 1024) {
-    static cudaError_t attr = cudaFuncSetAttribute(
-        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
-    if (attr != cudaSuccess) return attr;
+    static std::atomic<unsigned long long> attr_set{0};
+    const cudaError_t e = smem_limit_once((const void *)kern, C::SMEM, attr_set);
+    if (e != cudaSuccess) return e;
   }
   const long long tiles = pass_tiles<T, LOGL>(log_n);
   PassGeom g{log_n, log_m, twiddle, tiles, 0, tiles, 0, 0};
@@ -209,11 +209,8 @@ cudaError_t launch_pass_t(Load load, Store store, int log_n, int log_m, int twid
   g.total = g.grid_per_batch * batch;
   if (g.total <= 0) return cudaErrorInvalidConfiguration;
   // Persistent grid: as many blocks as fit on the device at once.
-  static int per_sm = 0;
-  if (per_sm == 0 &&
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::THREADS, C::SMEM) !=
-          cudaSuccess)
-    return cudaGetLastError();
+  static std::atomic<int> occupancy[64];
+  const int per_sm = blocks_per_sm_once((const void *)kern, C::THREADS, C::SMEM, occupancy);
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

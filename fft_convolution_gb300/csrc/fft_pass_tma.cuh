@@ -336,14 +336,12 @@ cudaError_t launch_pass_tma_t(const void *in, void *out, int log_n, int log_m, i
       tout = tin;  // unused: the first pass stores linearly
     }
     auto kern = fft_pass_tma_kernel<T, LOGL, DIR>;
-    static cudaError_t attr = cudaFuncSetAttribute(
-        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
+    static std::atomic<unsigned long long> attr_set{0};
+    const cudaError_t attr = smem_limit_once((const void *)kern, Cfg::SMEM, attr_set);
     if (attr != cudaSuccess) return attr;
     TmaGeom g{log_n, log_m, twiddle, cols / Cfg::C, (cols / Cfg::C) * batch};
-    static int per_sm = 0;
-    if (per_sm == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                           &per_sm, kern, Cfg::THREADS, Cfg::SMEM) != cudaSuccess)
-      return cudaGetLastError();
+    static std::atomic<int> occupancy[64];
+    const int per_sm = blocks_per_sm_once((const void *)kern, Cfg::THREADS, Cfg::SMEM, occupancy);
     long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);
     if (grid > g.total_tiles) grid = g.total_tiles;
     kern<<<(unsigned)grid, Cfg::THREADS, Cfg::SMEM, st>>>(

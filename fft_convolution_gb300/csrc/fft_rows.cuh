@@ -69,9 +69,9 @@ cudaError_t launch_rows_t(const void *in, void *out, long long batch, cudaStream
   using C = RowsConfig<T, LOGN>;
   auto kern = fft_rows_kernel<T, LOGN, DIR>;
   if (C::SMEM > 48 * 1024) {
-    static cudaError_t attr = cudaFuncSetAttribute(
-        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
-    if (attr != cudaSuccess) return attr;
+    static std::atomic<unsigned long long> attr_set{0};
+    const cudaError_t e = smem_limit_once((const void *)kern, C::SMEM, attr_set);
+    if (e != cudaSuccess) return e;
   }
   const long long grid = (batch + C::F - 1) / C::F;
   kern<<<(unsigned)grid, C::THREADS, C::SMEM, st>>>(

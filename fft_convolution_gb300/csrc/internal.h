@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -13,6 +15,35 @@ namespace fftgb {
 template <typename T> struct RowsMaxLog;
 template <> struct RowsMaxLog<float> { static constexpr int value = 14; };
 template <> struct RowsMaxLog<double> { static constexpr int value = 13; };
+
+// Sets a kernel's dynamic shared-memory limit once per device (the
+// attribute belongs to the device's context).  `done` is the calling
+// launcher's own bitmask of devices already set.
+inline cudaError_t smem_limit_once(const void *kern, size_t bytes,
+                                   std::atomic<unsigned long long> &done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const unsigned long long bit = 1ull << dev;
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// Resident blocks per SM of a kernel on the current device, computed once
+// per device into the launcher's own `cache`; 0 if the query fails.
+inline int blocks_per_sm_once(const void *kern, int threads, size_t smem,
+                              std::atomic<int> (&cache)[64]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  int v = cache[dev].load(std::memory_order_acquire);
+  if (v == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, threads, smem) ==
+                    cudaSuccess)
+    cache[dev].store(v, std::memory_order_release);
+  return v;
+}
 
 // Batched contiguous transforms of length 2^logn (fft_rows_*.cu).
 cudaError_t launch_rows_f32(int logn, int dir, const void *in, void *out, long long batch,

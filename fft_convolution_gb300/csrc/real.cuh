@@ -199,9 +199,9 @@ cudaError_t launch_real_rows_t(const void *in, void *out, long long batch, cudaS
   using V = vec2_t<T>;
   auto kern = FWD ? r2c_rows_kernel<T, LOGH> : c2r_rows_kernel<T, LOGH>;
   if (C::SMEM > 48 * 1024) {
-    static cudaError_t attr = cudaFuncSetAttribute(
-        kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
-    if (attr != cudaSuccess) return attr;
+    static std::atomic<unsigned long long> attr_set{0};
+    const cudaError_t e = smem_limit_once((const void *)kern, C::SMEM, attr_set);
+    if (e != cudaSuccess) return e;
   }
   const long long grid = (batch + C::F - 1) / C::F;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

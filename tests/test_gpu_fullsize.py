@@ -264,3 +264,46 @@ def test_nd1_3d_volumes(fg):
     assert rel_rows(zd.cpu().numpy().reshape(batch, -1), x.reshape(batch, -1)).max() <= 2 * TOL32 * 23
     pf.close()
     pi.close()
+
+
+def test_max_length_2e30_tones(fg):
+    # The longest 1D plan (2^30 fp32 points, four HBM passes, 8 GiB per array):
+    # a sum of 8 unit tones at seeded integer bins has the exact spectrum N at
+    # those bins and 0 elsewhere, so every one of the 2^30 outputs is checked;
+    # the inverse returns the input.  (The input is formed on the device in
+    # fp64 with every phase index reduced mod N in integers.)
+    n = 1 << 30
+    bins, phases, _ = workloads.tone_params(n, 91, ntones=8)
+    dev = torch.device("cuda")
+    idx = torch.arange(n, dtype=torch.int64, device=dev)
+    re = torch.zeros(n, dtype=torch.float64, device=dev)
+    im = torch.zeros(n, dtype=torch.float64, device=dev)
+    for f, ph in zip(bins.tolist(), phases.tolist()):
+        ang = (idx * f).remainder_(n).to(torch.float64).mul_(2 * np.pi / n).add_(2 * np.pi * ph)
+        re += torch.cos(ang)
+        im += torch.sin(ang)
+        del ang
+    del idx
+    x = torch.complex(re.float(), im.float())
+    del re, im
+    y = torch.empty_like(x)
+    pf = fg.Plan(n, 1, 1, fg.FFT_FORWARD, fg.FFT_C2C_F32)
+    assert pf.num_kernels >= 4
+    pf.exec(x, y)
+    torch.cuda.synchronize()
+    tol = TOL32 * 30
+    kb = torch.from_numpy(bins).to(dev)
+    expect = torch.from_numpy(np.exp(2j * np.pi * phases).astype(np.complex128) * n).to(dev)
+    at_tones = y[kb].clone()
+    assert (at_tones.to(torch.complex128) - expect).abs().max().item() / n <= tol
+    y[kb] = 0
+    assert y.abs().max().item() / n <= tol
+    y[kb] = at_tones
+    pi = fg.Plan(n, 1, 1, fg.FFT_INVERSE, fg.FFT_C2C_F32)
+    pi.exec(y, y)
+    torch.cuda.synchronize()
+    err = torch.linalg.vector_norm(y - x).item() / torch.linalg.vector_norm(x).item()
+    assert err <= 2 * tol
+    assert fg.fft_device_status(int(torch.cuda.current_stream().cuda_stream)) == 0
+    pf.close()
+    pi.close()
