@@ -154,7 +154,13 @@ int fft_plan_num_kernels(const fft_plan *plan);
  *             complex plans (FFT_ERR_INVALID_ARG for real ones); other
  *             overlaps are not.  `in` is only read unless in == out.
  *   stream    a cudaStream_t (NULL = the legacy default stream).
- * Enqueues the kernels and returns; no synchronisation.
+ * Enqueues the kernels and returns; no synchronisation, no allocation, so
+ * the call can be captured into a CUDA graph.  Plans that own a workspace
+ * (fft_plan_workspace_bytes() > 0 beyond their tables: multi-pass,
+ * Bluestein beyond the on-chip length, the split real kinds) use it on
+ * every execution: executions of one such plan must not overlap on the GPU
+ * (one stream, or events between streams); use one plan per concurrent
+ * stream.
  */
 int fft_exec(const fft_plan *plan, const void *in, void *out, void *stream);
 
