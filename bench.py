@@ -371,6 +371,28 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def time_host_steps(step, stream, steps: int, warmup: int = 2) -> dict:
+    """Times `step` (host buffers in, host buffers out, asynchronous on
+    `stream`) with CUDA events around each step after `warmup` untimed ones;
+    the median step is the figure (host-memory effects make single steps
+    noisy)."""
+    import torch
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return {"median_ms": statistics.median(times), "mean_ms": statistics.mean(times),
+            "min_ms": min(times), "steps": steps}
+
+
 def whole_job_value(bytes_per_step: float, world: int, ms_step: float) -> float:
     """Weak scaling: every rank moves bytes_per_step per step; the job's GB/s
     is all ranks' bytes over the slowest rank's step time."""
@@ -536,28 +558,22 @@ def run_gpu(args):
     if info["kind"] in ("fft1d", "fft2d", "fftnd", "real") and not args.no_e2e:
         h_in = torch.from_numpy(x_h).pin_memory()
         h_out = torch.empty_like(h_in).pin_memory()
-        e2e_steps = max(1, min(args.steps, 5))
+        e2e_steps = max(5, min(args.steps, 10))
         # Chunks of the batch stream through the device: uploads, transforms
         # and downloads of different chunks overlap (fft_exec_host_chain).
-        chunk = max(1, c["batch"] // 16)
+        chunk = max(1, c["batch"] // args.e2e_chunks)
         # Samples in x_d, spectra in X_d for the real round trip.
         dev_b = X_d if info["kind"] == "real" else y_d
 
         def e2e_step():
             plans[0].chain_host(plans[1:], h_in, h_out, x_d, dev_b, chunk, stream)
-        e2e_step()
-        torch.cuda.synchronize(dev)
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        s1.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = s0.elapsed_time(s1) / e2e_steps
+        t = time_host_steps(e2e_step, stream, e2e_steps)
+        e2e_ms = t["median_ms"]
         e2e = {"value": info["bytes_per_step"] * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": info["h2d"], "d2h_bytes_per_step": info["d2h"],
-               "ms_per_step": round(e2e_ms, 4), "chunk_transforms": chunk}
+               "ms_per_step": round(e2e_ms, 4), "ms_mean": round(t["mean_ms"], 4),
+               "ms_min": round(t["min_ms"], 4), "timed_steps": e2e_steps,
+               "chunk_transforms": chunk}
     elif info["kind"] == "conv" and not args.no_e2e:
         hx = torch.from_numpy(xc_h).pin_memory()
         hy = torch.empty(yc_d.shape, dtype=torch.float32).pin_memory()
@@ -567,19 +583,12 @@ def run_gpu(args):
                 xc_d.copy_(hx, non_blocking=True)
                 step()
                 hy.copy_(yc_d, non_blocking=True)
-        e2e_step()
-        torch.cuda.synchronize(dev)
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for _ in range(max(1, min(args.steps, 5))):
-            e2e_step()
-        s1.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = s0.elapsed_time(s1) / max(1, min(args.steps, 5))
+        t = time_host_steps(e2e_step, stream, max(5, min(args.steps, 10)))
+        e2e_ms = t["median_ms"]
         e2e = {"value": info["bytes_per_step"] * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": info["h2d"], "d2h_bytes_per_step": info["d2h"],
-               "ms_per_step": round(e2e_ms, 4)}
+               "ms_per_step": round(e2e_ms, 4), "ms_mean": round(t["mean_ms"], 4),
+               "ms_min": round(t["min_ms"], 4), "timed_steps": t["steps"]}
     elif info["kind"] == "polymul" and not args.no_e2e:
         ha, hb = torch.from_numpy(a_h).pin_memory(), torch.from_numpy(b_h).pin_memory()
         hc = torch.empty(c_d.shape, dtype=torch.int64).pin_memory()
@@ -592,19 +601,12 @@ def run_gpu(args):
                                         c_d.data_ptr(), c["batch"], sh)
                 hc.copy_(c_d, non_blocking=True)
             assert rc == 0
-        e2e_step()
-        torch.cuda.synchronize(dev)
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for _ in range(max(1, min(args.steps, 3))):
-            e2e_step()
-        s1.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = s0.elapsed_time(s1) / max(1, min(args.steps, 3))
+        t = time_host_steps(e2e_step, stream, 3, warmup=1)
+        e2e_ms = t["median_ms"]
         e2e = {"value": info["bytes_per_step"] * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": info["h2d"], "d2h_bytes_per_step": info["d2h"],
-               "ms_per_step": round(e2e_ms, 4)}
+               "ms_per_step": round(e2e_ms, 4), "ms_mean": round(t["mean_ms"], 4),
+               "ms_min": round(t["min_ms"], 4), "timed_steps": t["steps"]}
 
     peak, peak_kind = measured_peaks()
     value = whole_job_value(info["bytes_per_step"], world, ms_step)
@@ -800,6 +802,8 @@ def main():
     ap.add_argument("--config", choices=sorted(workloads.CONFIGS), default="c2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-chunks", type=int, default=16,
+                    help="batch chunks streamed through the device by the end-to-end pipeline")
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--clock-soak", type=float, default=0.6,
                     help="seconds of untimed load sampled for clocks before the timed region")
