@@ -40,6 +40,12 @@ __global__ void __launch_bounds__(RowsConfig<T, LOGN>::THREADS)
   const long long tr = (long long)blockIdx.x * F + f;
   const bool active = tr < batch;
 
+  // Launched with programmatic dependent launch: wait until the previous
+  // kernel on the stream has finished (and its writes are visible) before
+  // reading, and let the next kernel's blocks be scheduled once every block
+  // of this one holds its data (they then fill the SMs this launch's tail
+  // frees, and wait the same way).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   V x[P::E];
   if (active) {
     const V *src = in + tr * P::L;
@@ -49,6 +55,7 @@ __global__ void __launch_bounds__(RowsConfig<T, LOGN>::THREADS)
 #pragma unroll
     for (int w = 0; w < P::E; ++w) x[w] = make_c<V>((T)0, (T)0);
   }
+  asm volatile("griddepcontrol.launch_dependents;");
 
   const SmemView<V> sm{smem + f * P::SMEM_ELEMS, 1};
   fft_on_chip<LOGN, DIR>(x, t, sm);
@@ -74,9 +81,19 @@ cudaError_t launch_rows_t(const void *in, void *out, long long batch, cudaStream
     if (e != cudaSuccess) return e;
   }
   const long long grid = (batch + C::F - 1) / C::F;
-  kern<<<(unsigned)grid, C::THREADS, C::SMEM, st>>>(
-      static_cast<const vec2_t<T> *>(in), static_cast<vec2_t<T> *>(out), batch);
-  return cudaGetLastError();
+  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<const vec2_t<T> *>(in),
+                            static_cast<vec2_t<T> *>(out), batch);
 }
 
 template <typename T, int DIR, int LOGN = 0>
