@@ -286,16 +286,27 @@ def convolve(x, h) -> np.ndarray:
     return np.stack(rows)
 
 
+def _transform_rows(x2: np.ndarray, direction: int) -> np.ndarray:
+    """1D transform of every row: the recursive CT for power-of-two lengths,
+    the direct DFT for the others."""
+    n = x2.shape[-1]
+    if n & (n - 1) == 0:
+        return fft(x2, direction)
+    return np.stack([dft(np.ascontiguousarray(r), direction) for r in x2.reshape(-1, n)]
+                    ).reshape(x2.shape)
+
+
 def fftn(x, ndim: int, direction: int = -1) -> np.ndarray:
-    """The recursive CT along each of the last `ndim` axes in turn, the
-    contiguous axis first (separable transform); the inverse scales by
+    """The 1D transform along each of the last `ndim` axes in turn, the
+    contiguous axis first (separable transform): recursive CT for
+    power-of-two sides, direct DFT for the others; the inverse scales by
     1/(product of the sides).  numpy only moves axes; the arithmetic is the
     oracle's."""
     y = _c128(x)
     for k in range(1, ndim + 1):
         axis = y.ndim - k
         moved = np.ascontiguousarray(np.moveaxis(y, axis, -1))
-        y = np.moveaxis(fft(moved, direction), -1, axis)
+        y = np.moveaxis(_transform_rows(moved, direction), -1, axis)
     return np.ascontiguousarray(y)
 
 

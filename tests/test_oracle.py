@@ -402,7 +402,8 @@ def test_convolve_rows():
     assert rel_l2(y1[2], np.convolve(x[2], h[0])) < 1e-14
 
 
-@pytest.mark.parametrize("shape", [(2, 8), (16, 4), (4, 8, 16), (2, 1, 32), (8, 8, 8)])
+@pytest.mark.parametrize("shape", [(2, 8), (16, 4), (4, 8, 16), (2, 1, 32), (8, 8, 8),
+                                   (3, 5), (6, 10), (12, 7, 9), (1, 100), (5, 1, 3)])
 def test_fftn_matches_numpy(shape):
     x = workloads.normal_complex((2,) + shape, 900 + len(shape), np.complex128)
     nd = len(shape)
@@ -412,7 +413,7 @@ def test_fftn_matches_numpy(shape):
     d = np.zeros(shape, complex)
     d[(0,) * nd] = 1
     assert np.array_equal(oracle.fftn(d, nd), np.ones(shape))
-    if nd == 2:
+    if nd == 2 and all(v & (v - 1) == 0 for v in shape):
         assert rel_l2(X, oracle.fft2d(x)) < 1e-15
 
 
