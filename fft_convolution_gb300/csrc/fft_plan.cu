@@ -51,7 +51,8 @@ enum Kind {
   KIND_REAL_ROWS = 5,  // real, N = 2H with H a power of two on chip: one kernel
   KIND_REAL_EVEN = 6,  // real, other even N: complex plan of length N/2 + pre/post kernel
   KIND_REAL_ODD = 7,   // real, odd N: complex plan of length N + widen/narrow kernels
-  KIND_MIXED = 8       // N = 2^a 3^b 5^c 7^d (not a power of two) on chip
+  KIND_MIXED = 8,      // N = 2^a 3^b 5^c 7^d (not a power of two) on chip
+  KIND_ND_ANY = 9      // 2D / 3D with a side that is not a power of two (or beyond KIND_ND's limits)
 };
 
 // Lengths that are not powers of two: the direct DFT up to this length,
@@ -155,6 +156,12 @@ struct fft_plan {
   // Mixed radix: the stages and their forward twiddle table (in aux).
   MixedStages ms;
   void *mtw;
+  // KIND_ND_ANY: the sides (outermost first), and per axis either a 1D plan
+  // of any length (run on the contiguous axis, or between two transposes)
+  // or an in-place power-of-two column pass (axis_pass).
+  int64_t side[3];
+  fft_plan *axis_plan[3];
+  int axis_pass[3];
 };
 
 namespace {
@@ -177,7 +184,8 @@ size_t out_tbytes(const fft_plan *p) {
 // reused whole by every batch range on one stream, as Bluestein's is).
 size_t ws_tbytes(const fft_plan *p) {
   if (p->kind == KIND_MULTI) return (size_t)p->n * complex_bytes(p);
-  if (p->kind == KIND_REAL_EVEN || p->kind == KIND_REAL_ODD) return p->ws_stride;
+  if (p->kind == KIND_REAL_EVEN || p->kind == KIND_REAL_ODD || p->kind == KIND_ND_ANY)
+    return p->ws_stride;
   return 0;
 }
 
@@ -413,6 +421,76 @@ static fft_plan *plan_any_length(int64_t n, int64_t batch, int direction, int dt
   return p;
 }
 
+// Plans a 2D / 3D transform whose sides are not all powers of two within
+// the one-kernel-per-axis limits (the caller validated the arguments and
+// the sizes).  The contiguous axis runs as a 1D plan of any length over
+// batch * (other sides) rows.  Every other axis of length > 1 runs as an
+// in-place power-of-two column pass when its length and its stride are
+// powers of two within the pass limits; otherwise it is transposed to the
+// contiguous position in the workspace, transformed there by a 1D plan of
+// any length, and transposed back.
+static fft_plan *plan_nd_any(int rank, const int64_t *shape, int64_t batch, int direction,
+                             int dtype) {
+  const size_t elem = dtype == FFT_C2C_F32 ? 8 : 16;
+  const int pass_max = dtype == FFT_C2C_F32 ? kPassMaxLogF32 : kPassMaxLogF64;
+  fft_plan *p = new (std::nothrow) fft_plan;
+  if (!p) {
+    g_status = FFT_ERR_ALLOC;
+    return nullptr;
+  }
+  memset(p, 0, sizeof(*p));
+  p->kind = KIND_ND_ANY;
+  p->rank = rank;
+  p->dims = rank;
+  p->batch = batch;
+  p->direction = direction;
+  p->dtype = dtype;
+  int64_t total = 1;
+  for (int k = 0; k < rank; ++k) {
+    p->side[k] = shape[k];
+    total *= shape[k];
+  }
+  p->elems = total;
+  p->n = shape[rank - 1];
+  bool need_ws = false;
+  int64_t stride = 1;  // product of the sides inside axis k
+  for (int k = rank - 1; k >= 0; --k) {
+    const int64_t L = shape[k];
+    if (L > 1) {
+      const bool pow2_pass = k < rank - 1 && is_pow2(L) && is_pow2(stride) &&
+                             ilog2_exact(L) <= pass_max;
+      if (pow2_pass) {
+        p->axis_pass[k] = 1;
+      } else {
+        p->axis_plan[k] = fft_plan_create(L, batch * (total / L), 1, direction, dtype);
+        if (!p->axis_plan[k]) {  // g_status says why
+          const int st = g_status;
+          fft_plan_destroy(p);
+          g_status = st;
+          return nullptr;
+        }
+        if (k < rank - 1) need_ws = true;
+      }
+    }
+    stride *= L;
+  }
+  g_status = FFT_OK;
+  if (need_ws) {
+    p->ws_stride = (size_t)total * elem;
+    p->workspace_bytes = (size_t)batch * p->ws_stride;
+    cudaError_t e = cudaMalloc(&p->workspace, p->workspace_bytes);
+    if (e != cudaSuccess) {
+      g_cuda_error = e;
+      (void)cudaGetLastError();
+      p->workspace = nullptr;
+      fft_plan_destroy(p);
+      g_status = e == cudaErrorMemoryAllocation ? FFT_ERR_ALLOC : FFT_ERR_CUDA;
+      return nullptr;
+    }
+  }
+  return p;
+}
+
 extern "C" {
 
 fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int dtype) {
@@ -501,27 +579,32 @@ fft_plan *fft_plan_create_nd(int rank, const int64_t *shape, int64_t batch, int 
   const int pass_max = dtype == FFT_C2C_F32 ? kPassMaxLogF32 : kPassMaxLogF64;
   int logs[3] = {0, 0, 0};
   int total_log = 0;
+  bool fast = true;  // every side a power of two within the one-kernel-per-axis limits
+  int64_t total = 1;
   for (int k = 0; k < rank; ++k) {
-    if (shape[k] <= 0) {
-      g_status = FFT_ERR_INVALID_ARG;
+    if (shape[k] <= 0 || shape[k] > ((int64_t)1 << 30)) {
+      g_status = shape[k] <= 0 ? FFT_ERR_INVALID_ARG : FFT_ERR_UNSUPPORTED;
+      return nullptr;
+    }
+    total *= shape[k];
+    if (total > ((int64_t)1 << 40)) {
+      g_status = FFT_ERR_UNSUPPORTED;
       return nullptr;
     }
     if (!is_pow2(shape[k])) {
-      g_status = FFT_ERR_NOT_POW2;
-      return nullptr;
+      fast = false;
+      continue;
     }
     logs[k] = ilog2_exact(shape[k]);
     total_log += logs[k];
     // The innermost side runs on chip; the others as in-place column passes.
-    if (logs[k] > (k == rank - 1 ? on_chip_max : pass_max)) {
-      g_status = FFT_ERR_UNSUPPORTED;
-      return nullptr;
-    }
+    if (logs[k] > (k == rank - 1 ? on_chip_max : pass_max)) fast = false;
   }
-  if (total_log > 34 || batch > ((int64_t)1 << 40) / ((int64_t)1 << total_log)) {
+  if (batch > ((int64_t)1 << 40) / total) {
     g_status = FFT_ERR_UNSUPPORTED;
     return nullptr;
   }
+  if (!fast) return plan_nd_any(rank, shape, batch, direction, dtype);
   fft_plan *p = new (std::nothrow) fft_plan;
   if (!p) {
     g_status = FFT_ERR_ALLOC;
@@ -548,12 +631,16 @@ void fft_plan_destroy(fft_plan *plan) {
   if (plan->rtw) cudaFree(plan->rtw);
   if (plan->mtw) cudaFree(plan->mtw);
   if (plan->inner) fft_plan_destroy(plan->inner);
+  for (int k = 0; k < 3; ++k)
+    if (plan->axis_plan[k]) fft_plan_destroy(plan->axis_plan[k]);
   delete plan;
 }
 
 size_t fft_plan_workspace_bytes(const fft_plan *plan) {
   if (!plan) return 0;
-  return plan->workspace_bytes + plan->aux_bytes + fft_plan_workspace_bytes(plan->inner);
+  size_t b = plan->workspace_bytes + plan->aux_bytes + fft_plan_workspace_bytes(plan->inner);
+  for (int k = 0; k < 3; ++k) b += fft_plan_workspace_bytes(plan->axis_plan[k]);
+  return b;
 }
 
 }  // extern "C"
@@ -614,6 +701,49 @@ struct Schedule {
         }
         inner += l;
       }
+    }
+    return cudaSuccess;
+  }
+
+  // KIND_ND_ANY (see plan_nd_any), over this range of the batch.
+  cudaError_t run_nd_any(const char *in, char *out) {
+    const int64_t total = p->elems;
+    const size_t elem = this->elem();
+    const int r = p->rank;
+    cudaError_t e = cudaSuccess;
+    // Contiguous axis: in -> out.
+    if (p->axis_plan[r - 1]) {
+      const long long rows = total / p->side[r - 1];
+      Schedule s1(p->axis_plan[r - 1], st, dry, batch * rows, b0 * rows);
+      e = s1.run(in, out);
+      count += s1.count;
+      if (e != cudaSuccess) return e;
+    } else if (in != out && !dry) {  // contiguous side of length 1: the data moves as is
+      e = cudaMemcpyAsync(out, in, (size_t)batch * total * elem, cudaMemcpyDeviceToDevice, st);
+      if (e != cudaSuccess) return e;
+    }
+    int64_t stride = p->side[r - 1];
+    for (int k = r - 2; k >= 0; --k) {
+      const int64_t L = p->side[k];
+      const long long outer = batch * (total / (L * stride));
+      if (p->axis_pass[k]) {
+        const int l = ilog2_exact(L), inner = ilog2_exact(stride);
+        PassArgs a{l + inner, l, inner, 0, outer, {}};
+        e = pass(a, out, out);
+      } else if (p->axis_plan[k]) {
+        // [outer][L][stride] -> ws [outer][stride][L], transform, and back.
+        count += 2;
+        if (!dry) e = transpose_complex(p->dtype == FFT_C2C_F64, out, ws, outer, L, stride, st);
+        if (e != cudaSuccess) return e;
+        const long long rows = total / L;
+        Schedule sk(p->axis_plan[k], st, dry, batch * rows, b0 * rows);
+        e = sk.run(ws, ws);
+        count += sk.count;
+        if (e != cudaSuccess) return e;
+        if (!dry) e = transpose_complex(p->dtype == FFT_C2C_F64, ws, out, outer, stride, L, st);
+      }
+      if (e != cudaSuccess) return e;
+      stride *= L;
     }
     return cudaSuccess;
   }
@@ -704,6 +834,8 @@ struct Schedule {
         return rows(in, out, batch);
       case KIND_ND:
         return run_nd(i, o);
+      case KIND_ND_ANY:
+        return run_nd_any(i, o);
       case KIND_DFT: {
         ++count;
         if (dry) return cudaSuccess;

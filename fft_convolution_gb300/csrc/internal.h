@@ -161,6 +161,11 @@ cudaError_t mixed_exec_f32(const void *in, void *out, long long batch, const Mix
 cudaError_t mixed_exec_f64(const void *in, void *out, long long batch, const MixedStages &ms,
                            const void *tw, int dir, cudaStream_t st);
 
+// Batched transpose of complex matrices, in [B][R][C] -> out [B][C][R]
+// (transpose.cu); in and out must not overlap.
+cudaError_t transpose_complex(int f64, const void *in, void *out, long long B, long long R,
+                              long long C, cudaStream_t st);
+
 // Transforms of real sequences (real_*.cu).  On chip: N = 2H, H = 2^logh,
 // forward (dir < 0) batch x 2H reals -> batch x (H + 1) bins, inverse the
 // reverse with 1/N.

@@ -88,8 +88,8 @@ typedef struct fft_plan fft_plan;
  * n x n images (dims = 2) in the given direction and element type.
  *   n         1 <= n.  dims = 1: a power of two up to 2^30 (fp32) / 2^29
  *             (fp64), or any other length up to 2^26 (fp32) / 2^25 (fp64);
- *             batch * n * element size must fit the device.  dims = 2: a
- *             power of two up to 2^14 (fp32) / 2^13 (fp64).
+ *             batch * n * element size must fit the device.  dims = 2: as
+ *             fft_plan_create_nd with shape {n, n}.
  *   batch     number of independent transforms, >= 1.
  *   dims      1, or 2 for an n x n transform (= fft_plan_create_nd with
  *             shape {n, n}).
@@ -125,10 +125,15 @@ fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int
  * shape[0] x ... x shape[rank-1] (row-major: the last side is contiguous),
  * rank 1, 2 or 3 ("Stockham FFT Butterfly Algorithm in Parallel GLSL",
  * section Multi-Dimensional Transforms: the 1D transform along each axis in
- * turn, rows first).  Every side a power of two; the last side at most
- * 2^14 (fp32) / 2^13 (fp64), the others at most the same.  The inverse
- * scales by 1/(product of the sides).  Runs as one on-chip row kernel plus
- * one in-place column pass per other axis; no workspace.  rank 1 is
+ * turn, rows first).  Sides of any length 1 .. 2^30 (at most 2^40 elements
+ * in all).  The inverse scales by 1/(product of the sides).  When every
+ * side is a power of two, the last at most 2^14 (fp32) / 2^13 (fp64) and
+ * the others at most the same, the plan is one on-chip row kernel plus one
+ * in-place column pass per other axis, with no workspace.  Otherwise the
+ * contiguous axis runs as a 1D plan of any length (fft_plan_create), and
+ * every other axis either as an in-place column pass (power-of-two length
+ * and stride) or through a transpose into a workspace of batch * elements,
+ * a 1D plan there, and a transpose back.  rank 1 is
  * fft_plan_create(shape[0], batch, 1, ...).  Errors as fft_plan_create.
  */
 fft_plan *fft_plan_create_nd(int rank, const int64_t *shape, int64_t batch, int direction,

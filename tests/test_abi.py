@@ -60,9 +60,8 @@ def test_status_strings(fg):
     ((8, 1, 3, -1, 0), 1),        # dims
     ((8, 1, 1, 0, 0), 1),         # direction
     ((8, 1, 1, -1, 7), 1),        # dtype
-    ((1000, 4, 2, 1, 1), 2),      # 2D side not a power of two
-    ((1 << 15, 1, 2, -1, 0), 3),  # 2D side beyond the on-chip limit
-    ((1 << 14, 1, 2, -1, 1), 3),
+    ((1 << 31, 1, 2, 1, 1), 3),   # 2D side beyond 2^30
+    ((1 << 21, 1 << 20, 2, -1, 0), 3),  # more than 2^40 elements
     ((1 << 31, 1, 1, -1, 0), 3),  # 1D beyond the supported length
 ])
 def test_plan_create_rejects(fg, args, status):

@@ -240,11 +240,58 @@ def test_nd_large_3d(fg):
 
 def test_nd_rejects(fg):
     with pytest.raises(fg.FFTError):
-        fg.Plan(0, 1, shape=(6, 8))                 # not a power of two
+        fg.Plan(0, 1, shape=(6, 0))                 # empty side
     with pytest.raises(fg.FFTError):
-        fg.Plan(0, 1, shape=(2, 2, 1 << 15))        # contiguous side beyond on chip
+        fg.Plan(0, 1, shape=(2, 1 << 31))           # side beyond 2^30
     with pytest.raises(fg.FFTError):
         fg.fft_plan_create_nd(4, (2, 2, 2, 2), 1, -1, 0)
+
+
+# Sides that are not powers of two, or beyond one kernel per axis: the
+# contiguous axis as a 1D plan of any length, the others as power-of-two
+# column passes or between two transposes.
+@pytest.mark.parametrize("dtype,shape,batch", [
+    (F32, (6, 8), 3), (F32, (100, 64), 2), (F32, (30, 50), 2), (F32, (3, 5, 7), 3),
+    (F32, (12, 16, 20), 2), (F32, (7, 1, 9), 2), (F32, (1, 100), 3), (F32, (64, 3000), 2),
+    (F32, (2, 2, 1 << 15), 2), (F32, (1 << 15, 4), 2), (F32, (1009, 6), 2),
+    (F64, (6, 8), 3), (F64, (30, 50), 2), (F64, (12, 16, 20), 2), (F64, (1 << 14, 4), 1)])
+def test_nd_any_sides(fg, dtype, shape, batch):
+    x = workloads.normal_complex((batch,) + shape, 5600 + sum(shape), NP[dtype])
+    p = fg.Plan(0, batch, direction=fg.FFT_FORWARD, dtype=dtype, shape=shape)
+    pi = fg.Plan(0, batch, direction=fg.FFT_INVERSE, dtype=dtype, shape=shape)
+    xd = torch.from_numpy(x).cuda()
+    yd, zd = torch.empty_like(xd), torch.empty_like(xd)
+    p.exec(xd, yd)
+    pi.exec(yd, zd)
+    torch.cuda.synchronize()
+    npts = int(np.prod(shape))
+    work = 1
+    for v in shape:   # the Bluestein axes carry their convolution length
+        pow2_or_smooth = v & (v - 1) == 0 or v <= 64 or all(
+            f in (2, 3, 5, 7) for f in _factors(v))
+        work *= v if pow2_or_smooth else bluestein_len(v)
+    t = tol(dtype, work)
+    ref = oracle.fftn(x.astype(np.complex128), len(shape))
+    assert rel_rows(yd.cpu().numpy(), ref).max() <= t
+    assert rel_rows(zd.cpu().numpy(), x).max() <= 2 * t
+    # in place
+    p.exec(xd, xd)
+    torch.cuda.synchronize()
+    assert rel_rows(xd.cpu().numpy(), ref).max() <= t
+    p.close()
+    pi.close()
+
+
+def _factors(v):
+    out, f = [], 2
+    while f * f <= v:
+        while v % f == 0:
+            out.append(f)
+            v //= f
+        f += 1
+    if v > 1:
+        out.append(v)
+    return out
 
 
 # --- lengths that are not powers of two ---------------------------------------
