@@ -425,7 +425,7 @@ def irfft(X, n: int, out=None, stream=None):
 
 def fftn(x, ndim: int, direction: int = FFT_FORWARD, out=None, stream=None):
     """Transforms over the last `ndim` (1-3) axes of a contiguous CUDA
-    tensor, power-of-two sides."""
+    tensor, sides of any length."""
     shape = tuple(x.shape[-ndim:])
     batch = x.numel()
     for v in shape:
