@@ -80,6 +80,9 @@ def workload_info(name: str, pass_log: int = 9):
         elif smooth_2357(n) and 64 < n <= 12288:
             passes = 1    # mixed radix on chip: one read, one write
             info.update(mixed=True)
+        elif smooth_2357(n):
+            passes = 5    # four-step: 3 transposes + 2 on-chip mixed-radix passes
+            info.update(four_step=True)
         else:
             # Bluestein: a length-M cyclic convolution per row, M = 2^ceil(log2(2n - 1));
             # fused on chip (one read, one write) while M <= 2^14.
@@ -225,6 +228,7 @@ KERNEL_SOURCES = {
     "conv1": ["fft_device.cuh", "fft_rows.cuh", "conv.cuh", "conv_f32.cu"],
     "any1": ["fft_device.cuh", "mixed.cuh", "mixed_f32.cu", "fft_plan.cu"],
     "any2": ["fft_device.cuh", "fft_rows.cuh", "conv.cuh", "anylen.cuh", "anylen_f32.cu"],
+    "any3": ["fft_device.cuh", "mixed.cuh", "mixed_f32.cu", "transpose.cu", "fft_plan.cu"],
     "real1": ["fft_device.cuh", "fft_rows.cuh", "real.cuh", "real_f32.cu"],
     "nd1": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_f32.cu", "fft_pass.cuh",
             "fft_pass_tma.cuh", "fft_pass_f32.cu", "fft_plan.cu"],
@@ -293,6 +297,16 @@ def cpu_oracle_sample(name: str, budget_s: float = 12.0):
             done_units = k / c["batch"]
             sample = f"{k} of {c['batch']} transforms of N={n}" + \
                 (" (forward+inverse)" if info["directions"] == 2 else "")
+        elif n & (n - 1):
+            # a long length that is not a power of two: the oracle is the direct
+            # DFT; time bins of one row (O(N) each) and scale by the bins of the step
+            x = workloads.config_input(name, scale_batch=1)[0].astype(np.complex128)
+            bins = 0
+            while time.perf_counter() - t0 < budget_s and bins < n:
+                oracle.dft_bins(x, np.arange(bins, bins + 64, dtype=np.int64) % n)
+                bins += 64
+            done_units = bins / (n * c["batch"] * info["directions"])
+            sample = f"{bins} bins of one N={n} row by the direct sum, scaled to the step"
         else:
             # one long transform: time a 2^20 transform and scale by N log N
             m = 1 << 20
@@ -631,6 +645,8 @@ def run_gpu(args):
             info["kind"] == "fft1d" else "forward plan (%d kernels)" % plans[0].num_kernels
         if info.get("mixed"):
             dom_name = "mixed_rows_kernel<float,-1> (N=%d)" % c["n"]
+        if info.get("four_step"):
+            dom_name = "forward four-step plan (%d kernels, N=%d)" % (plans[0].num_kernels, c["n"])
     achieved = per_launch_bytes / (dom_ms * 1e-3) / 1e9
     tr = committed_traffic(name)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -739,6 +755,9 @@ def workload_label(name: str) -> str:
         return "1D real R2C+C2R, N=8192, batch 32768, fp32 (1 GiB of samples)"
     if name == "any1":
         return "1D C2C forward+inverse, N=3000 = 2^3 3 5^3 (mixed radix on chip), batch 16384, fp32"
+    if name == "any3":
+        return ("1D C2C forward+inverse, N=100000 = 2^5 5^5 (four-step: 2 mixed-radix passes, "
+                "3 transposes), batch 1024, fp32")
     if name == "any2":
         return "1D C2C forward+inverse, N=3001 prime (Bluestein, M=8192 on chip), batch 16384, fp32"
     if name == "nd1":
@@ -773,7 +792,7 @@ def run_reference(args):
     line = {
         "impl": "reference",
         "metric": metric_name(info["kind"]),
-        "value": round(value, 4),
+        "value": float(f"{value:.4g}"),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -785,9 +804,9 @@ def run_reference(args):
         "dtype": "f64",
         "data": "synthetic (seeded)",
         "config": {"workload": workload_label(name), "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": float(f"{value:.4g}"), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": last["sample"] + " per step"},
-        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+        "e2e": {"value": float(f"{value:.4g}"), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

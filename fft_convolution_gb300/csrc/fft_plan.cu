@@ -52,7 +52,8 @@ enum Kind {
   KIND_REAL_EVEN = 6,  // real, other even N: complex plan of length N/2 + pre/post kernel
   KIND_REAL_ODD = 7,   // real, odd N: complex plan of length N + widen/narrow kernels
   KIND_MIXED = 8,      // N = 2^a 3^b 5^c 7^d (not a power of two) on chip
-  KIND_ND_ANY = 9      // 2D / 3D with a side that is not a power of two (or beyond KIND_ND's limits)
+  KIND_ND_ANY = 9,     // 2D / 3D with a side that is not a power of two (or beyond KIND_ND's limits)
+  KIND_FOUR_STEP = 10  // N = N1 N2 (2, 3, 5, 7 only) beyond one block: two mixed-radix plans
 };
 
 // Lengths that are not powers of two: the direct DFT up to this length,
@@ -184,7 +185,8 @@ size_t out_tbytes(const fft_plan *p) {
 // reused whole by every batch range on one stream, as Bluestein's is).
 size_t ws_tbytes(const fft_plan *p) {
   if (p->kind == KIND_MULTI) return (size_t)p->n * complex_bytes(p);
-  if (p->kind == KIND_REAL_EVEN || p->kind == KIND_REAL_ODD || p->kind == KIND_ND_ANY)
+  if (p->kind == KIND_REAL_EVEN || p->kind == KIND_REAL_ODD || p->kind == KIND_ND_ANY ||
+      p->kind == KIND_FOUR_STEP)
     return p->ws_stride;
   return 0;
 }
@@ -336,6 +338,81 @@ static void mixed_twiddles(const MixedStages &ms, bool f64, void *host) {
   }
 }
 
+static bool is_smooth_2357(int64_t n) {
+  const int f[4] = {2, 3, 5, 7};
+  for (int k = 0; k < 4; ++k)
+    while (n % f[k] == 0) n /= f[k];
+  return n == 1;
+}
+
+// Split twiddle table of W_N = e^{-2 pi i / N}: lo[j] = W_N^j (j < 2^log_s),
+// hi[i] = W_N^{i 2^log_s} (i < nhi), host double precision, rounded once.
+static void split_twiddles(int64_t n, int log_s, int64_t nhi, bool f64, void *host) {
+  const double two_pi = 6.283185307179586476925286766559;
+  const int64_t S = (int64_t)1 << log_s;
+  for (int64_t i = 0; i < S + nhi; ++i) {
+    const int64_t e = i < S ? i % n : (int64_t)(((unsigned __int128)(i - S) * (unsigned __int128)S) % (unsigned __int128)n);
+    const double ang = two_pi * (double)e / (double)n;
+    if (f64) {
+      static_cast<double *>(host)[2 * i] = cos(ang);
+      static_cast<double *>(host)[2 * i + 1] = -sin(ang);
+    } else {
+      static_cast<float *>(host)[2 * i] = (float)cos(ang);
+      static_cast<float *>(host)[2 * i + 1] = (float)-sin(ang);
+    }
+  }
+}
+
+// Four-step plan of a smooth length n = n1 * n2 (p: the caller's plan,
+// already holding n, batch, direction, dtype; freed on failure).  x viewed
+// as [n1][n2]: transpose, n2 * batch transforms of length n1, twiddle
+// W_N^{n2 k1} folded into the second transpose, n1 * batch transforms of
+// length n2, transpose to the output order k1 + n1 k2.
+static fft_plan *plan_four_step(int64_t n, int64_t n1, int64_t batch, int direction, int dtype,
+                                fft_plan *p) {
+  const size_t elem = dtype == FFT_C2C_F32 ? 8 : 16;
+  const int64_t n2 = n / n1;
+  p->kind = KIND_FOUR_STEP;
+  p->side[0] = n1;
+  p->side[1] = n2;
+  cudaError_t e = cudaSuccess;
+  p->axis_plan[0] = fft_plan_create(n1, batch * n2, 1, direction, dtype);
+  if (p->axis_plan[0]) p->axis_plan[1] = fft_plan_create(n2, batch * n1, 1, direction, dtype);
+  if (!p->axis_plan[0] || !p->axis_plan[1]) {
+    const int st = g_status;
+    fft_plan_destroy(p);
+    g_status = st;
+    return nullptr;
+  }
+  g_status = FFT_OK;
+  int log_s = 0;
+  while (((int64_t)1 << (2 * log_s)) < n) ++log_s;
+  p->rtw_log_s = log_s;
+  p->rtw_nhi = ((n - 1) >> log_s) + 1;
+  p->aux_bytes = (((size_t)1 << log_s) + (size_t)p->rtw_nhi) * elem;
+  void *host = malloc(p->aux_bytes);
+  e = host ? cudaMalloc(&p->rtw, p->aux_bytes) : cudaErrorMemoryAllocation;
+  if (e == cudaSuccess) {
+    split_twiddles(n, log_s, p->rtw_nhi, dtype == FFT_C2C_F64, host);
+    e = cudaMemcpy(p->rtw, host, p->aux_bytes, cudaMemcpyHostToDevice);
+  }
+  free(host);
+  if (e == cudaSuccess) {
+    p->ws_stride = (size_t)n * elem;
+    p->workspace_bytes = (size_t)batch * p->ws_stride;
+    e = cudaMalloc(&p->workspace, p->workspace_bytes);
+    if (e != cudaSuccess) p->workspace = nullptr;
+  }
+  if (e != cudaSuccess) {
+    g_cuda_error = e;
+    (void)cudaGetLastError();
+    fft_plan_destroy(p);
+    g_status = e == cudaErrorMemoryAllocation ? FFT_ERR_ALLOC : FFT_ERR_CUDA;
+    return nullptr;
+  }
+  return p;
+}
+
 // Plans a 1D length that is not a power of two (the caller validated the
 // other arguments): the direct DFT for n <= kDirectDftMax; mixed radix on
 // chip for longer lengths whose prime factors are 2, 3, 5, 7 (up to
@@ -385,6 +462,15 @@ static fft_plan *plan_any_length(int64_t n, int64_t batch, int direction, int dt
       return nullptr;
     }
     return p;
+  }
+  const int64_t mixed_max = dtype == FFT_C2C_F32 ? kMixedMaxF32 : kMixedMaxF64;
+  if (n > mixed_max && is_smooth_2357(n)) {
+    // Smooth but longer than one block: the four-step split N = N1 N2 with
+    // both factors on chip, N1 the divisor closest to sqrt(N).
+    int64_t n1 = 0;
+    for (int64_t d = 1; d * d <= n; ++d)
+      if (n % d == 0 && n / d <= mixed_max) n1 = d;
+    if (n1 > 1 && batch <= ((int64_t)1 << 40) / n) return plan_four_step(n, n1, batch, direction, dtype, p);
   }
   const int log_m = ilog2_exact(2 * n - 1);
   if (log_m > (dtype == FFT_C2C_F32 ? 27 : 26) || batch > ((int64_t)1 << 40) / ((int64_t)1 << log_m)) {
@@ -748,6 +834,38 @@ struct Schedule {
     return cudaSuccess;
   }
 
+  // KIND_FOUR_STEP (see plan_four_step) over this range of the batch.  Out
+  // of place: in -> out (transpose), out (length n1), out -> ws (twiddled
+  // transpose), ws (length n2), ws -> out (transpose).  In place the first
+  // transpose goes to ws and the last result comes back by a copy.
+  cudaError_t run_four_step(const char *in, char *out) {
+    const int64_t n1 = p->side[0], n2 = p->side[1];
+    const int f64 = p->dtype == FFT_C2C_F64;
+    const size_t elem = this->elem();
+    const char *lo = static_cast<const char *>(p->rtw);
+    const char *hi = lo + ((size_t)1 << p->rtw_log_s) * elem;
+    char *a = in != out ? out : ws;  // holds [n2][k1] after the first two steps
+    char *b = in != out ? ws : out;  // holds [k1][k2] after the next two
+    cudaError_t e = cudaSuccess;
+    count += 3;
+    if (!dry) e = transpose_complex(f64, in, a, batch, n1, n2, st);
+    if (e != cudaSuccess) return e;
+    Schedule s1(p->axis_plan[0], st, dry, batch * n2, b0 * n2);
+    if ((e = s1.run(a, a)) != cudaSuccess) return e;
+    count += s1.count;
+    if (!dry)
+      e = transpose_twiddle_complex(f64, a, b, batch, n2, n1, p->n, lo, hi, p->rtw_log_s,
+                                    p->direction > 0, st);
+    if (e != cudaSuccess) return e;
+    Schedule s2(p->axis_plan[1], st, dry, batch * n1, b0 * n1);
+    if ((e = s2.run(b, b)) != cudaSuccess) return e;
+    count += s2.count;
+    if (dry) return cudaSuccess;
+    if (in != out) return transpose_complex(f64, b, out, batch, n1, n2, st);
+    if ((e = transpose_complex(f64, b, ws, batch, n1, n2, st)) != cudaSuccess) return e;
+    return cudaMemcpyAsync(out, ws, (size_t)batch * p->n * elem, cudaMemcpyDeviceToDevice, st);
+  }
+
   // Passes k_begin.. of `batch` transforms.  Pass k reads the previous
   // pass's output; intermediates alternate between the workspace and `out`
   // and the last pass always writes `out` (it reads and writes the same
@@ -836,6 +954,8 @@ struct Schedule {
         return run_nd(i, o);
       case KIND_ND_ANY:
         return run_nd_any(i, o);
+      case KIND_FOUR_STEP:
+        return run_four_step(i, o);
       case KIND_DFT: {
         ++count;
         if (dry) return cudaSuccess;

@@ -165,6 +165,12 @@ cudaError_t mixed_exec_f64(const void *in, void *out, long long batch, const Mix
 // (transpose.cu); in and out must not overlap.
 cudaError_t transpose_complex(int f64, const void *in, void *out, long long B, long long R,
                               long long C, cudaStream_t st);
+// The same with out[b][c][r] = in[b][r][c] W_N^{(r c) mod N}, W_N^e from the
+// split table hi[e >> log_s] lo[e & (2^log_s - 1)] of the forward root,
+// conjugated when conj != 0.
+cudaError_t transpose_twiddle_complex(int f64, const void *in, void *out, long long B,
+                                      long long R, long long C, long long N, const void *lo,
+                                      const void *hi, int log_s, int conj, cudaStream_t st);
 
 // Transforms of real sequences (real_*.cu).  On chip: N = 2H, H = 2^logh,
 // forward (dir < 0) batch x 2H reals -> batch x (H + 1) bins, inverse the

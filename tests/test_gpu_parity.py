@@ -350,15 +350,32 @@ def test_mixed_radix(fg, dtype, n):
     assert rel_rows(z[list(rows)], refi).max() <= tol(dtype, n)
 
 
-def test_mixed_radix_limits_route_to_bluestein(fg):
-    # Beyond the on-chip mixed-radix length (fp32 12288) a smooth length takes
-    # Bluestein: 12800 = 2^9 5^2.
-    n = 12800
-    x = workloads.normal_complex((2, n), 5500, np.complex64)
-    y = run_plan(fg, x, n, 2, 1, fg.FFT_FORWARD, F32)
-    ks = workloads.sample_indices(16, n, 5501)
-    ref = oracle.dft_bins(x[0].astype(np.complex128), ks)
-    assert np.linalg.norm(y[0][ks] - ref) / np.linalg.norm(ref) <= tol(F32, bluestein_len(n))
+# Smooth lengths beyond one block: four-step N = N1 N2 with both factors on
+# chip (transpose, N1-point transforms, twiddled transpose, N2-point
+# transforms, transpose); 16 sampled bins of two rows against the direct sum,
+# Parseval, the inverse round trip, and the in-place form.
+@pytest.mark.parametrize("dtype,n", [(F32, 12800), (F32, 100000), (F32, 59049), (F32, 78125),
+                                     (F32, 53760), (F64, 24576), (F64, 10000)])
+def test_four_step_smooth(fg, dtype, n):
+    batch = 3
+    x = workloads.normal_complex((batch, n), 5500 + n % 997, NP[dtype])
+    p = fg.Plan(n, batch, 1, fg.FFT_FORWARD, dtype)
+    assert p.num_kernels >= 5 and p.workspace_bytes > 0
+    p.close()
+    y = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, dtype)
+    t = tol(dtype, n)
+    ks = np.unique(np.concatenate([workloads.sample_indices(14, n, 5501), [0, n - 1]]))
+    for r in (0, batch - 1):
+        x64 = x[r].astype(np.complex128)
+        ref = oracle.dft_bins(x64, ks)
+        rms = np.linalg.norm(y[r]) / np.sqrt(n)
+        assert np.linalg.norm(y[r][ks] - ref) / (np.sqrt(ks.size) * rms) <= t
+        assert abs(np.sum(np.abs(x64) ** 2) - np.sum(np.abs(y[r].astype(np.complex128)) ** 2) / n) \
+            <= t * np.sum(np.abs(x64) ** 2)
+    z = run_plan(fg, y, n, batch, 1, fg.FFT_INVERSE, dtype, inplace=True)
+    assert rel_rows(z, x).max() <= 2 * t
+    w = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, dtype, inplace=True)
+    assert rel_rows(w, y).max() <= t
 
 
 def test_bluestein_large_prime_sampled(fg):

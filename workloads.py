@@ -26,6 +26,7 @@ Workloads (sizes and distributions):
 * ``any1``: 16384 transforms of 3000 = 2^3 3 5^3 points, fp32, re and im
   i.i.d. standard normal; forward then inverse.
 * ``any2``: the same with the prime length 3001.
+* ``any3``: 1024 transforms of 100000 = 2^5 5^5 points, fp32, N(0, 1).
 * ``nd1``: 4 volumes of 128 x 256 x 256 fp32 complex (256 MiB), standard
   normal; 3D forward then inverse.
 * ``real1``: 32768 real fp32 rows of 8192 samples (1 GiB), standard normal;
@@ -44,6 +45,7 @@ CONFIGS = {
     "conv1": dict(kind="conv", n=3072, nh=1025, batch=32768, dtype="f32", seed=6),
     "any1": dict(kind="fft1d", n=3000, batch=16384, dtype="f32", seed=7),
     "any2": dict(kind="fft1d", n=3001, batch=16384, dtype="f32", seed=10),
+    "any3": dict(kind="fft1d", n=100000, batch=1024, dtype="f32", seed=11),
     "nd1": dict(kind="fftnd", n=256, shape=(128, 256, 256), batch=4, dtype="f32", seed=8),
     "real1": dict(kind="real", n=8192, batch=32768, dtype="f32", seed=9),
 }
@@ -159,7 +161,7 @@ def config_input(name: str, scale_batch: int | None = None):
         return poly_coeffs((batch, c["n"]), c["seed"])
     if name == "conv1":
         return conv_signals(batch, c["n"], c["nh"], c["seed"])
-    if name in ("any1", "any2"):
+    if name in ("any1", "any2", "any3"):
         return normal_complex((batch, c["n"]), c["seed"])
     if name == "nd1":
         return normal_complex((batch,) + tuple(c["shape"]), c["seed"])
