@@ -50,10 +50,13 @@ SIGNATURES = {
     "fft_exec_host_chain": (_INT, [_VP, _INT, _VP, _VP, _VP, _VP, _I64, _VP]),
     "polymul": (_INT, [_VP, _I64, _VP, _I64, _VP, _VP]),
     "polymul_batched": (_INT, [_VP, _I64, _VP, _I64, _VP, _I64, _VP]),
+    "polymul_batched_host": (_INT, [_VP, _I64, _VP, _I64, _VP, _I64, _VP, _VP, _VP, _I64, _VP]),
     "polymul_noalloc": (_INT, [_VP, _I64, _VP, _I64, _VP, _VP]),
     "polymul_num_kernels": (_INT, [_I64, _I64]),
     "fft_convolve": (_INT, [_VP, _I64, _VP, _I64, _VP, _I64, _INT, _INT, _INT, _VP]),
     "fft_convolve_num_kernels": (_INT, [_I64, _I64, _I64, _INT, _INT, _INT]),
+    "fft_convolve_host": (_INT, [_VP, _I64, _VP, _I64, _VP, _I64, _INT, _INT, _INT, _VP, _VP,
+                                 _I64, _VP]),
     "fft_debug_radix2_pass": (_INT, [_VP, _VP, _I64, _I64, _INT, _VP]),
     "fft_device_status": (_INT, [_VP]),
     "fft_debug_wait_timeout": (_INT, [_I64, _VP]),
@@ -149,6 +152,12 @@ def polymul_batched(a_ptr: int, na: int, b_ptr: int, nb: int, c_ptr: int, batch:
     return _lib.polymul_batched(a_ptr, na, b_ptr, nb, c_ptr, batch, stream)
 
 
+def polymul_batched_host(a_host: int, na: int, b_host: int, nb: int, c_host: int, batch: int,
+                         dev_a: int, dev_b: int, dev_c: int, chunk: int, stream: int) -> int:
+    return _lib.polymul_batched_host(a_host, na, b_host, nb, c_host, batch, dev_a, dev_b, dev_c,
+                                     chunk, stream)
+
+
 def polymul_noalloc(a_ptr: int, na: int, b_ptr: int, nb: int, c_ptr: int, stream: int) -> int:
     """polymul without device allocation (fixed scratch; na+nb-1 <=
     POLYMUL_NOALLOC_MAX_LEN).  For callers that may not allocate."""
@@ -165,6 +174,13 @@ def polymul_num_kernels(na: int, nb: int) -> int:
 def fft_convolve(x_ptr: int, nx: int, h_ptr: int, nh: int, y_ptr: int, batch: int,
                  h_per_row: int, kind: int, dtype: int, stream: int) -> int:
     return _lib.fft_convolve(x_ptr, nx, h_ptr, nh, y_ptr, batch, h_per_row, kind, dtype, stream)
+
+
+def fft_convolve_host(x_host: int, nx: int, h_ptr: int, nh: int, y_host: int, batch: int,
+                      h_per_row: int, kind: int, dtype: int, dev_x: int, dev_y: int, chunk: int,
+                      stream: int) -> int:
+    return _lib.fft_convolve_host(x_host, nx, h_ptr, nh, y_host, batch, h_per_row, kind, dtype,
+                                  dev_x, dev_y, chunk, stream)
 
 
 def fft_convolve_num_kernels(nx: int, nh: int, batch: int, h_per_row: int, kind: int,

@@ -1141,6 +1141,47 @@ cudaError_t pipe_for_device(int chunks, HostPipe **out) {
   return cudaSuccess;
 }
 
+// Streams `batch` items through the device in chunks of `chunk`: for each
+// chunk, up() on the upload stream, compute() on the compute stream once the
+// upload is done, down() on the download stream once the compute is done;
+// forked from and joined back to `st`.  Each callback gets (first item,
+// count, stream) and returns a cudaError_t.  Calls on one device enqueue
+// under one lock (the pipeline's streams and events are shared).
+template <class Up, class Comp, class Down>
+int host_pipeline(long long batch, long long chunk, cudaStream_t st, Up up, Comp compute,
+                  Down down) {
+  if (chunk > batch) chunk = batch;
+  const long long nchunks = (batch + chunk - 1) / chunk;
+  if (nchunks > 4096) return FFT_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_pipe_mutex);
+  HostPipe *hp = nullptr;
+  cudaError_t e = pipe_for_device((int)nchunks, &hp);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // Fork: the three pipeline streams start after the work already on `st`.
+  if ((e = cudaEventRecord(hp->fork, st)) != cudaSuccess) return cuda_fail(e);
+  cudaStreamWaitEvent(hp->in, hp->fork, 0);
+  cudaStreamWaitEvent(hp->comp, hp->fork, 0);
+  cudaStreamWaitEvent(hp->out, hp->fork, 0);
+  for (long long k = 0; k < nchunks; ++k) {
+    const long long b0 = k * chunk;
+    const long long cnt = batch - b0 < chunk ? batch - b0 : chunk;
+    if ((e = up(b0, cnt, hp->in)) != cudaSuccess) return cuda_fail(e);
+    cudaEventRecord(hp->loaded[k], hp->in);
+    cudaStreamWaitEvent(hp->comp, hp->loaded[k], 0);
+    if ((e = compute(b0, cnt, hp->comp)) != cudaSuccess) return cuda_fail(e);
+    cudaEventRecord(hp->done[k], hp->comp);
+    cudaStreamWaitEvent(hp->out, hp->done[k], 0);
+    if ((e = down(b0, cnt, hp->out)) != cudaSuccess) return cuda_fail(e);
+  }
+  // Join: `st` continues after the last download.
+  cudaEventRecord(hp->join_comp, hp->comp);
+  cudaEventRecord(hp->join_out, hp->out);
+  cudaStreamWaitEvent(st, hp->join_comp, 0);
+  e = cudaStreamWaitEvent(st, hp->join_out, 0);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FFT_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1159,8 +1200,6 @@ int fft_exec_host_chain(const fft_plan *const *plans, int nplans, const void *ho
   if (misaligned(dev_a) || misaligned(dev_b)) return FFT_ERR_MISALIGNED;
   const long long batch = p0->batch;
   if (chunk > batch) chunk = batch;
-  const long long nchunks = (batch + chunk - 1) / chunk;
-  if (nchunks > 4096) return FFT_ERR_INVALID_ARG;
   // Every chunk's slices must start 16-byte aligned, like whole buffers.
   for (int k = 0; k < nplans; ++k)
     if (((size_t)chunk * in_tbytes(plans[k])) % 16 || ((size_t)chunk * out_tbytes(plans[k])) % 16 ||
@@ -1169,49 +1208,29 @@ int fft_exec_host_chain(const fft_plan *const *plans, int nplans, const void *ho
   for (int k = 0; k < nplans; ++k)
     if (plans[k]->real && dev_a == dev_b) return FFT_ERR_INVALID_ARG;  // real: out of place only
   const size_t in_bytes0 = in_tbytes(p0), out_bytes_last = out_tbytes(plans[nplans - 1]);
-
-  std::lock_guard<std::mutex> lock(g_pipe_mutex);
-  HostPipe *hp = nullptr;
-  cudaError_t e = pipe_for_device((int)nchunks, &hp);
-  if (e != cudaSuccess) return cuda_fail(e);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-  // Fork: the three pipeline streams start after the work already on `stream`.
-  if ((e = cudaEventRecord(hp->fork, st)) != cudaSuccess) return cuda_fail(e);
-  cudaStreamWaitEvent(hp->in, hp->fork, 0);
-  cudaStreamWaitEvent(hp->comp, hp->fork, 0);
-  cudaStreamWaitEvent(hp->out, hp->fork, 0);
-
   char *bufs[2] = {static_cast<char *>(dev_a), static_cast<char *>(dev_b)};
-  for (long long k = 0; k < nchunks; ++k) {
-    const long long b0 = k * chunk;
-    const long long cnt = batch - b0 < chunk ? batch - b0 : chunk;
-    e = cudaMemcpyAsync(bufs[0] + (size_t)b0 * in_bytes0,
-                        static_cast<const char *>(host_in) + (size_t)b0 * in_bytes0,
-                        (size_t)cnt * in_bytes0, cudaMemcpyHostToDevice, hp->in);
-    if (e != cudaSuccess) return cuda_fail(e);
-    cudaEventRecord(hp->loaded[k], hp->in);
-    cudaStreamWaitEvent(hp->comp, hp->loaded[k], 0);
-    for (int j = 0; j < nplans; ++j) {
-      const fft_plan *q = plans[j];
-      Schedule s(q, hp->comp, false, cnt, b0);
-      e = s.run(bufs[j % 2] + (size_t)b0 * in_tbytes(q), bufs[(j + 1) % 2] + (size_t)b0 * out_tbytes(q));
-      if (e != cudaSuccess) return cuda_fail(e);
-    }
-    cudaEventRecord(hp->done[k], hp->comp);
-    cudaStreamWaitEvent(hp->out, hp->done[k], 0);
-    e = cudaMemcpyAsync(static_cast<char *>(host_out) + (size_t)b0 * out_bytes_last,
-                        bufs[nplans % 2] + (size_t)b0 * out_bytes_last, (size_t)cnt * out_bytes_last,
-                        cudaMemcpyDeviceToHost, hp->out);
-    if (e != cudaSuccess) return cuda_fail(e);
-  }
-  // Join: `stream` continues after the last download.
-  cudaEventRecord(hp->join_comp, hp->comp);
-  cudaEventRecord(hp->join_out, hp->out);
-  cudaStreamWaitEvent(st, hp->join_comp, 0);
-  e = cudaStreamWaitEvent(st, hp->join_out, 0);
-  if (e != cudaSuccess) return cuda_fail(e);
-  return FFT_OK;
+  return host_pipeline(
+      batch, chunk, static_cast<cudaStream_t>(stream),
+      [&](long long b0, long long cnt, cudaStream_t s) {
+        return cudaMemcpyAsync(bufs[0] + (size_t)b0 * in_bytes0,
+                               static_cast<const char *>(host_in) + (size_t)b0 * in_bytes0,
+                               (size_t)cnt * in_bytes0, cudaMemcpyHostToDevice, s);
+      },
+      [&](long long b0, long long cnt, cudaStream_t s) {
+        for (int j = 0; j < nplans; ++j) {
+          const fft_plan *q = plans[j];
+          Schedule sc(q, s, false, cnt, b0);
+          cudaError_t e = sc.run(bufs[j % 2] + (size_t)b0 * in_tbytes(q),
+                                 bufs[(j + 1) % 2] + (size_t)b0 * out_tbytes(q));
+          if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+      },
+      [&](long long b0, long long cnt, cudaStream_t s) {
+        return cudaMemcpyAsync(static_cast<char *>(host_out) + (size_t)b0 * out_bytes_last,
+                               bufs[nplans % 2] + (size_t)b0 * out_bytes_last,
+                               (size_t)cnt * out_bytes_last, cudaMemcpyDeviceToHost, s);
+      });
 }
 
 int polymul_batched(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, int64_t *c,
@@ -1293,6 +1312,70 @@ int fft_convolve_num_kernels(int64_t nx, int64_t nh, int64_t batch, int h_per_ro
   if (convolve_setup(nx, nh, batch, h_per_row, kind, dtype, &ikind, &log_len) != FFT_OK)
     return 0;
   return convolve_num_kernels(ikind, dtype, log_len);
+}
+
+int polymul_batched_host(const int64_t *a_host, int64_t na, const int64_t *b_host, int64_t nb,
+                         int64_t *c_host, int64_t batch, int64_t *dev_a, int64_t *dev_b,
+                         int64_t *dev_c, int64_t chunk, void *stream) {
+  if (!a_host || !b_host || !c_host || !dev_a || !dev_b || !dev_c || na <= 0 || nb <= 0 ||
+      batch <= 0 || chunk <= 0)
+    return FFT_ERR_INVALID_ARG;
+  if (((uintptr_t)dev_a & 7u) || ((uintptr_t)dev_b & 7u) || ((uintptr_t)dev_c & 7u))
+    return FFT_ERR_MISALIGNED;
+  if (polymul_num_kernels(na, nb) == 0) return FFT_ERR_UNSUPPORTED;
+  const int64_t nc = na + nb - 1;
+  return host_pipeline(
+      batch, chunk, static_cast<cudaStream_t>(stream),
+      [&](long long b0, long long cnt, cudaStream_t s) {
+        cudaError_t e = cudaMemcpyAsync(dev_a + b0 * na, a_host + b0 * na, (size_t)cnt * na * 8,
+                                        cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return e;
+        return cudaMemcpyAsync(dev_b + b0 * nb, b_host + b0 * nb, (size_t)cnt * nb * 8,
+                               cudaMemcpyHostToDevice, s);
+      },
+      [&](long long b0, long long cnt, cudaStream_t s) {
+        const int rc = polymul_batched(dev_a + b0 * na, na, dev_b + b0 * nb, nb, dev_c + b0 * nc,
+                                       cnt, s);
+        return rc == FFT_OK ? cudaSuccess : (g_cuda_error != cudaSuccess ? g_cuda_error
+                                                                          : cudaErrorInvalidValue);
+      },
+      [&](long long b0, long long cnt, cudaStream_t s) {
+        return cudaMemcpyAsync(c_host + b0 * nc, dev_c + b0 * nc, (size_t)cnt * nc * 8,
+                               cudaMemcpyDeviceToHost, s);
+      });
+}
+
+int fft_convolve_host(const void *x_host, int64_t nx, const void *h, int64_t nh, void *y_host,
+                      int64_t batch, int h_per_row, int kind, int dtype, void *dev_x, void *dev_y,
+                      int64_t chunk, void *stream) {
+  if (!x_host || !h || !y_host || !dev_x || !dev_y || chunk <= 0) return FFT_ERR_INVALID_ARG;
+  int ikind = 0, log_len = 0;
+  const int rc = convolve_setup(nx, nh, batch, h_per_row, kind, dtype, &ikind, &log_len);
+  if (rc != FFT_OK) return rc;
+  const size_t elem = (kind == FFT_CONV_COMPLEX ? 8 : 4) * (dtype == FFT_C2C_F32 ? 1 : 2);
+  const int64_t ny = nx + nh - 1;
+  char *dx = static_cast<char *>(dev_x);
+  char *dy = static_cast<char *>(dev_y);
+  const char *hh = static_cast<const char *>(h);
+  return host_pipeline(
+      batch, chunk, static_cast<cudaStream_t>(stream),
+      [&](long long b0, long long cnt, cudaStream_t s) {
+        return cudaMemcpyAsync(dx + (size_t)b0 * nx * elem,
+                               static_cast<const char *>(x_host) + (size_t)b0 * nx * elem,
+                               (size_t)cnt * nx * elem, cudaMemcpyHostToDevice, s);
+      },
+      [&](long long b0, long long cnt, cudaStream_t s) {
+        const int r = fft_convolve(dx + (size_t)b0 * nx * elem, nx,
+                                   hh + (h_per_row ? (size_t)b0 * nh * elem : 0), nh,
+                                   dy + (size_t)b0 * ny * elem, cnt, h_per_row, kind, dtype, s);
+        return r == FFT_OK ? cudaSuccess : (g_cuda_error != cudaSuccess ? g_cuda_error
+                                                                         : cudaErrorInvalidValue);
+      },
+      [&](long long b0, long long cnt, cudaStream_t s) {
+        return cudaMemcpyAsync(static_cast<char *>(y_host) + (size_t)b0 * ny * elem,
+                               dy + (size_t)b0 * ny * elem, (size_t)cnt * ny * elem,
+                               cudaMemcpyDeviceToHost, s);
+      });
 }
 
 int fft_debug_radix2_pass(const void *in, void *out, int64_t n, int64_t half, int dtype,

@@ -237,6 +237,23 @@ int polymul_batched(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, 
                     int64_t batch, void *stream);
 
 /*
+ * polymul_batched_host -- polymul_batched of coefficient arrays in host
+ * memory, streamed through the device in chunks of `chunk` pairs: for each
+ * chunk its rows of a_host and b_host are copied to dev_a / dev_b, multiplied
+ * into dev_c (polymul_batched on that range) and copied back to c_host,
+ * overlapping across chunks on three internal streams.
+ *   a_host, b_host, c_host  host arrays of batch * na, batch * nb and
+ *             batch * (na + nb - 1) int64 (pinned for the copies to overlap).
+ *   dev_a, dev_b, dev_c     caller-owned device arrays of the same sizes,
+ *             8-byte aligned.
+ *   chunk     pairs per chunk (>= 1; at most 4096 chunks).
+ * Errors as polymul_batched; asynchronous on `stream`.
+ */
+int polymul_batched_host(const int64_t *a_host, int64_t na, const int64_t *b_host, int64_t nb,
+                         int64_t *c_host, int64_t batch, int64_t *dev_a, int64_t *dev_b,
+                         int64_t *dev_c, int64_t chunk, void *stream);
+
+/*
  * polymul_noalloc -- the same product as polymul for one pair, for callers
  * that must not allocate device memory where they need it (a plug-in whose
  * host application owns the device-memory budget, or a latency-critical
@@ -290,6 +307,24 @@ int fft_convolve(const void *x, int64_t nx, const void *h, int64_t nh, void *y, 
  * arguments are invalid). */
 int fft_convolve_num_kernels(int64_t nx, int64_t nh, int64_t batch, int h_per_row, int kind,
                              int dtype);
+
+/*
+ * fft_convolve_host -- fft_convolve of signals in host memory, streamed
+ * through the device in chunks of `chunk` rows: for each chunk the rows of
+ * x_host are copied to dev_x, convolved into dev_y (fft_convolve on that
+ * range of rows) and copied back to y_host, uploads, convolutions and
+ * downloads of different chunks overlapping on three internal streams
+ * (as fft_exec_host_chain).
+ *   x_host, y_host  host buffers of batch * nx and batch * (nx + nh - 1)
+ *             samples (pinned for the copies to overlap); x_host only read.
+ *   h         DEVICE pointer to the filter(s), as for fft_convolve.
+ *   dev_x, dev_y    caller-owned device buffers of the same full sizes.
+ *   chunk     rows per chunk (>= 1; at most 4096 chunks).
+ * Other arguments and errors as fft_convolve; asynchronous on `stream`.
+ */
+int fft_convolve_host(const void *x_host, int64_t nx, const void *h, int64_t nh, void *y_host,
+                      int64_t batch, int h_per_row, int kind, int dtype, void *dev_x, void *dev_y,
+                      int64_t chunk, void *stream);
 
 /*
  * fft_debug_radix2_pass -- test hook (not part of the transform API): one
