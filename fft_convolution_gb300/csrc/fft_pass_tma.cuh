@@ -281,11 +281,13 @@ inline bool tma_disabled() {
 
 // Multiprocessors of the current device (cached per device).
 inline int sm_count() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (!cache[dev]) cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev);
-  return cache[dev];
+  int v = cache[dev].load(std::memory_order_acquire);
+  if (v == 0 && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+    cache[dev].store(v, std::memory_order_release);
+  return v;
 }
 
 // Launches the TMA pass kernel, or returns cudaErrorNotSupported (nothing

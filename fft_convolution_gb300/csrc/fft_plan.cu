@@ -26,14 +26,18 @@ static __device__ int g_device_status;
 
 namespace fftgb {
 int *device_status_word() {
-  static int *cache[64] = {nullptr};
+  static std::atomic<int *> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!cache[dev]) {
+  int *w = cache[dev].load(std::memory_order_acquire);
+  if (!w) {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess) cache[dev] = static_cast<int *>(p);
+    if (cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess) {
+      w = static_cast<int *>(p);
+      cache[dev].store(w, std::memory_order_release);
+    }
   }
-  return cache[dev];
+  return w;
 }
 }  // namespace fftgb
 
