@@ -167,6 +167,8 @@ struct fft_plan {
   int64_t side[3];
   fft_plan *axis_plan[3];
   int axis_pass[3];
+  // KIND_ND with every axis as on-chip rows stored transposed (nd_rows_t).
+  int nd_rows_t;
 };
 
 namespace {
@@ -190,7 +192,7 @@ size_t out_tbytes(const fft_plan *p) {
 size_t ws_tbytes(const fft_plan *p) {
   if (p->kind == KIND_MULTI) return (size_t)p->n * complex_bytes(p);
   if (p->kind == KIND_REAL_EVEN || p->kind == KIND_REAL_ODD || p->kind == KIND_ND_ANY ||
-      p->kind == KIND_FOUR_STEP)
+      p->kind == KIND_FOUR_STEP || (p->kind == KIND_ND && p->nd_rows_t))
     return p->ws_stride;
   return 0;
 }
@@ -511,6 +513,26 @@ static fft_plan *plan_any_length(int64_t n, int64_t batch, int direction, int dt
   return p;
 }
 
+// Whether a power-of-two 2D / 3D plan runs every axis as rows with
+// transposed stores instead of rows plus column passes.  Measured on GB300
+// (fp32, one forward transform): faster when every side is 128 or 256
+// (256^2 x 512: 0.163 vs 0.170 ms; 128x256x256 x 4: 0.253 vs 0.264;
+// 256^3 x 2: 0.249 vs 0.264), slower for longer sides (2048^2 x 8: 0.240 vs
+// 0.209; 512^2 x 128: 0.188 vs 0.175; 32x512^2 x 4: 0.306 vs 0.263) and for
+// shorter ones (64^3 x 256: 0.649 vs 0.540).  FFT_GB300_ND_ROWS_T=0 / 1
+// forces the choice (sides 2^4 .. the transposed-store limit) for tuning.
+static int nd_rows_t_wanted(int rank, const int *logs, int dtype) {
+  const int lim = dtype == FFT_C2C_F32 ? rows_t_max_log_f32() : rows_t_max_log_f64();
+  int ok = 1, preferred = 1;
+  for (int k = 0; k < rank; ++k) {
+    if (logs[k] < 4 || logs[k] > lim) ok = 0;
+    if (logs[k] < 7 || logs[k] > 8) preferred = 0;
+  }
+  const char *env = getenv("FFT_GB300_ND_ROWS_T");
+  if (env && *env) return ok && atoi(env) != 0;
+  return ok && preferred;
+}
+
 // Plans a 2D / 3D transform whose sides are not all powers of two within
 // the one-kernel-per-axis limits (the caller validated the arguments and
 // the sizes).  The contiguous axis runs as a 1D plan of any length over
@@ -705,12 +727,27 @@ fft_plan *fft_plan_create_nd(int rank, const int64_t *shape, int64_t batch, int 
   p->rank = rank;
   p->dims = rank;
   for (int k = 0; k < rank; ++k) p->shape_log[k] = logs[k];
+  // Every axis as on-chip rows with transposed stores (contiguous reads in
+  // every pass) when each side fits one such block.
+  p->nd_rows_t = nd_rows_t_wanted(rank, logs, dtype);
   p->n = shape[rank - 1];
   p->logn = logs[rank - 1];
   p->elems = (int64_t)1 << total_log;
   p->batch = batch;
   p->direction = direction;
   p->dtype = dtype;
+  if (p->nd_rows_t) {
+    p->ws_stride = (size_t)p->elems * (dtype == FFT_C2C_F32 ? 8 : 16);
+    p->workspace_bytes = (size_t)batch * p->ws_stride;
+    cudaError_t e = cudaMalloc(&p->workspace, p->workspace_bytes);
+    if (e != cudaSuccess) {
+      g_cuda_error = e;
+      (void)cudaGetLastError();
+      delete p;
+      g_status = e == cudaErrorMemoryAllocation ? FFT_ERR_ALLOC : FFT_ERR_CUDA;
+      return nullptr;
+    }
+  }
   return p;
 }
 
@@ -770,7 +807,44 @@ struct Schedule {
   // an in-place column pass (stride = the product of the inner sides), from
   // the inner axes outward.  With an L2 budget set, one L2-sized group of
   // transforms at a time so the column passes read the rows' output from L2.
+  // KIND_ND with transposed-store rows: pass k transforms the contiguous
+  // axis of [R][L] and writes [L][R]; after `rank` passes the order is the
+  // original one.  Buffers: 2 passes in -> ws -> out; 3 passes in -> out ->
+  // ws -> out (in place: in -> ws -> in -> ws, then a copy back).
+  cudaError_t run_nd_rows_t(const char *in, char *out) {
+    const int r = p->rank;
+    int total_log = 0;
+    for (int k = 0; k < r; ++k) total_log += p->shape_log[k];
+    const char *src = in;
+    cudaError_t e = cudaSuccess;
+    for (int k = 0; k < r; ++k) {
+      // Pass k: contiguous axis = original axis r-1-k.
+      const int l = p->shape_log[r - 1 - k];
+      char *dst;
+      if (r == 2) {
+        dst = k == 0 ? ws : out;
+      } else if (in != out) {
+        dst = k == 1 ? ws : out;
+      } else {
+        dst = k == 1 ? out : ws;
+      }
+      ++count;
+      if (!dry) {
+        const long long rows = batch << (total_log - l);
+        e = p->dtype == FFT_C2C_F32
+                ? launch_rows_t_f32(l, p->direction, src, dst, rows, total_log - l, st)
+                : launch_rows_t_f64(l, p->direction, src, dst, rows, total_log - l, st);
+        if (e != cudaSuccess) return e;
+      }
+      src = dst;
+    }
+    if (!dry && src != out)
+      e = cudaMemcpyAsync(out, src, (size_t)batch * p->elems * elem(), cudaMemcpyDeviceToDevice, st);
+    return e;
+  }
+
   cudaError_t run_nd(const char *in, char *out) {
+    if (p->nd_rows_t) return run_nd_rows_t(in, out);
     const size_t tbytes = (size_t)p->elems * elem();
     const size_t budget = l2_group_bytes();
     long long g = budget ? (long long)(budget / tbytes) : batch;

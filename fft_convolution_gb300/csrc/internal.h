@@ -161,6 +161,16 @@ cudaError_t mixed_exec_f32(const void *in, void *out, long long batch, const Mix
 cudaError_t mixed_exec_f64(const void *in, void *out, long long batch, const MixedStages &ms,
                            const void *tw, int dir, cudaStream_t st);
 
+// Row transforms with transposed stores (rows_t_*.cu): `rows` rows of
+// length 2^logn, R = 2^log_r rows per matrix, [b][R][L] in -> [b][L][R] out.
+// cudaErrorNotSupported outside 4 <= logn <= rows_t_max_log_*().
+cudaError_t launch_rows_t_f32(int logn, int dir, const void *in, void *out, long long rows,
+                              int log_r, cudaStream_t st);
+cudaError_t launch_rows_t_f64(int logn, int dir, const void *in, void *out, long long rows,
+                              int log_r, cudaStream_t st);
+int rows_t_max_log_f32();
+int rows_t_max_log_f64();
+
 // Batched transpose of complex matrices, in [B][R][C] -> out [B][C][R]
 // (transpose.cu); in and out must not overlap.
 cudaError_t transpose_complex(int f64, const void *in, void *out, long long B, long long R,

@@ -1,0 +1,19 @@
+// rows_t_f64.cu -- double instantiations of the row transforms with transposed
+// stores (fft_rows_t.cuh).
+#include "fft_rows_t.cuh"
+
+namespace fftgb {
+
+cudaError_t launch_rows_t_f64(int logn, int dir, const void *in, void *out, long long rows,
+                              int log_r, cudaStream_t st) {
+  return dir < 0 ? dispatch_rows_t<double, -1>(logn, in, out, rows, log_r, st)
+                 : dispatch_rows_t<double, 1>(logn, in, out, rows, log_r, st);
+}
+
+int rows_t_max_log_f64() {
+  // Largest length whose transposed-store kernel fits one block (1024
+  // threads, 227 KB of shared memory: 2 rows of 4096 doubles staged).
+  return 12;
+}
+
+}  // namespace fftgb

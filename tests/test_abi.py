@@ -73,10 +73,11 @@ def test_plan_create_rejects(fg, args, status):
 @pytest.mark.parametrize("n,dims,dtype,kernels", [
     (1, 1, 0, 1), (1024, 1, 0, 1), (1 << 14, 1, 0, 1), (1 << 13, 1, 1, 1),
     (12, 1, 0, 1), (63, 1, 1, 1),  # short non-power-of-two lengths: the direct DFT
-    (64, 2, 0, 2), (2048, 2, 0, 2), (1 << 13, 2, 1, 2), (1, 2, 0, 1)])
+    (1, 2, 0, 1)])
 def test_on_chip_plans_need_no_device(fg, n, dims, dtype, kernels):
-    # Single-kernel and 2D plans own no workspace, so they are created
-    # without touching the device.
+    # Single-kernel plans own no workspace, so they are created without
+    # touching the device.  (2D plans of power-of-two sides own one for their
+    # transposed-store passes.)
     h = fg._lib.fft_plan_create(n, 3, dims, -1, dtype)
     assert h
     assert fg.fft_plan_num_kernels(h) == kernels

@@ -234,8 +234,41 @@ def test_nd_large_3d(fg):
     x = workloads.uniform_complex((1,) + shape, 3600, np.complex64)
     y = fg.fftn(torch.from_numpy(x).cuda(), 3)
     torch.cuda.synchronize()
-    ref = np.fft.fftn(x.astype(np.complex128), axes=(1, 2, 3))
+    ref = oracle.fftn(x.astype(np.complex128), 3)
     assert rel_rows(y.cpu().numpy(), ref).max() <= tol(F32, int(np.prod(shape)))
+
+
+# Every axis as on-chip rows with transposed stores: the default when every
+# side is 128 or 256, forced here (FFT_GB300_ND_ROWS_T=1) on other sides
+# too; out of place and in place (rank 3 in place ends with a copy).
+@pytest.mark.parametrize("dtype,shape,force", [
+    (F32, (128, 256), False), (F32, (256, 256), False), (F32, (128, 128, 256), False),
+    (F32, (64, 32), True), (F32, (16, 1024), True), (F32, (4096, 16), True),
+    (F32, (32, 16, 64), True), (F64, (256, 128), False), (F64, (64, 4096), True), (F64, (64, 8192), True),
+    (F64, (16, 32, 64), True)])
+def test_nd_rows_transposed(fg, monkeypatch, dtype, shape, force):
+    if force:
+        monkeypatch.setenv("FFT_GB300_ND_ROWS_T", "1")
+    batch = 3
+    x = workloads.normal_complex((batch,) + shape, 3700 + sum(shape), NP[dtype])
+    p = fg.Plan(0, batch, direction=fg.FFT_FORWARD, dtype=dtype, shape=shape)
+    pi = fg.Plan(0, batch, direction=fg.FFT_INVERSE, dtype=dtype, shape=shape)
+    assert p.num_kernels == len(shape)
+    # Sides beyond the transposed-store limit (2^12) keep the column passes.
+    assert (p.workspace_bytes > 0) == (max(shape) <= 4096)
+    d = torch.from_numpy(x).cuda()
+    y = p.exec(d)
+    z = pi.exec(y)
+    torch.cuda.synchronize()
+    npts = int(np.prod(shape))
+    ref = oracle.fftn(x.astype(np.complex128), len(shape))
+    assert rel_rows(y.cpu().numpy(), ref).max() <= tol(dtype, npts)
+    assert rel_rows(z.cpu().numpy(), x).max() <= 2 * tol(dtype, npts)
+    p.exec(d, d)
+    torch.cuda.synchronize()
+    assert rel_rows(d.cpu().numpy(), ref).max() <= tol(dtype, npts)
+    p.close()
+    pi.close()
 
 
 def test_nd_rejects(fg):
