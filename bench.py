@@ -230,8 +230,7 @@ KERNEL_SOURCES = {
     "any2": ["fft_device.cuh", "fft_rows.cuh", "conv.cuh", "anylen.cuh", "anylen_f32.cu"],
     "any3": ["fft_device.cuh", "mixed.cuh", "mixed_f32.cu", "transpose.cu", "fft_plan.cu"],
     "real1": ["fft_device.cuh", "fft_rows.cuh", "real.cuh", "real_f32.cu"],
-    "nd1": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_f32.cu", "fft_pass.cuh",
-            "fft_pass_tma.cuh", "fft_pass_f32.cu", "fft_plan.cu"],
+    "nd1": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_t.cuh", "rows_t_f32.cu", "fft_plan.cu"],
 }
 
 
