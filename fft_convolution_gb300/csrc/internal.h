@@ -1,5 +1,6 @@
 // internal.h -- declarations shared between the library's translation units
-// (kernel launchers and the C ABI in fft_plan.cu).  Not installed.
+// (kernel launchers and the C ABI in fft_plan.cu, fft_exec.cu, fft_ops.cu).
+// Not installed.
 #pragma once
 
 #include <cuda_runtime.h>
