@@ -62,8 +62,8 @@ __global__ void __launch_bounds__(kTile *kRowsPerPass)
     for (int j = threadIdx.y; j < kTile; j += kRowsPerPass) {
       const long long r = r0 + j, c = c0 + threadIdx.x;
       if (r < R && c < C) {
-        const long long e = (long long)(((unsigned long long)r * (unsigned long long)c) %
-                                        (unsigned long long)N);
+        long long e = r * c;  // < N when R C = N (the four-step), so no reduction
+        if (e >= N) e %= N;
         V w = c_mul(hi[e >> log_s], lo[e & mask]);
         if (conj) w.y = -w.y;
         tile[j][threadIdx.x] = c_mul(src[r * C + c], w);
