@@ -70,3 +70,46 @@ def test_polymul_host(fg, na, nb, batch, chunk):
     assert rc == 0, fg.fft_status_string(rc)
     for r in range(batch):
         assert np.array_equal(hc[r].numpy(), oracle.polymul_schoolbook(a[r], b[r]))
+
+
+@pytest.mark.parametrize("kind", ["c2c", "real_fwd", "real_inv", "nd"])
+def test_exec_host_single_shot(fg, kind):
+    # fft_exec_host: upload, transform and download on one stream, with the
+    # plan's own input and output sizes (real plans differ).
+    if kind == "c2c":
+        n, batch = 3000, 4
+        p = fg.Plan(n, batch, 1, fg.FFT_FORWARD, fg.FFT_C2C_F32)
+        x = workloads.normal_complex((batch, n), 9950, np.complex64)
+        ref = np.stack([oracle.dft(r.astype(np.complex128)) for r in x])
+        out_shape, out_dt = (batch, n), torch.complex64
+    elif kind == "real_fwd":
+        n, batch = 1000, 3
+        p = fg.Plan(n, batch, 1, fg.FFT_FORWARD, fg.FFT_REAL_F32)
+        x = workloads.normal_real((batch, n), 9951, np.float32)
+        ref = oracle.rfft(x.astype(np.float64))
+        out_shape, out_dt = (batch, n // 2 + 1), torch.complex64
+    elif kind == "real_inv":
+        n, batch = 1000, 3
+        p = fg.Plan(n, batch, 1, fg.FFT_INVERSE, fg.FFT_REAL_F32)
+        g = workloads.generator(9952)
+        x = (g.standard_normal((batch, n // 2 + 1)) +
+             1j * g.standard_normal((batch, n // 2 + 1))).astype(np.complex64)
+        ref = oracle.irfft(x.astype(np.complex128), n)
+        out_shape, out_dt = (batch, n), torch.float32
+    else:
+        shape, batch = (30, 64), 2
+        p = fg.Plan(0, batch, direction=fg.FFT_FORWARD, dtype=fg.FFT_C2C_F32, shape=shape)
+        x = workloads.normal_complex((batch,) + shape, 9953, np.complex64)
+        ref = oracle.fftn(x.astype(np.complex128), 2).reshape(batch, -1)
+        out_shape, out_dt = (batch,) + shape, torch.complex64
+    hin = torch.from_numpy(x).pin_memory()
+    hout = torch.empty(out_shape, dtype=out_dt).pin_memory()
+    din = torch.empty_like(hin, device="cuda")
+    dout = torch.empty(out_shape, dtype=out_dt, device="cuda")
+    p.exec_host(hin, hout, din, dout)
+    torch.cuda.synchronize()
+    got = hout.numpy().reshape(ref.shape[0], -1).astype(np.complex128)
+    want = ref.reshape(ref.shape[0], -1)
+    err = np.linalg.norm(got - want, axis=1) / np.linalg.norm(want, axis=1)
+    assert err.max() <= 1e-5 * 13
+    p.close()
