@@ -616,7 +616,7 @@ def run_gpu(args):
                                          hc.data_ptr(), c["batch"], a_d.data_ptr(),
                                          b_d.data_ptr(), c_d.data_ptr(), chunk, sh)
             assert rc == 0, fg.fft_status_string(rc)
-        t = time_host_steps(e2e_step, stream, 3, warmup=1)
+        t = time_host_steps(e2e_step, stream, 5, warmup=2)
         e2e_ms = t["median_ms"]
         e2e = {"value": info["bytes_per_step"] * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": info["h2d"], "d2h_bytes_per_step": info["d2h"],

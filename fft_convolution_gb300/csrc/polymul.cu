@@ -11,7 +11,7 @@
 //  1. z = a + i b, zero-padded to L = 2^log_len >= na + nb - 1; Z = FFT_L(z)
 //     (the int64 -> fp64 conversion and the padding happen in the first
 //     pass's loads).
-//  2. combine (one O(L) kernel), for k < L/2:
+//  2. combine (in the loads of the inverse's first pass), for k < L/2:
 //        A_k = (Z_k + conj Z_{L-k}) / 2,   B_k = (Z_k - conj Z_{L-k}) / (2i)
 //        C_k = A_k B_k  (the pointwise product of the point values),
 //     and the same at k + L/2; then
@@ -58,28 +58,33 @@ __global__ void poly_twiddle_tables(double2 *lo, int n_lo, double2 *hi, int n_hi
   if (j < n_hi) hi[j] = twiddle<+1>((long long)j << lb, log_len, 0.0);
 }
 
-__global__ void poly_combine(const double2 *__restrict__ Z, double2 *__restrict__ Y,
-                             const double2 *__restrict__ tw_lo, const double2 *__restrict__ tw_hi,
-                             int lb, int log_len, long long batch) {
-  const long long L = 1LL << log_len, H = L >> 1;
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= batch * H) return;
-  const long long p = idx / H, k = idx % H;
-  const double2 *z = Z + p * L;
-  const double2 zk = z[k], zmk = z[(L - k) & (L - 1)];
-  const double2 zh = z[k + H], zmh = z[H - k];
-  // A B = (u + conj w)(u - conj w) / (2i) / 2 = (u^2 - conj(w)^2) (-i/4) with
-  // u = Z_k, w = Z_{L-k}; returned halved (C/2), the factor E and O need.
-  auto half_product = [](double2 u, double2 w) {
-    const double re = u.x * u.y + w.x * w.y;                    // Im(u^2 - conj(w)^2) / 2
-    const double im = (u.x * u.x - u.y * u.y) - (w.x * w.x - w.y * w.y);  // Re(...)
-    return make_c<double2>(0.25 * re, -0.125 * im);
-  };
-  const double2 Ck = half_product(zk, zmk), Ch = half_product(zh, zmh);  // C/2
-  const double2 w = c_mul(tw_hi[k >> lb], tw_lo[k & ((1LL << lb) - 1)]);  // W_L^{-k}
-  const double2 O = c_mul(c_sub(Ck, Ch), w);                               // O_k
-  Y[p * H + k] = make_c<double2>(Ck.x + Ch.x - O.y, Ck.y + Ch.y + O.x);    // E_k + i O_k
-}
+// Y_k (step 2) formed inside the first inverse pass's loads: the point-value
+// product of the two packed spectra and the even/odd packing read Z_k,
+// Z_{L-k}, Z_{k+L/2} and Z_{L/2-k} straight from the forward transform's
+// output, so the product never makes its own trip through HBM.
+struct LoadCombine {
+  const double2 *Z;
+  const double2 *tw_lo, *tw_hi;  // W_L^{-k} = tw_hi[k >> lb] tw_lo[k & (2^lb - 1)]
+  int lb;
+  long long L;
+  __device__ __forceinline__ double2 operator()(long long p, long long k) const {
+    const long long H = L >> 1;
+    const double2 *z = Z + p * L;
+    const double2 zk = z[k], zmk = z[(L - k) & (L - 1)];
+    const double2 zh = z[k + H], zmh = z[H - k];
+    // A B = (u + conj w)(u - conj w) / (2i) / 2 = (u^2 - conj(w)^2) (-i/4) with
+    // u = Z_k, w = Z_{L-k}; returned halved (C/2), the factor E and O need.
+    auto half_product = [](double2 u, double2 w) {
+      const double re = u.x * u.y + w.x * w.y;                              // Im(u^2 - conj(w)^2) / 2
+      const double im = (u.x * u.x - u.y * u.y) - (w.x * w.x - w.y * w.y);  // Re(...)
+      return make_c<double2>(0.25 * re, -0.125 * im);
+    };
+    const double2 Ck = half_product(zk, zmk), Ch = half_product(zh, zmh);  // C/2
+    const double2 w = c_mul(tw_hi[k >> lb], tw_lo[k & ((1LL << lb) - 1)]);  // W_L^{-k}
+    const double2 O = c_mul(c_sub(Ck, Ch), w);                               // O_k
+    return make_c<double2>(Ck.x + Ch.x - O.y, Ck.y + Ch.y + O.x);            // E_k + i O_k
+  }
+};
 
 // Inter-pass twiddle tables W_{2^log_lm}^e (direction dir) for e < 2^log_lm.
 __global__ void poly_pass_tables(double2 *lo, int lo_bits, double2 *hi, int log_lm, int dir) {
@@ -178,34 +183,31 @@ cudaError_t launch_polymul(const long long *a, long long na, const long long *b,
     log_m += logs[k];
   }
   double2 *Z = R[(P - 1) % 2];
-  double2 *Y = R[P % 2];
 
-  // 2. Y_k from Z (point-value product, then the even/odd packing).
-  {
-    const long long total = batch * H;
-    poly_combine<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(Z, Y, tw_lo, tw_hi, lb,
-                                                                  log_len, batch);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-
-  // 3. y = IFFT_{L/2}(Y), the last pass rounds into c.  Intermediates
-  // alternate between Z's buffer and Y's.
+  // 2 + 3. y = IFFT_{L/2}(Y) with Y formed in the first pass's loads (from Z,
+  // which that pass only reads); the last pass rounds into c.  Intermediates
+  // alternate between the other buffer and Z's.
   int ilogs[8];
   const int IP = split_passes(log_len - 1, ilogs);
-  const double2 *src = Y;
-  double2 *bufs[2] = {Z, Y};
+  const LoadCombine comb{Z, tw_lo, tw_hi, lb, L};
+  const StoreRoundPairsInt64 round_store{c, nc};
+  double2 *bufs[2] = {R[P % 2], Z};
+  const double2 *src = nullptr;
   log_m = 0;
   for (int k = 0; k < IP; ++k) {
-    if (k == IP - 1) {
-      e = poly_pass<+1>(ilogs[k], LC{src, H}, StoreRoundPairsInt64{c, nc}, log_len - 1, log_m,
-                        batch, st, itt);
+    const bool last = k == IP - 1;
+    double2 *dst = bufs[k % 2];
+    if (k == 0) {
+      e = last ? poly_pass<+1>(ilogs[k], comb, round_store, log_len - 1, log_m, batch, st, itt)
+               : poly_pass<+1>(ilogs[k], comb, SC{dst, H}, log_len - 1, log_m, batch, st, itt);
     } else {
-      double2 *dst = bufs[k % 2];
-      e = poly_pass<+1>(ilogs[k], LC{src, H}, SC{dst, H}, log_len - 1, log_m, batch, st, itt);
-      src = dst;
+      e = last ? poly_pass<+1>(ilogs[k], LC{src, H}, round_store, log_len - 1, log_m, batch, st,
+                               itt)
+               : poly_pass<+1>(ilogs[k], LC{src, H}, SC{dst, H}, log_len - 1, log_m, batch, st,
+                               itt);
     }
     if (e != cudaSuccess) return e;
+    src = dst;
     log_m += ilogs[k];
   }
   return cudaSuccess;
@@ -213,7 +215,7 @@ cudaError_t launch_polymul(const long long *a, long long na, const long long *b,
 
 int polymul_num_kernels(int log_len) {
   int logs[8];
-  return 3 + 1 + split_passes(log_len, logs) + split_passes(log_len - 1, logs);
+  return 3 + split_passes(log_len, logs) + split_passes(log_len - 1, logs);
 }
 
 }  // namespace fftgb

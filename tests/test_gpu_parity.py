@@ -479,7 +479,7 @@ def test_polymul_three_pass_forward(fg):
 
 
 def test_polymul_kernel_count(fg):
-    assert fg.polymul_num_kernels(1 << 20, 1 << 20) == 8   # 3 tables, 2 + 2 passes, combine
+    assert fg.polymul_num_kernels(1 << 20, 1 << 20) == 7   # 3 tables, 2 + 2 passes (product fused)
     assert fg.polymul_num_kernels(0, 5) == 0
 
 
