@@ -198,7 +198,7 @@ const char *fft_status_string(int status) {
   switch (status) {
     case FFT_OK: return "ok";
     case FFT_ERR_INVALID_ARG: return "invalid argument";
-    case FFT_ERR_NOT_POW2: return "length is not a power of two";
+    case FFT_ERR_NOT_POW2: return "not a power of two (no longer returned)";
     case FFT_ERR_UNSUPPORTED: return "unsupported size, type or dimensionality";
     case FFT_ERR_CUDA: return "CUDA error";
     case FFT_ERR_ALLOC: return "device allocation failed";

@@ -1,11 +1,16 @@
 /*
- * fft_gb300.h -- C ABI of the GB300 (sm_103a) power-of-two FFT library.
+ * fft_gb300.h -- C ABI of the GB300 (sm_103a) FFT library.
  *
  * Operations (all on one GPU, asynchronous on the caller's CUDA stream):
- *   - batched 1D complex-to-complex transforms of power-of-two length,
- *     forward (unscaled) and inverse (scaled by 1/N), fp32 or fp64;
- *   - the separable 2D transform of N x N images (rows, then columns);
- *   - integer polynomial multiplication through fp64 transforms.
+ *   - batched 1D complex-to-complex transforms of any length, forward
+ *     (unscaled) and inverse (scaled by 1/N), fp32 or fp64: powers of two on
+ *     chip or in 2-4 HBM passes; other lengths by the direct DFT (N <= 64),
+ *     mixed radix (prime factors 2, 3, 5, 7) or Bluestein;
+ *   - transforms of real sequences (half spectrum out / in, any length);
+ *   - separable 2D and 3D transforms of any sides (rows, then columns, ...);
+ *   - linear convolution of complex or real signals;
+ *   - integer polynomial multiplication through fp64 transforms;
+ *   - host-buffer forms of these, streamed through the device in chunks.
  *
  * Definitions followed:
  *   forward   X_k = sum_{n<N} x_n e^{-i 2 pi k n / N}
@@ -14,28 +19,32 @@
  *   inverse   x_n = (1/N) sum_{k<N} X_k e^{+i 2 pi k n / N}
  *             (same page, polynomial-multiplication section: omega replaced
  *             by omega^{-1} and the factor 1/N)
- *   2D        1D transforms along every row, then along every column
+ *   2D / 3D   1D transforms along every row, then along every column, ...
  *             ("Stockham FFT Butterfly Algorithm in Parallel GLSL",
  *             section Multi-Dimensional Transforms and Separability)
  *   polymul   c_k = sum_i a_i b_{k-i}, computed as transform, pointwise
  *             product of the point values, inverse transform ("FFT on GPU",
  *             polynomial-multiplication section, whole pipeline)
+ *   convolve  y_k = sum_i x_i h_{k-i}, the same pipeline for signals
  *
  * Data layout: complex arrays are interleaved (re, im) pairs of float
  * (FFT_C2C_F32) or double (FFT_C2C_F64) -- the layout of the pages' CUDA
  * code, and of torch.complex64 / torch.complex128.  A batch is contiguous:
- * transform b starts at element b*N (1D) or b*N*N (2D, row-major rows of N).
+ * transform b starts at element b * (number of points of one transform),
+ * multi-dimensional transforms row-major (the last side contiguous).
  *
- * Ownership: the caller owns every buffer passed in.  A plan owns only its
- * own workspace (allocated in fft_plan_create, freed in fft_plan_destroy).
- * polymul allocates its fp64 scratch stream-ordered on the given stream and
- * frees it the same way before returning.
+ * Ownership: the caller owns every buffer passed in.  A plan owns its
+ * workspace and tables (allocated in fft_plan_create / fft_plan_create_nd,
+ * freed in fft_plan_destroy).  polymul / fft_convolve allocate their scratch
+ * stream-ordered on the given stream and free it the same way.
  *
  * Errors: every call returns FFT_OK (0) or one FFT_ERR_* code; calls that
  * return a pointer return NULL and record the code for fft_last_status()
  * (per host thread).  Arguments are validated before anything is enqueued;
  * FFT_ERR_CUDA means a CUDA runtime call or kernel launch failed, and
- * fft_last_cuda_error() names it.  No call synchronises the device.
+ * fft_last_cuda_error() names it.  Execution calls never synchronise the
+ * device; plan creation may (it uploads or computes the plan's tables and
+ * waits for them).
  */
 #ifndef FFT_GB300_H
 #define FFT_GB300_H
@@ -50,7 +59,7 @@ extern "C" {
 /* Status codes. */
 #define FFT_OK 0
 #define FFT_ERR_INVALID_ARG 1 /* null pointer, size <= 0, bad enum value       */
-#define FFT_ERR_NOT_POW2 2    /* a 2D / 3D side is not a power of two           */
+#define FFT_ERR_NOT_POW2 2    /* kept for compatibility: no call returns it now */
 #define FFT_ERR_UNSUPPORTED 3 /* valid but not implemented (size / dtype / dims) */
 #define FFT_ERR_CUDA 4        /* CUDA runtime error or launch failure           */
 #define FFT_ERR_ALLOC 5       /* device allocation failed                       */
@@ -110,12 +119,16 @@ typedef struct fft_plan fft_plan;
  * into factors of at most 2^9) and need a workspace of batch * n elements,
  * allocated here on the current device.  Lengths that are not powers of two
  * ("FFT on GPU", sections FFT on GPU and Algorithm per signal Length): up to
- * 64 the direct DFT, one kernel; beyond, Bluestein's algorithm -- a
- * power-of-two convolution of length M >= 2n - 1 with a chirp -- whose chirp
- * and filter spectrum are computed here (small kernels on the legacy default
- * stream, waited for) and kept by the plan, plus 2 * batch * M work elements
- * when M exceeds the on-chip length.  Returns NULL on error
- * (fft_last_status(): INVALID_ARG, NOT_POW2 (2D only), UNSUPPORTED, ALLOC,
+ * 64 the direct DFT, one kernel; lengths whose only prime factors are 2, 3,
+ * 5 and 7 up to 12288 (fp32) / 6144 (fp64) as mixed-radix Stockham stages
+ * in one on-chip kernel; longer such lengths as N = N1 N2 (four-step: two
+ * mixed-radix plans between three transposes, the middle one applying the
+ * twiddles W_N^{n1 k2}; workspace batch * n); every other length by
+ * Bluestein's algorithm -- a power-of-two convolution of length M >= 2n - 1
+ * with a chirp -- whose chirp and filter spectrum are computed here (small
+ * kernels on the legacy default stream, waited for) and kept by the plan,
+ * plus 2 * batch * M work elements when M exceeds the on-chip length.
+ * Returns NULL on error (fft_last_status(): INVALID_ARG, UNSUPPORTED, ALLOC,
  * CUDA).
  */
 fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int dtype);
@@ -129,7 +142,10 @@ fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int
  * in all).  The inverse scales by 1/(product of the sides).  When every
  * side is a power of two, the last at most 2^14 (fp32) / 2^13 (fp64) and
  * the others at most the same, the plan is one on-chip row kernel plus one
- * in-place column pass per other axis, with no workspace.  Otherwise the
+ * in-place column pass per other axis, with no workspace -- except when
+ * every side is 128 or 256: then each axis is one on-chip row kernel that
+ * stores its output transposed (the next axis becomes contiguous), with a
+ * workspace of batch * elements.  Otherwise the
  * contiguous axis runs as a 1D plan of any length (fft_plan_create), and
  * every other axis either as an in-place column pass (power-of-two length
  * and stride) or through a transpose into a workspace of batch * elements,
