@@ -45,8 +45,13 @@ template <typename T, int LOGL> struct PassConfig {
   static constexpr int ROW_ELEMS =
       P::SMEM_ELEMS > P::L + 1 ? P::SMEM_ELEMS : P::L + 1;  // exchange or transpose
   static constexpr int EXCHANGE_ELEMS = C * ROW_ELEMS;
-  // Exchange space, then the stage-twiddle table shared by the tile's columns.
-  static constexpr size_t SMEM = ((size_t)EXCHANGE_ELEMS + P::TW_ELEMS) * sizeof(vec2_t<T>);
+  // Exchange space, then the stage-twiddle table shared by the tile's
+  // columns -- unless the two together would not fit shared memory (fp64,
+  // L = 2^13): then the stage twiddles are computed.
+  static constexpr bool TABLE =
+      ((size_t)EXCHANGE_ELEMS + P::TW_ELEMS) * sizeof(vec2_t<T>) <= 200 * 1024;
+  static constexpr size_t SMEM =
+      ((size_t)EXCHANGE_ELEMS + (TABLE ? P::TW_ELEMS : 0)) * sizeof(vec2_t<T>);
 };
 
 // Plain complex load / store (element `pos` of transform `b`).
@@ -108,7 +113,7 @@ __global__ void __launch_bounds__(PassConfig<T, LOGL>::THREADS, PassConfig<T, LO
   const int c = threadIdx.x % C;   // column within the tile
   const int t = threadIdx.x / C;   // thread within the column
   const long long cols = 1LL << (g.log_n - LOGL);  // N / L butterflies
-  fill_twiddle_table<LOGL, DIR>(twt, threadIdx.x, Cfg::THREADS);
+  if constexpr (Cfg::TABLE) fill_twiddle_table<LOGL, DIR>(twt, threadIdx.x, Cfg::THREADS);
   __syncthreads();
 
   for (long long blk = blockIdx.x; blk < g.total; blk += gridDim.x) {
@@ -146,7 +151,7 @@ __global__ void __launch_bounds__(PassConfig<T, LOGL>::THREADS, PassConfig<T, LO
     }
 
     const SmemView<V> sm{smem + c, C};
-    fft_on_chip<LOGL, DIR, true>(x, t, sm, twt);
+    fft_on_chip<LOGL, DIR, Cfg::TABLE>(x, t, sm, Cfg::TABLE ? twt : nullptr);
 
     if constexpr (DIR > 0) {
 #pragma unroll
@@ -223,6 +228,9 @@ cudaError_t launch_pass_t(Load load, Store store, int log_n, int log_m, int twid
 template <typename T, int LOGL, int DIR>
 cudaError_t launch_pass_tma_t(const void *in, void *out, int log_n, int log_m, int twiddle,
                               long long batch, cudaStream_t st);
+template <typename T, int LOGL, int DIR>
+cudaError_t launch_pass_cluster_t(const void *in, void *out, int log_n, int log_m, int twiddle,
+                                  long long batch, cudaStream_t st);
 
 template <typename T, int DIR, int MAXLOG, int LOGL = 1>
 cudaError_t dispatch_pass(const PassArgs &a, const void *in, void *out, cudaStream_t st) {
@@ -233,8 +241,10 @@ cudaError_t dispatch_pass(const PassArgs &a, const void *in, void *out, cudaStre
       using V = vec2_t<T>;
       const long long n = 1LL << a.log_n;
       if (a.subset.runs == 0) {
-        cudaError_t e = launch_pass_tma_t<T, LOGL, DIR>(in, out, a.log_n, a.log_m, a.twiddle,
-                                                        a.batch, st);
+        cudaError_t e = launch_pass_cluster_t<T, LOGL, DIR>(in, out, a.log_n, a.log_m,
+                                                            a.twiddle, a.batch, st);
+        if (e != cudaErrorNotSupported) return e;
+        e = launch_pass_tma_t<T, LOGL, DIR>(in, out, a.log_n, a.log_m, a.twiddle, a.batch, st);
         if (e != cudaErrorNotSupported) return e;
       }
       return launch_pass_t<T, LOGL, DIR>(LoadComplex<V>{static_cast<const V *>(in), n},

@@ -1,6 +1,6 @@
 // fft_pass_f64.cu -- instantiates the HBM pass / 2D column pass kernel for
 // double complex data, every supported on-chip length, both directions.
-#include "fft_pass_tma.cuh"
+#include "fft_pass_cluster.cuh"
 
 namespace fftgb {
 

@@ -68,6 +68,29 @@ int pass_log_limit(int dtype) {
   return lim > hard ? hard : lim;
 }
 
+// FFT_GB300_PASS_SPLIT = "a,b[,c...]" (tuning and tests): the passes of a
+// multi-pass transform of 2^logn points, first pass first, when the factors
+// add up to logn and each is within 1 .. the pass kernels' limit.  Returns
+// the number of passes, or 0 (no override, or one that does not apply).
+static int pass_split_override(int logn, int dtype, int *split) {
+  const char *env = getenv("FFT_GB300_PASS_SPLIT");
+  if (!env || !*env) return 0;
+  const int hard = dtype == FFT_C2C_F32 ? kPassMaxLogF32 : kPassMaxLogF64;
+  int count = 0, sum = 0;
+  const char *s = env;
+  while (*s) {
+    char *end = nullptr;
+    const long v = strtol(s, &end, 10);
+    if (end == s || v < 1 || v > hard || count == kMaxPasses) return 0;
+    split[count++] = (int)v;
+    sum += (int)v;
+    s = end;
+    if (*s == ',') ++s;
+    else if (*s) return 0;
+  }
+  return count >= 2 && sum == logn ? count : 0;
+}
+
 // Bytes of data an L2-grouped schedule keeps in flight between two
 // dependent kernels so that the second finds the first's output in L2.
 // Measured on GB300, grouping 2D images (32 MiB) or fusing the first two
@@ -531,18 +554,24 @@ fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int
     return nullptr;
   }
   // Stockham passes over HBM: logn split into nearly equal factors of at
-  // most pass_log_limit bits, larger factors first.
-  const int lim = pass_log_limit(dtype);
-  int P = (logn + lim - 1) / lim;
-  if (P < 2) P = 2;
-  if (P > kMaxPasses) {
-    delete p;
-    g_status = FFT_ERR_UNSUPPORTED;
-    return nullptr;
+  // most pass_log_limit bits, larger factors first (or the split
+  // FFT_GB300_PASS_SPLIT names).
+  int split[kMaxPasses];
+  int P = pass_split_override(logn, dtype, split);
+  if (P == 0) {
+    const int lim = pass_log_limit(dtype);
+    P = (logn + lim - 1) / lim;
+    if (P < 2) P = 2;
+    if (P > kMaxPasses) {
+      delete p;
+      g_status = FFT_ERR_UNSUPPORTED;
+      return nullptr;
+    }
+    for (int k = 0; k < P; ++k) split[k] = logn / P + (k < logn % P ? 1 : 0);
   }
   p->kind = KIND_MULTI;
   p->npasses = P;
-  for (int k = 0; k < P; ++k) p->pass_log[k] = logn / P + (k < logn % P ? 1 : 0);
+  for (int k = 0; k < P; ++k) p->pass_log[k] = split[k];
   p->workspace_bytes = (size_t)batch * (size_t)n * elem;
   cudaError_t e = cudaMalloc(&p->workspace, p->workspace_bytes);
   if (e != cudaSuccess) {

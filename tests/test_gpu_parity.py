@@ -158,6 +158,59 @@ def test_lsu_pass_kernel(fg, monkeypatch, dims, dtype, logn):
     assert rel_rows(y, ref).max() <= tol(dtype, npts)
 
 
+# --- passes whose on-chip length (2^11 .. 2^13) is split over a cluster --------
+
+@pytest.mark.parametrize("dtype,logn,split,batch", [
+    (F32, 22, "11,11", 1),   # clusters of 2 in both passes
+    (F32, 20, "13,7", 2),    # clusters of 8 in the first pass (linear stores)
+    (F32, 20, "7,13", 2),    # clusters of 8 in the last pass (twiddled, TMA stores)
+    (F32, 24, "12,12", 1),   # clusters of 4
+    (F32, 17, "4,13", 3),    # last pass with m = 16 (four tiles per block of m)
+    (F32, 15, "13,2", 2),    # first pass with 4 columns: one tile per transform
+    (F32, 21, "7,12,2", 1),  # a middle pass
+    (F64, 21, "11,10", 1),
+    (F64, 20, "8,12", 2),
+])
+def test_cluster_passes(fg, monkeypatch, dtype, logn, split, batch):
+    monkeypatch.setenv("FFT_GB300_PASS_SPLIT", split)
+    monkeypatch.setenv("FFT_GB300_CLUSTER_LOG_MIN", "11")  # clusters of 2 as well
+    n = 1 << logn
+    x = workloads.normal_complex((batch, n), 6000 + logn, NP[dtype])
+    ref = oracle.fft(x.astype(np.complex128))
+    y = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, dtype)
+    assert rel_rows(y, ref).max() <= tol(dtype, n)
+    y2 = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, dtype, inplace=True)
+    assert rel_rows(y2, ref).max() <= tol(dtype, n)
+    z = run_plan(fg, y, n, batch, 1, fg.FFT_INVERSE, dtype)
+    assert rel_rows(z, oracle.ifft(y.astype(np.complex128))).max() <= tol(dtype, n)
+    assert fg.fft_device_status(stream()) == 0
+
+
+@pytest.mark.parametrize("split", ["13,11", "11,13", "12,12", "8,8,8"])
+def test_cluster_pass_splits_2e24(fg, monkeypatch, split):
+    # One 2^24 transform split into cluster passes of 2^11 .. 2^13 points
+    # (and, for comparison, into single-block passes), against the oracle at
+    # every bin, forward and inverse.
+    monkeypatch.setenv("FFT_GB300_PASS_SPLIT", split)
+    monkeypatch.setenv("FFT_GB300_CLUSTER_LOG_MIN", "11")
+    n = 1 << 24
+    x = workloads.normal_complex((1, n), 6100, np.complex64)
+    y = run_plan(fg, x, n, 1, 1, fg.FFT_FORWARD, F32)
+    assert rel_rows(y, oracle.fft(x.astype(np.complex128))).max() <= tol(F32, n)
+    z = run_plan(fg, y, n, 1, 1, fg.FFT_INVERSE, F32, inplace=True)
+    assert rel_rows(z, x.astype(np.complex128)).max() <= 2 * tol(F32, n)
+
+
+def test_cluster_pass_disabled_fallback(fg, monkeypatch):
+    # FFT_GB300_NO_CLUSTER: the same split runs on the single-block kernels.
+    monkeypatch.setenv("FFT_GB300_PASS_SPLIT", "12,10")
+    monkeypatch.setenv("FFT_GB300_NO_CLUSTER", "1")
+    n = 1 << 22
+    x = workloads.uniform_complex((1, n), 6200, np.complex64)
+    y = run_plan(fg, x, n, 1, 1, fg.FFT_FORWARD, F32)
+    assert rel_rows(y, oracle.fft(x.astype(np.complex128))).max() <= tol(F32, n)
+
+
 def test_device_status_clear_after_transforms(fg):
     # No bounded in-kernel wait ran out during the transforms above.
     assert fg.fft_device_status(stream()) == 0
@@ -197,7 +250,7 @@ def test_2d_forward_inverse(fg, dtype, logn):
     assert rel_rows(z, oracle.fft2d(y.astype(np.complex128), +1)).max() <= tol(dtype, n * n)
 
 
-@pytest.mark.parametrize("dtype,logn", [(F32, 11), (F32, 13), (F64, 12)])
+@pytest.mark.parametrize("dtype,logn", [(F32, 11), (F32, 12), (F32, 13), (F64, 11), (F64, 12)])
 def test_2d_large_sides(fg, dtype, logn):
     n = 1 << logn
     x = workloads.uniform_complex((1, n, n), 3100 + logn, NP[dtype])
@@ -211,7 +264,8 @@ def test_2d_large_sides(fg, dtype, logn):
 
 @pytest.mark.parametrize("dtype", [F32, F64])
 @pytest.mark.parametrize("shape", [(2, 8), (64, 32), (16, 1024), (1024, 16), (4, 8, 16),
-                                   (32, 16, 64), (2, 2, 2), (1, 16, 16), (128, 1, 4), (8, 4, 1)])
+                                   (32, 16, 64), (2, 2, 2), (1, 16, 16), (128, 1, 4), (8, 4, 1),
+                                   (2048, 8), (4096, 4), (8192, 2), (2, 4096, 4)])
 def test_nd_forward_inverse(fg, dtype, shape):
     batch = 3
     x = workloads.normal_complex((batch,) + shape, 3500 + sum(shape), NP[dtype])
@@ -227,6 +281,21 @@ def test_nd_forward_inverse(fg, dtype, shape):
     assert rel_rows(z.cpu().numpy(), x).max() <= 2 * tol(dtype, npts)
     p.close()
     pi.close()
+
+
+@pytest.mark.parametrize("dtype", [F32, F64])
+@pytest.mark.parametrize("shape", [(8192, 2), (2048, 4), (4096, 8)])
+def test_nd_columns_single_block(fg, monkeypatch, dtype, shape):
+    # Long columns on the single-block pass kernels (FFT_GB300_NO_CLUSTER);
+    # fp64 columns of 8192 compute their stage twiddles (no shared table).
+    monkeypatch.setenv("FFT_GB300_NO_CLUSTER", "1")
+    x = workloads.normal_complex((2,) + shape, 3550 + sum(shape), NP[dtype])
+    p = fg.Plan(0, 2, direction=fg.FFT_FORWARD, dtype=dtype, shape=shape)
+    y = p.exec(torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    ref = oracle.fftn(x.astype(np.complex128), len(shape))
+    assert rel_rows(y.cpu().numpy(), ref).max() <= tol(dtype, int(np.prod(shape)))
+    p.close()
 
 
 def test_nd_large_3d(fg):
