@@ -219,12 +219,13 @@ class ClockSampler:
 KERNEL_SOURCES = {
     "c1": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_f32.cu"],
     "c2": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_f32.cu"],
-    "c3": ["fft_device.cuh", "fft_pass.cuh", "fft_pass_tma.cuh", "fft_pass_f32.cu",
-           "fft_plan.cu", "fft_exec.cu", "plan.h"],
+    "c3": ["fft_device.cuh", "fft_pass.cuh", "fft_pass_tma.cuh", "fft_pass_cluster.cuh",
+           "fft_pass_f32.cu", "fft_plan.cu", "fft_exec.cu", "plan.h"],
     "c4": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_f32.cu", "fft_pass.cuh",
-           "fft_pass_tma.cuh", "fft_pass_f32.cu", "fft_plan.cu", "fft_exec.cu", "plan.h"],
-    "c5": ["fft_device.cuh", "fft_pass.cuh", "fft_pass_tma.cuh", "fft_pass_f64.cu",
-           "polymul.cu"],
+           "fft_pass_tma.cuh", "fft_pass_cluster.cuh", "fft_pass_f32.cu", "fft_plan.cu",
+           "fft_exec.cu", "plan.h"],
+    "c5": ["fft_device.cuh", "fft_pass.cuh", "fft_pass_tma.cuh", "fft_pass_cluster.cuh",
+           "fft_pass_f64.cu", "polymul.cu"],
     "conv1": ["fft_device.cuh", "fft_rows.cuh", "conv.cuh", "conv_f32.cu"],
     "any1": ["fft_device.cuh", "mixed.cuh", "mixed_f32.cu", "fft_plan.cu", "fft_exec.cu", "plan.h"],
     "any2": ["fft_device.cuh", "fft_rows.cuh", "conv.cuh", "anylen.cuh", "anylen_f32.cu"],

@@ -84,15 +84,6 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
-// Contiguous shared -> global copy by the bulk-copy engine (both addresses
-// 16-byte aligned, size a multiple of 16), tracked by the bulk group.
-__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                   reinterpret_cast<uint64_t>(dst)),
-               "r"(smem_addr(src)), "r"(bytes)
-               : "memory");
-}
-
 // Split of an on-chip length 2^LOGL over a cluster: L' = 2^10 rows per
 // block, R = L / L' blocks (2, 4 or 8: L = 2^11 .. 2^13), C columns of 32
 // bytes per tile (4 fp32, 2 fp64 complex values).  Shared memory: a load

@@ -74,6 +74,14 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, const void 
       "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
+// Contiguous shared -> global copy by the bulk-copy engine (both addresses
+// 16-byte aligned, size a multiple of 16), tracked by the bulk group.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_addr(src)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -100,7 +108,13 @@ template <typename T, int LOGL> struct TmaConfig {
   static constexpr int ROWS_PER_BOX = L < 256 ? L : 256;  // TMA box limit per dimension
   static constexpr int BOXES = L / ROWS_PER_BOX;
   static constexpr uint32_t TILE_BYTES = (uint32_t)(C * L * sizeof(V));
-  static constexpr int RAW_ELEMS = PassConfig<T, LOGL>::ROW_ELEMS * C;  // exchange / transpose
+  // First-pass staging stride: column c at c * RS.  RS - L = 32 / C (the
+  // rows one warp covers) spreads the writes of a warp's lanes evenly over
+  // the banks; at least 2 for fp32, so every column starts 16-byte aligned.
+  static constexpr int PAD = 32 / C >= 2 ? 32 / C : (sizeof(T) == 4 ? 2 : 1);
+  static constexpr int RS = L + PAD;
+  static constexpr int RAW_EX = PassConfig<T, LOGL>::ROW_ELEMS * C;  // exchange
+  static constexpr int RAW_ELEMS = RAW_EX > C * RS ? RAW_EX : C * RS;
   static constexpr int MIN_BLOCKS = THREADS >= 1024 ? 1 : (THREADS >= 512 ? 2 : (THREADS >= 256 ? 3 : 4));
   static constexpr int BUF_ELEMS =
       ((RAW_ELEMS * (int)sizeof(V) + 127) / 128) * 128 / (int)sizeof(V);
@@ -171,17 +185,18 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
     const int s = Cfg::NBUF == 2 ? (k & 1) : 0;
     V *const cur = buf0 + s * Cfg::BUF_ELEMS;
     const long long next = tile + gridDim.x;
-    __syncthreads();  // every thread is done with the previous tile's buffer
+    // The previous tile's stores (issued by threads < C) have left its
+    // buffer, and every thread is done with it.
+    if (tid < C) bulk_wait_read_all();
+    __syncthreads();
     bool prefetched = false;
     if (tid == 0) {
       if (Cfg::NBUF == 2) {
         if (next < g.total_tiles) {
-          bulk_wait_read_all();  // the previous tile's TMA store has left buffer s^1
           issue_load(next, s ^ 1);
           prefetched = true;
         }
       } else {
-        bulk_wait_read_all();  // the previous tile's TMA store has left the buffer
         issue_load(tile, 0);
       }
     }
@@ -217,16 +232,18 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
 
     __syncthreads();  // the last exchange has been read
     if (g.log_m == 0) {
-      // Outputs of butterfly i go to i*L + v: one contiguous block per tile.
-      constexpr int RS = L + 1;
+      // Outputs of butterfly i go to i*L + v: one contiguous block per tile,
+      // staged column by column (stride RS) and copied by the bulk-copy
+      // engine, one column of L values per thread c < C.
+      constexpr int RS = Cfg::RS;
 #pragma unroll
       for (int w = 0; w < P::E; ++w) cur[c * RS + t + w * P::TP] = x[w];
+      fence_async_smem();
       __syncthreads();
-      V *dst = out_linear + b * (1LL << g.log_n) + (tile % g.tiles_per_batch) * C * L;
-#pragma unroll
-      for (int w = 0; w < P::E; ++w) {
-        const int o = tid + w * Cfg::THREADS;
-        dst[o] = cur[(o / L) * RS + (o % L)];
+      if (tid < C) {
+        V *dst = out_linear + b * (1LL << g.log_n) + ((tile % g.tiles_per_batch) * C + tid) * L;
+        bulk_store(dst, cur + tid * RS, (uint32_t)(L * sizeof(V)));
+        bulk_commit();
       }
     } else {
       // Rows of the output tile are m elements apart: TMA tensor store.
@@ -246,7 +263,7 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
       }
     }
   }
-  if (tid == 0) bulk_wait_all();
+  if (tid < C) bulk_wait_all();
   (void)cols;
 }
 
