@@ -13,7 +13,8 @@
 //     the load/store units carry only the shared-memory exchanges;
 //   * outputs of passes with m > 1 (rows m elements apart) leave by a TMA
 //     tensor store from the same buffer; the first pass (m = 1), whose tile
-//     output is one contiguous block, keeps its linear coalesced stores.
+//     output is one contiguous block, stages it column by column and
+//     writes each column's L values with one bulk copy.
 // Every mbarrier wait is bounded: a wait that runs out records
 // kDeviceErrorTimeout in the device status word and the block stops
 // (fft_device_status reports it).
