@@ -65,6 +65,24 @@ def smooth_2357(n: int) -> bool:
     return n == 1
 
 
+def planned_passes(logn: int, pass_log: int) -> int:
+    """HBM passes the library plans for a 2^logn-point transform beyond the
+    on-chip length: the FFT_GB300_PASS_SPLIT / FFT_GB300_PASS_LOG tuning
+    overrides when set (as the planner reads them), else factors of at most
+    pass_log bits."""
+    split = os.environ.get("FFT_GB300_PASS_SPLIT", "")
+    try:
+        parts = [int(v) for v in split.split(",")] if split else []
+    except ValueError:
+        parts = []
+    if len(parts) >= 2 and sum(parts) == logn and all(1 <= v <= 14 for v in parts):
+        return len(parts)
+    env_log = os.environ.get("FFT_GB300_PASS_LOG", "")
+    if env_log.isdigit() and int(env_log) >= 4:
+        pass_log = min(int(env_log), 14)
+    return max(2, math.ceil(logn / pass_log))
+
+
 def workload_info(name: str, pass_log: int = 9):
     c = config_of(name)
     n, batch = c["n"], c["batch"]
@@ -76,7 +94,7 @@ def workload_info(name: str, pass_log: int = 9):
                     transforms_per_step=directions * batch, h2d=arr, d2h=arr,
                     flops_per_step=directions * 5.0 * n * math.log2(max(n, 2)) * batch)
         if n & (n - 1) == 0:
-            passes = 1 if log2i(n) <= 14 else max(2, math.ceil(log2i(n) / pass_log))
+            passes = 1 if log2i(n) <= 14 else planned_passes(log2i(n), pass_log)
         elif smooth_2357(n) and 64 < n <= 12288:
             passes = 1    # mixed radix on chip: one read, one write
             info.update(mixed=True)
