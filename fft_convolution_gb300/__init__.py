@@ -60,6 +60,7 @@ SIGNATURES = {
     "fft_debug_radix2_pass": (_INT, [_VP, _VP, _I64, _I64, _INT, _VP]),
     "fft_device_status": (_INT, [_VP]),
     "fft_debug_wait_timeout": (_INT, [_I64, _VP]),
+    "fft_debug_cluster_timeout": (_INT, [_VP, _I64, _VP]),
     "fft_last_status": (_INT, []),
     "fft_status_string": (ctypes.c_char_p, [_INT]),
     "fft_last_cuda_error": (ctypes.c_char_p, []),
@@ -195,6 +196,10 @@ def fft_debug_radix2_pass(in_ptr: int, out_ptr: int, n: int, half: int, dtype: i
 
 def fft_debug_wait_timeout(polls: int, stream: int) -> int:
     return int(_lib.fft_debug_wait_timeout(polls, stream))
+
+
+def fft_debug_cluster_timeout(data_ptr: int, polls: int, stream: int) -> int:
+    return int(_lib.fft_debug_cluster_timeout(data_ptr, polls, stream))
 
 
 def fft_device_status(stream: int) -> int:

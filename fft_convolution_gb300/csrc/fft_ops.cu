@@ -174,6 +174,15 @@ int fft_debug_wait_timeout(int64_t polls, void *stream) {
   return FFT_OK;
 }
 
+int fft_debug_cluster_timeout(void *data, int64_t polls, void *stream) {
+  if (!data || polls <= 0 || polls > ((int64_t)1 << 22)) return FFT_ERR_INVALID_ARG;
+  if (misaligned(data)) return FFT_ERR_MISALIGNED;
+  cudaError_t e = debug_cluster_timeout_f32(data, (unsigned)polls, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return FFT_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FFT_OK;
+}
+
 int fft_device_status(void *stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(st);

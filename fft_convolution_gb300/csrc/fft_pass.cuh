@@ -230,7 +230,8 @@ cudaError_t launch_pass_tma_t(const void *in, void *out, int log_n, int log_m, i
                               long long batch, cudaStream_t st);
 template <typename T, int LOGL, int DIR>
 cudaError_t launch_pass_cluster_t(const void *in, void *out, int log_n, int log_m, int twiddle,
-                                  long long batch, cudaStream_t st);
+                                  long long batch, cudaStream_t st, int debug_fail = 0,
+                                  unsigned poll_limit = 0);
 
 template <typename T, int DIR, int MAXLOG, int LOGL = 1>
 cudaError_t dispatch_pass(const PassArgs &a, const void *in, void *out, cudaStream_t st) {

@@ -143,6 +143,11 @@ __global__ void __launch_bounds__(ClusterConfig<T, LOGL>::THREADS,
   const long long cluster = blockIdx.x / R, nclusters = gridDim.x / R;
   const uint32_t work_addr = smem_addr(work), my_flag = smem_addr(flags + r);
 
+  // Test hook: the failing block arms its first load for 16 bytes and
+  // issues no copy (nothing is in flight when it leaves); only its waits
+  // are shortened.
+  const bool failing = g.debug_fail == r + 1;
+  const uint32_t limit = failing && g.poll_limit ? g.poll_limit : 1u << 22;
   auto issue_load = [&](long long tile) {
     const long long b = tile / g.tiles_per_batch;
     const long long i0 = (tile % g.tiles_per_batch) * C;
@@ -158,14 +163,17 @@ __global__ void __launch_bounds__(ClusterConfig<T, LOGL>::THREADS,
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  if (tid == 0 && cluster < g.total_tiles) issue_load(cluster);
+  if (tid == 0 && cluster < g.total_tiles) {
+    if (failing) mbar_expect_tx(&bar[0], 16);
+    else issue_load(cluster);
+  }
 
   int k = 0;
   for (long long tile = cluster; tile < g.total_tiles; tile += nclusters, ++k) {
     const long long b = tile / g.tiles_per_batch;
     const long long i0 = (tile % g.tiles_per_batch) * C;
     const long long next = tile + nclusters;
-    const bool ok = mbar_wait(&bar[0], (uint32_t)k & 1u);
+    const bool ok = mbar_wait(&bar[0], (uint32_t)k & 1u, limit);
     const int bad = __syncthreads_or(!ok);
 
     // Step 1: rows r + R*(t + w*TP) of column i0 + c, inter-pass twiddle,
@@ -202,7 +210,7 @@ __global__ void __launch_bounds__(ClusterConfig<T, LOGL>::THREADS,
       if (tid == 0) {
         atomicExch(status, kDeviceErrorTimeout);
         // Let the prefetch issued above land before the block exits.
-        if (prefetched) mbar_wait(&bar[0], (uint32_t)(k + 1) & 1u);
+        if (prefetched) mbar_wait(&bar[0], (uint32_t)(k + 1) & 1u, limit);
       }
       break;
     }
@@ -304,7 +312,8 @@ inline int cluster_min_log() {
 // point, or no cluster fits the device.
 template <typename T, int LOGL, int DIR>
 cudaError_t launch_pass_cluster_t(const void *in, void *out, int log_n, int log_m, int twiddle,
-                                  long long batch, cudaStream_t st) {
+                                  long long batch, cudaStream_t st, int debug_fail,
+                                  unsigned poll_limit) {
   using Cfg = ClusterConfig<T, LOGL>;
   if constexpr (!Cfg::OK) {
     return cudaErrorNotSupported;
@@ -373,7 +382,8 @@ cudaError_t launch_pass_cluster_t(const void *in, void *out, int log_n, int log_
       }
       resident[dev].store(ncl, std::memory_order_release);
     }
-    TmaGeom g{log_n, log_m, twiddle, cols / Cfg::C, (cols / Cfg::C) * batch};
+    TmaGeom g{log_n, log_m, twiddle, cols / Cfg::C, (cols / Cfg::C) * batch, debug_fail,
+              poll_limit};
     long long clusters = ncl < g.total_tiles ? ncl : g.total_tiles;
     cfg.gridDim = dim3((unsigned)(clusters * Cfg::R));
     return cudaLaunchKernelEx(&cfg, kern, tin, tout, static_cast<vec2_t<T> *>(out), g,

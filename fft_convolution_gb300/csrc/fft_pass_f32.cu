@@ -23,4 +23,11 @@ template <int LOGL = 1> int tile_cols(int log_l) {
 
 int pass_tile_cols_f32(int log_l) { return tile_cols(log_l); }
 
+// Test hook: one in-place pass of on-chip length 2^13 over 2^15 points (one
+// tile, one cluster of 8 blocks) in which block 1's tile load never
+// completes; every wait gives up after `polls` polls.
+cudaError_t debug_cluster_timeout_f32(void *data, unsigned polls, cudaStream_t st) {
+  return launch_pass_cluster_t<float, 13, -1>(data, data, 15, 0, 1, 1, st, 2, polls);
+}
+
 }  // namespace fftgb

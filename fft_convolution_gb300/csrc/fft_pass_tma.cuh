@@ -53,9 +53,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
-// Bounded wait: false if the phase did not complete within ~2^22 polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  for (uint32_t it = 0; it < (1u << 22); ++it)
+// Bounded wait: false if the phase did not complete within `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          uint32_t limit = 1u << 22) {
+  for (uint32_t it = 0; it < limit; ++it)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
@@ -136,6 +137,11 @@ struct TmaGeom {
   int twiddle;
   long long tiles_per_batch;
   long long total_tiles;
+  // Test hook of the cluster kernel (0 in every transform): block rank
+  // debug_fail - 1 arms its first tile load for 16 bytes that never come
+  // (and issues no copy); its waits give up after poll_limit polls.
+  int debug_fail;
+  unsigned poll_limit;
 };
 
 template <typename T, int LOGL, int DIR>
@@ -359,7 +365,7 @@ cudaError_t launch_pass_tma_t(const void *in, void *out, int log_n, int log_m, i
     static std::atomic<unsigned long long> attr_set{0};
     const cudaError_t attr = smem_limit_once((const void *)kern, Cfg::SMEM, attr_set);
     if (attr != cudaSuccess) return attr;
-    TmaGeom g{log_n, log_m, twiddle, cols / Cfg::C, (cols / Cfg::C) * batch};
+    TmaGeom g{log_n, log_m, twiddle, cols / Cfg::C, (cols / Cfg::C) * batch, 0, 0};
     static std::atomic<int> occupancy[64];
     const int per_sm = blocks_per_sm_once((const void *)kern, Cfg::THREADS, Cfg::SMEM, occupancy);
     long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);

@@ -95,6 +95,9 @@ int *device_status_word();
 
 // Bounded-wait test hook (debug_pass.cu).
 cudaError_t launch_wait_timeout(long long polls, cudaStream_t st);
+// One cluster pass (2^15 fp32 points in place) whose block 1 waits for a
+// load that never completes (fft_pass_f32.cu).
+cudaError_t debug_cluster_timeout_f32(void *data, unsigned polls, cudaStream_t st);
 
 // One radix-2 butterfly pass (debug_pass.cu).
 cudaError_t launch_radix2_pass(int dtype, const void *in, void *out, long long n, long long half,

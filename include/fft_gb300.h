@@ -377,6 +377,20 @@ int fft_device_status(void *stream);
  */
 int fft_debug_wait_timeout(int64_t polls, void *stream);
 
+/*
+ * fft_debug_cluster_timeout -- test hook (not part of the transform API):
+ * runs the cluster pass kernel once, in place, on `data` (device, 16-byte
+ * aligned, 2^15 fp32 complex values = 256 KiB, overwritten with
+ * meaningless values), with the tile load of one of its 8 blocks armed for
+ * 16 bytes that never arrive and every load wait bounded to `polls` polls
+ * (1 .. 2^22).  That block's wait runs out; the whole cluster sees its
+ * flag, leaves together, and the device status word reads
+ * FFT_ERR_DEVICE_TIMEOUT (fft_device_status).  Returns FFT_ERR_UNSUPPORTED
+ * when the cluster kernel is switched off (FFT_GB300_NO_CLUSTER).  Faults
+ * nothing.  No counterpart on the source pages.
+ */
+int fft_debug_cluster_timeout(void *data, int64_t polls, void *stream);
+
 /* Last status recorded on this host thread by a call that returns a
  * pointer (fft_plan_create). */
 int fft_last_status(void);

@@ -116,6 +116,10 @@ def test_polymul_and_debug_argument_checks(fg):
     assert fg.fft_debug_radix2_pass(16, 32, 8, 0, 0, None) == fg.FFT_ERR_INVALID_ARG
     assert fg.fft_debug_radix2_pass(16, 32, 8, 2, 5, None) == fg.FFT_ERR_INVALID_ARG
     assert fg.fft_debug_radix2_pass(24, 32, 8, 2, 0, None) == fg.FFT_ERR_MISALIGNED
+    assert fg.fft_debug_cluster_timeout(None, 10, None) == fg.FFT_ERR_INVALID_ARG
+    assert fg.fft_debug_cluster_timeout(16, 0, None) == fg.FFT_ERR_INVALID_ARG
+    assert fg.fft_debug_cluster_timeout(16, (1 << 22) + 1, None) == fg.FFT_ERR_INVALID_ARG
+    assert fg.fft_debug_cluster_timeout(24, 10, None) == fg.FFT_ERR_MISALIGNED
 
 
 @pytest.mark.parametrize("n,dtype", [(2, 2), (8, 2), (4096, 2), (1 << 15, 2), (1 << 14, 3), (2, 3)])

@@ -643,6 +643,26 @@ def test_bounded_wait_reports_timeout(fg):
     assert fg.fft_debug_wait_timeout(0, stream()) == fg.FFT_ERR_INVALID_ARG
 
 
+def test_cluster_pass_timeout_reported(fg):
+    # One block of a cluster waits for a tile load that never completes: the
+    # whole cluster leaves after the bounded wait, the status word says so,
+    # and the next cluster pass on the context is correct.
+    buf = torch.zeros(1 << 15, dtype=torch.complex64, device="cuda")
+    assert fg.fft_debug_cluster_timeout(buf.data_ptr(), 2000, stream()) == 0
+    assert fg.fft_device_status(stream()) == fg.FFT_ERR_DEVICE_TIMEOUT
+    assert fg.fft_device_status(stream()) == 0
+    x = workloads.normal_complex((1, 8192, 8), 6300, np.complex64)
+    p = fg.Plan(0, 1, direction=fg.FFT_FORWARD, dtype=F32, shape=(8192, 8))
+    y = p.exec(torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    assert rel_rows(y.cpu().numpy(), oracle.fftn(x.astype(np.complex128), 2)).max() <= \
+        tol(F32, 8192 * 8)
+    p.close()
+    assert fg.fft_device_status(stream()) == 0
+    assert fg.fft_debug_cluster_timeout(buf.data_ptr(), 0, stream()) == fg.FFT_ERR_INVALID_ARG
+    assert fg.fft_debug_cluster_timeout(buf.data_ptr() + 8, 10, stream()) == fg.FFT_ERR_MISALIGNED
+
+
 def test_misaligned_device_pointer(fg):
     p = fg.Plan(64, 1, 1, fg.FFT_FORWARD, F32)
     buf = torch.zeros(2 * 64 + 8, dtype=torch.complex64, device="cuda")
