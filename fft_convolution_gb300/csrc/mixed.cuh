@@ -8,8 +8,8 @@
 //   out[q R m + p + v m] = sum_{u<R} W_R^{u v} (W_{R m}^{p u} in[i + u N/R]),
 //   i = q m + p,  p < m,  q < N/(R m),
 // natural order in and out.  A block holds F whole transforms in shared
-// memory (loaded with asynchronous copies; two buffers, one barrier per
-// stage; the last stage writes global memory); every stage is a loop of its 256 threads
+// memory (two buffers, one barrier per stage; the first stage reads global
+// memory, the last one writes it); every stage is a loop of its 256 threads
 // over the F * N/R butterflies, each loading its R inputs,
 // applying the stage twiddles (read from a per-plan table of the forward
 // roots, conjugated for the inverse), running the radix-R DFT in registers
@@ -92,19 +92,6 @@ __device__ __forceinline__ int div_magic(int x, int d, unsigned magic) {
   return d == 1 ? x : (int)__umulhi((unsigned)x, magic);
 }
 
-// Asynchronous global -> shared copy of one element (8 or 16 bytes), and
-// the wait for all of this thread's copies.
-template <typename V> __device__ __forceinline__ void cp_async_elem(V *dst, const V *src) {
-  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
-  if constexpr (sizeof(V) == 16)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
-  else
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(d), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;\n" ::: "memory");
-}
-
 // One stage of radix R over the F transforms of a block: src and dst hold
 // F transforms of N values each (stride N).  tw: this stage's table,
 // W_{Rm}^{p u} (forward) at (u - 1) m + p.  The last stage writes the
@@ -162,8 +149,60 @@ __device__ __forceinline__ void mixed_stage_any(const V *src, V *dst, const Mixe
   }
 }
 
+// The first stage (m = 1, no twiddles) read straight from global memory:
+// butterfly i of row f takes g[f*N + i + u*nb] (consecutive threads read
+// consecutive elements) and writes dst[f*N + i*R + v].  Each thread first
+// loads G butterflies (G*R <= 16 fp32 / 8 fp64 values in flight), then
+// computes and stores them.  Rows at or beyond `rows` read as zeros.
+template <int R, int DIR, typename V>
+__device__ __forceinline__ void mixed_first_stage(const V *g, V *dst, const MixedStages &ms,
+                                                  int rows) {
+  using T = decltype(V::x);
+  constexpr int MAXV = sizeof(T) == 4 ? 16 : 8;
+  constexpr int G = 4 * R <= MAXV ? 4 : (2 * R <= MAXV ? 2 : 1);
+  const int N = ms.N, nb = N / R;
+  const int total = ms.F * nb;
+  for (int b0 = threadIdx.x; b0 < total; b0 += G * kMixedThreads) {
+    V y[G][R];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const int b = b0 + j * kMixedThreads;
+      const int f = div_magic(b, nb, ms.nb_magic[0]), i = b - f * nb;
+      const bool live = b < total && f < rows;
+      const V *s = g + (long long)f * N + i;
+#pragma unroll
+      for (int u = 0; u < R; ++u) y[j][u] = live ? s[u * nb] : make_c<V>((T)0, (T)0);
+    }
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const int b = b0 + j * kMixedThreads;
+      if (b < total) {
+        const int f = div_magic(b, nb, ms.nb_magic[0]), i = b - f * nb;
+        dft_any<R, DIR>(y[j]);
+        V *d = dst + f * N + i * R;
+#pragma unroll
+        for (int v = 0; v < R; ++v) d[v] = y[j][v];
+      }
+    }
+  }
+}
+
+template <int DIR, typename V>
+__device__ __forceinline__ void mixed_first_stage_any(const V *g, V *dst, const MixedStages &ms,
+                                                      int rows) {
+  switch (ms.radix[0]) {
+    case 2: mixed_first_stage<2, DIR>(g, dst, ms, rows); break;
+    case 3: mixed_first_stage<3, DIR>(g, dst, ms, rows); break;
+    case 4: mixed_first_stage<4, DIR>(g, dst, ms, rows); break;
+    case 5: mixed_first_stage<5, DIR>(g, dst, ms, rows); break;
+    case 7: mixed_first_stage<7, DIR>(g, dst, ms, rows); break;
+    case 8: mixed_first_stage<8, DIR>(g, dst, ms, rows); break;
+    default: mixed_first_stage<16, DIR>(g, dst, ms, rows); break;
+  }
+}
+
 template <typename T, int DIR>
-__global__ void __launch_bounds__(kMixedThreads)
+__global__ void __launch_bounds__(kMixedThreads, sizeof(T) == 4 ? 4 : 2)
     mixed_rows_kernel(const vec2_t<T> *in, vec2_t<T> *out, long long batch, MixedStages ms,
                       const vec2_t<T> *__restrict__ tw, T scale) {
   using V = vec2_t<T>;
@@ -173,22 +212,16 @@ __global__ void __launch_bounds__(kMixedThreads)
   const long long row0 = (long long)blockIdx.x * ms.F;
   const long long left = batch - row0;
   const int rows = left < ms.F ? (int)left : ms.F;
-  // The block's rows into shared memory with asynchronous copies (all in
-  // flight at once; rows beyond the batch as zeros), the stages between the
-  // two shared buffers (one barrier each: a stage's output is complete and
-  // its input buffer free for the next output), the last stage to global
-  // memory.  (Persistent blocks prefetching the next rows into a third
-  // buffer measured slower: one block fewer per SM.)
-  const int count = rows * ms.N;
-  const V *src = in + row0 * ms.N;
-  for (int e = threadIdx.x; e < ms.F * ms.N; e += kMixedThreads) {
-    if (e < count) cp_async_elem(cur + e, src + e);
-    else cur[e] = make_c<V>((T)0, (T)0);
-  }
-  cp_async_wait_all();
+  // The first stage straight from global memory into shared memory, the
+  // middle stages between the two shared buffers (one barrier each: a
+  // stage's output is complete and its input buffer free for the next
+  // output), the last stage to global memory.  (Persistent blocks
+  // prefetching the next rows into a third buffer measured slower: one
+  // block fewer per SM.)
+  mixed_first_stage_any<DIR>(in + row0 * ms.N, cur, ms, rows);
   __syncthreads();
   const int S = ms.nstages;  // >= 2 for every planned length (N > 64, R <= 16)
-  for (int k = 0; k < S - 1; ++k) {
+  for (int k = 1; k < S - 1; ++k) {
     mixed_stage_any<DIR, false>(cur, nxt, ms, k, tw, rows, (T)1);
     __syncthreads();
     V *tmp = cur;
