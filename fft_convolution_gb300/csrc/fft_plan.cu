@@ -211,6 +211,10 @@ static bool mixed_stages(int64_t n, int elem, MixedStages *ms) {
     ms->tw_off[j] = off;
     ms->nb_magic[j] = magic(n / radix[j]);
     ms->m_magic[j] = magic(m);
+    ms->nq[j] = (int)(n / ((int64_t)radix[j] * m));
+    ms->q_magic[j] = magic(ms->nq[j]);
+    if (j > 0 && j + 1 < k && m > 1 && m < 16 && (m & 1) && (radix[j] & 1))
+      ms->qorder |= 1u << j;
     off += (radix[j] - 1) * m;
     m *= radix[j];
   }

@@ -157,6 +157,14 @@ struct MixedStages {
   // floor(x / d) = umulhi(x, magic) while x * d < 2^32.
   unsigned nb_magic[16];
   unsigned m_magic[16];
+  // Stages whose butterflies are walked q-fastest (bit k of qorder): the
+  // middle stages with odd R and odd m < 16, whose shared-memory stores at
+  // q R m + p + v m then run at the odd stride R m across a warp (free of
+  // bank conflicts) instead of in runs of m.  nq[k] = N / (R m) and its
+  // magic number q_magic[k] split the butterfly index as p * nq + q.
+  unsigned qorder;
+  int nq[16];
+  unsigned q_magic[16];
 };
 constexpr int kMixedMaxF32 = 12288;  // 2 buffers of N values within 192 KB of shared memory
 constexpr int kMixedMaxF64 = 6144;

@@ -104,9 +104,18 @@ __device__ __forceinline__ void mixed_stage(const V *src, V *dst, const MixedSta
   const int N = ms.N, m = ms.m[k];
   const int nb = N / R;
   const int total = ms.F * nb;
+  const bool qfast = !LAST && ((ms.qorder >> k) & 1u);
   for (int b = threadIdx.x; b < total; b += kMixedThreads) {
-    const int f = div_magic(b, nb, ms.nb_magic[k]), i = b - f * nb;
-    const int q = div_magic(i, m, ms.m_magic[k]), p = i - q * m;
+    const int f = div_magic(b, nb, ms.nb_magic[k]), j = b - f * nb;
+    int q, p;
+    if (qfast) {  // j = p * nq + q: a warp's stores at the odd stride R m
+      p = div_magic(j, ms.nq[k], ms.q_magic[k]);
+      q = j - p * ms.nq[k];
+    } else {      // j = q * m + p: runs of m consecutive stores
+      q = div_magic(j, m, ms.m_magic[k]);
+      p = j - q * m;
+    }
+    const int i = q * m + p;
     const V *s = src + f * N;
     V y[R];
 #pragma unroll
