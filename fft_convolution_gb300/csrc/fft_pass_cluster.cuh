@@ -129,8 +129,8 @@ __global__ void __launch_bounds__(ClusterConfig<T, LOGL>::THREADS,
   using V = vec2_t<T>;
   constexpr int C = Cfg::C, R = Cfg::R, L = Cfg::L, LP = Cfg::LP, LPP = Cfg::LPP;
   constexpr int KB = 16 / R;  // R-point butterflies per thread
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  unsigned char *base = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
+  extern __shared__ __align__(128) unsigned char smem_cl[];
+  unsigned char *base = smem_cl + ((128u - (smem_addr(smem_cl) & 127u)) & 127u);
   uint64_t *bar = reinterpret_cast<uint64_t *>(base);
   int *flags = reinterpret_cast<int *>(base + 64);  // [R]: block q's load failed
   V *const lbuf = reinterpret_cast<V *>(base + 128);

@@ -154,10 +154,10 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
   using V = vec2_t<T>;
   constexpr int C = Cfg::C;
   constexpr int L = Cfg::L;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
+  extern __shared__ __align__(128) unsigned char smem_tma[];
   // TMA destinations must be 128-byte aligned: round the base up (the
   // allocation carries 128 spare bytes for this).
-  unsigned char *base = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
+  unsigned char *base = smem_tma + ((128u - (smem_addr(smem_tma) & 127u)) & 127u);
   uint64_t *bar = reinterpret_cast<uint64_t *>(base);
   V *const twt = reinterpret_cast<V *>(base + 128);
   V *const buf0 = twt + Cfg::TW_ELEMS;
