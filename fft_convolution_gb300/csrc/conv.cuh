@@ -79,11 +79,14 @@ template <typename T, int KIND> struct ConvSink {
 // MODE 1: y_r = IFFT_L(FFT_L(x_r padded) . H[r or 0]), first ny outputs.
 // ---------------------------------------------------------------------------
 // Registers capped for 1024 resident threads per SM (four 256-thread
-// blocks): the fused kernel does twice the on-chip work of a transform per
-// byte of HBM traffic, so it needs the occupancy to hide its exchanges.
+// blocks) in fp32: the fused kernel does twice the on-chip work of a
+// transform per byte of HBM traffic, so it needs the occupancy to hide its
+// exchanges.  fp64 values take two registers each: 512 threads (128
+// registers), which keeps the 16 values a thread holds out of local memory.
 template <typename T, int LOGN> struct ConvRowsBounds {
   static constexpr int THREADS = RowsConfig<T, LOGN>::THREADS;
-  static constexpr int MIN_BLOCKS = THREADS >= 1024 ? 1 : 1024 / THREADS;
+  static constexpr int RESIDENT = sizeof(T) == 8 ? 512 : 1024;
+  static constexpr int MIN_BLOCKS = THREADS >= RESIDENT ? 1 : RESIDENT / THREADS;
 };
 
 // Src: (row, idx) -> sample (zero beyond the data); Snk: (row, idx, value).

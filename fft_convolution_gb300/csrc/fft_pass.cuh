@@ -40,8 +40,11 @@ template <typename T, int LOGL> struct PassConfig {
   static constexpr int C = C_RAW < 1 ? 1 : (C_RAW > 64 ? 64 : (int)C_RAW);
   static constexpr int THREADS = C * P::TP;
   // Ask for registers that let 1024 threads (two 512-thread tiles) share an
-  // SM, so one tile's loads overlap another's compute and stores.
-  static constexpr int MIN_BLOCKS = THREADS >= 1024 ? 1 : 1024 / THREADS;
+  // SM in fp32, so one tile's loads overlap another's compute and stores;
+  // 512 threads in fp64 (128 registers: the 16 values a thread holds take
+  // 32 registers each way, and fewer registers spill them).
+  static constexpr int RESIDENT = sizeof(T) == 8 ? 512 : 1024;
+  static constexpr int MIN_BLOCKS = THREADS >= RESIDENT ? 1 : RESIDENT / THREADS;
   static constexpr int ROW_ELEMS =
       P::SMEM_ELEMS > P::L + 1 ? P::SMEM_ELEMS : P::L + 1;  // exchange or transpose
   static constexpr int EXCHANGE_ELEMS = C * ROW_ELEMS;

@@ -74,10 +74,12 @@ __device__ __forceinline__ void geometric_each(V a, V s, Fn f) {
 }
 
 template <typename T, int LOGH> struct RealRowsBounds {
-  // Four blocks of 256 threads per SM (64 registers a thread).
-  static constexpr int MIN_BLOCKS = RealRowsConfig<T, LOGH>::THREADS >= 1024
+  // Four blocks of 256 threads per SM in fp32 (64 registers a thread); two
+  // in fp64 (128 registers: the values a thread holds take two each).
+  static constexpr int RESIDENT = sizeof(T) == 8 ? 512 : 1024;
+  static constexpr int MIN_BLOCKS = RealRowsConfig<T, LOGH>::THREADS >= RESIDENT
                                         ? 1
-                                        : 1024 / RealRowsConfig<T, LOGH>::THREADS;
+                                        : RESIDENT / RealRowsConfig<T, LOGH>::THREADS;
 };
 
 // Forward: batch rows of N = 2H reals (read as H complex) -> batch rows of
