@@ -93,12 +93,10 @@ static int pass_split_override(int logn, int dtype, int *split) {
 
 // Bytes of data an L2-grouped schedule keeps in flight between two
 // dependent kernels so that the second finds the first's output in L2.
-// Measured on GB300, grouping 2D images or fusing the first two passes of a
-// 2^26 transform by 32 MiB groups is slower than whole-array passes (more,
-// smaller launches with partial last waves): 8 x 2048^2 forward + inverse
-// 0.428 ms whole, 0.541 / 0.469 / 0.460 / 0.453 ms in groups of 1 / 2 / 3 /
-// 4 images.  So grouping is off by default (0) and FFT_GB300_L2_BYTES turns
-// it on for tuning.
+// Measured on GB300, grouping 2D images (32 MiB) or fusing the first two
+// passes of a 2^26 transform by 32 MiB groups is slower than whole-array
+// passes (more, smaller launches with partial last waves), so grouping is
+// off by default (0) and FFT_GB300_L2_BYTES turns it on for tuning.
 size_t l2_group_bytes() {
   size_t v = 0;
   const char *env = getenv("FFT_GB300_L2_BYTES");
