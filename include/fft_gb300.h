@@ -5,7 +5,8 @@
  *   - batched 1D complex-to-complex transforms of any length, forward
  *     (unscaled) and inverse (scaled by 1/N), fp32 or fp64: powers of two on
  *     chip or in 2-4 HBM passes; other lengths by the direct DFT (N <= 64),
- *     mixed radix (prime factors 2, 3, 5, 7) or Bluestein;
+ *     mixed radix (prime factors 2, 3, 5, 7; four-step beyond one block) or
+ *     Bluestein;
  *   - transforms of real sequences (half spectrum out / in, any length);
  *   - separable 2D and 3D transforms of any sides (rows, then columns, ...);
  *   - linear convolution of complex or real signals;
@@ -35,8 +36,9 @@
  *
  * Ownership: the caller owns every buffer passed in.  A plan owns its
  * workspace and tables (allocated in fft_plan_create / fft_plan_create_nd,
- * freed in fft_plan_destroy).  polymul / fft_convolve allocate their scratch
- * stream-ordered on the given stream and free it the same way.
+ * freed in fft_plan_destroy).  polymul, polymul_batched and fft_convolve
+ * allocate their scratch stream-ordered on the given stream and free it the
+ * same way; polymul_noalloc uses a fixed device array of the library.
  *
  * Errors: every call returns FFT_OK (0) or one FFT_ERR_* code; calls that
  * return a pointer return NULL and record the code for fft_last_status()
