@@ -142,7 +142,7 @@ cudaError_t launch_conv_rows(int logn, Src src, Snk dst, vec2_t<T> *H, int h_per
     using C = RowsConfig<T, LOGN>;
     auto kern = conv_rows_kernel<T, LOGN, MODE, Src, Snk>;
     if (C::SMEM > 48 * 1024) {
-      static std::atomic<unsigned long long> attr_set{0};
+      static DeviceOnce attr_set;
       const cudaError_t e = smem_limit_once((const void *)kern, C::SMEM, attr_set);
       if (e != cudaSuccess) return e;
     }

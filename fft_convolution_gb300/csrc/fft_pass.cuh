@@ -202,7 +202,7 @@ cudaError_t launch_pass_t(Load load, Store store, int log_n, int log_m, int twid
   using C = PassConfig<T, LOGL>;
   auto kern = fft_pass_kernel<T, LOGL, DIR, Load, Store>;
   if (C::SMEM > 48 * 1024) {
-    static std::atomic<unsigned long long> attr_set{0};
+    static DeviceOnce attr_set;
     const cudaError_t e = smem_limit_once((const void *)kern, C::SMEM, attr_set);
     if (e != cudaSuccess) return e;
   }

@@ -354,7 +354,7 @@ cudaError_t launch_pass_cluster_t(const void *in, void *out, int log_n, int log_
       tout = tin;  // unused: the first pass stores contiguous runs
     }
     auto kern = fft_pass_cluster_kernel<T, LOGL, DIR>;
-    static std::atomic<unsigned long long> attr_set{0};
+    static DeviceOnce attr_set;
     const cudaError_t attr = smem_limit_once((const void *)kern, Cfg::SMEM, attr_set);
     if (attr != cudaSuccess) return attr;
 

@@ -362,7 +362,7 @@ cudaError_t launch_pass_tma_t(const void *in, void *out, int log_n, int log_m, i
       tout = tin;  // unused: the first pass stores linearly
     }
     auto kern = fft_pass_tma_kernel<T, LOGL, DIR>;
-    static std::atomic<unsigned long long> attr_set{0};
+    static DeviceOnce attr_set;
     const cudaError_t attr = smem_limit_once((const void *)kern, Cfg::SMEM, attr_set);
     if (attr != cudaSuccess) return attr;
     TmaGeom g{log_n, log_m, twiddle, cols / Cfg::C, (cols / Cfg::C) * batch, 0, 0};

@@ -8,6 +8,7 @@
 // kernel per butterfly stage with a device-wide synchronisation after each.
 // Here a plan fixes the kernel sequence once; fft_exec (fft_exec.cu) only
 // enqueues it on the caller's stream and never synchronises.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -15,7 +16,9 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
 #include <new>
+#include <utility>
 
 #include "plan.h"
 
@@ -29,19 +32,48 @@ namespace fftgb {
 thread_local int g_status = FFT_OK;
 thread_local cudaError_t g_cuda_error = cudaSuccess;
 
+unsigned long long context_id() {
+  // cuCtxGetCurrent / cuCtxGetId from the driver, found through the runtime
+  // (no link-time dependency on libcuda).
+  using GetCurrentFn = CUresult (*)(CUcontext *);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+  static const std::pair<GetCurrentFn, GetIdFn> fns = [] {
+    void *a = nullptr, *b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    const bool ok =
+        cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) ==
+            cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) ==
+            cudaSuccess &&
+        qb == cudaDriverEntryPointSuccess;
+    return ok ? std::make_pair(reinterpret_cast<GetCurrentFn>(a), reinterpret_cast<GetIdFn>(b))
+              : std::make_pair(static_cast<GetCurrentFn>(nullptr), static_cast<GetIdFn>(nullptr));
+  }();
+  if (!fns.first) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (fns.first(&ctx) != CUDA_SUCCESS || !ctx || fns.second(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// The device address of g_device_status, looked up once per device and
+// context (cudaGetSymbolAddress) and cached.
 int *device_status_word() {
-  static std::atomic<int *> cache[64];
+  static std::mutex mu;
+  static unsigned long long ctx_of[64];
+  static int *word_of[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  int *w = cache[dev].load(std::memory_order_acquire);
-  if (!w) {
+  const unsigned long long id = context_id();
+  std::lock_guard<std::mutex> lock(mu);
+  if (id == 0 || ctx_of[dev] != id || !word_of[dev]) {
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status) == cudaSuccess) {
-      w = static_cast<int *>(p);
-      cache[dev].store(w, std::memory_order_release);
-    }
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    word_of[dev] = static_cast<int *>(p);
+    ctx_of[dev] = context_id();
   }
-  return w;
+  return word_of[dev];
 }
 
 // Records a failed CUDA call and consumes the runtime's last-error state it

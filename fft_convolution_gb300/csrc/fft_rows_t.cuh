@@ -91,7 +91,7 @@ cudaError_t launch_rows_t_t(const void *in, void *out, long long rows, int log_r
   } else {
     auto kern = fft_rows_t_kernel<T, LOGN, DIR>;
     if (C::SMEM > 48 * 1024) {
-      static std::atomic<unsigned long long> attr_set{0};
+      static DeviceOnce attr_set;
       const cudaError_t e = smem_limit_once((const void *)kern, C::SMEM, attr_set);
       if (e != cudaSuccess) return e;
     }

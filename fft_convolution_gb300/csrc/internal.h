@@ -17,19 +17,31 @@ template <typename T> struct RowsMaxLog;
 template <> struct RowsMaxLog<float> { static constexpr int value = 14; };
 template <> struct RowsMaxLog<double> { static constexpr int value = 13; };
 
-// Sets a kernel's dynamic shared-memory limit once per device (the
-// attribute belongs to the device's context).  `done` is the calling
-// launcher's own bitmask of devices already set.
-inline cudaError_t smem_limit_once(const void *kern, size_t bytes,
-                                   std::atomic<unsigned long long> &done) {
+// Unique id of the calling thread's current CUDA context (cuCtxGetId), or 0
+// when there is none or the driver does not offer the query.  Set-up cached
+// per device (a kernel attribute, the device address of a symbol) is keyed
+// on it: after cudaDeviceReset the runtime creates a new context with a new
+// id, and that set-up is done again there instead of being taken from the
+// destroyed one.
+unsigned long long context_id();
+
+// Per-device record of the context a piece of set-up was last done in.
+struct DeviceOnce {
+  std::atomic<unsigned long long> ctx[64];
+};
+
+// Sets a kernel's dynamic shared-memory limit once per device and context
+// (the attribute belongs to the context).  `done` is the calling launcher's
+// own record.
+inline cudaError_t smem_limit_once(const void *kern, size_t bytes, DeviceOnce &done) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  const unsigned long long bit = 1ull << dev;
-  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  const unsigned long long id = context_id();
+  if (id != 0 && done.ctx[dev].load(std::memory_order_acquire) == id) return cudaSuccess;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  if (e == cudaSuccess) done.ctx[dev].store(context_id(), std::memory_order_release);
   return e;
 }
 

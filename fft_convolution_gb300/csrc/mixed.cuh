@@ -248,7 +248,7 @@ cudaError_t mixed_exec_t(const void *in, void *out, long long batch, const Mixed
   auto kern = dir < 0 ? mixed_rows_kernel<T, -1> : mixed_rows_kernel<T, 1>;
   if (smem > 48 * 1024) {
     // The largest size any plan needs, once per device and direction.
-    static std::atomic<unsigned long long> attr_set[2] = {{0}, {0}};
+    static DeviceOnce attr_set[2];
     const size_t max_smem = 2 * (size_t)(sizeof(T) == 4 ? kMixedMaxF32 : kMixedMaxF64) * sizeof(V);
     const cudaError_t e = smem_limit_once((const void *)kern, max_smem, attr_set[dir < 0 ? 0 : 1]);
     if (e != cudaSuccess) return e;

@@ -39,6 +39,7 @@ static __device__ __align__(256) double2 g_noalloc_scratch[3 * kMaxLen];
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 void *g_scratch_on_device[kMaxDevices];
+unsigned long long g_scratch_context[kMaxDevices];  // context the address belongs to
 
 int ilog2_ceil(long long n) {
   int l = 0;
@@ -59,8 +60,9 @@ extern "C" int polymul_noalloc(const int64_t *a, int64_t na, const int64_t *b, i
       fftgb::polymul_scratch_bytes(1, log_len) > sizeof(g_noalloc_scratch))
     return FFT_ERR_UNSUPPORTED;  // beyond the fixed scratch
 
-  // Set-up, once per device, with that device current: the device address
-  // of the scratch array.
+  // Set-up, once per device (and again if the device's context was
+  // destroyed by cudaDeviceReset and created anew), with that device
+  // current: the device address of the scratch array.
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return FFT_ERR_CUDA;
@@ -68,11 +70,13 @@ extern "C" int polymul_noalloc(const int64_t *a, int64_t na, const int64_t *b, i
   void *scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_on_device[dev]) {
+    const unsigned long long ctx = fftgb::context_id();
+    if (!g_scratch_on_device[dev] || ctx == 0 || g_scratch_context[dev] != ctx) {
       void *p = nullptr;
       e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
       if (e != cudaSuccess || !p) return FFT_ERR_CUDA;
       g_scratch_on_device[dev] = p;
+      g_scratch_context[dev] = fftgb::context_id();
     }
     scratch = g_scratch_on_device[dev];
   }

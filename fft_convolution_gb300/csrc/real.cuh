@@ -201,7 +201,7 @@ cudaError_t launch_real_rows_t(const void *in, void *out, long long batch, cudaS
   using V = vec2_t<T>;
   auto kern = FWD ? r2c_rows_kernel<T, LOGH> : c2r_rows_kernel<T, LOGH>;
   if (C::SMEM > 48 * 1024) {
-    static std::atomic<unsigned long long> attr_set{0};
+    static DeviceOnce attr_set;
     const cudaError_t e = smem_limit_once((const void *)kern, C::SMEM, attr_set);
     if (e != cudaSuccess) return e;
   }

@@ -238,8 +238,10 @@ int fft_exec_host_chain(const fft_plan *const *plans, int nplans, const void *ho
  * (e.g. coefficients in [0, 9] with na, nb <= 2^20 give |c_k| < 2^27 and an
  * error of order 1e-7).  L <= 2^27.  Both inputs ride in one complex
  * transform (a + i b) and the real product comes back through one of length
- * L/2.  Scratch (2 * L * 16 bytes plus 256 KiB of twiddle tables) is
- * allocated with cudaMallocAsync on `stream` and freed the same way.
+ * L/2.  Scratch of 2 * L * 16 bytes plus six twiddle tables of
+ * 2^ceil(log2(L) / 2) complex doubles each (6 * 16 * 2^ceil(log2(L) / 2)
+ * bytes: 192 KiB at L = 2^21, 1.5 MiB at L = 2^27) is allocated with
+ * cudaMallocAsync on `stream` and freed the same way.
  */
 int polymul(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, int64_t *c,
             void *stream);
@@ -250,7 +252,7 @@ int polymul_num_kernels(int64_t na, int64_t nb);
 
 /* polymul over `batch` independent pairs: pair p uses a + p*na, b + p*nb
  * and writes c + p*(na+nb-1).  Scratch is 2 * batch * L * 16 bytes plus
- * 256 KiB. */
+ * the same six twiddle tables as polymul's. */
 int polymul_batched(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, int64_t *c,
                     int64_t batch, void *stream);
 
@@ -285,9 +287,12 @@ int polymul_batched_host(const int64_t *a_host, int64_t na, const int64_t *b_hos
  * loads the library holds it until the process exits).  No call allocates
  * or frees memory.  The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current -- make that
- * first call outside any stream capture.  All calls on a device share the
- * array: calls that overlap on the GPU race and give wrong results, so order
- * them on one stream.  Nothing in the array needs clearing between calls.
+ * first call outside any stream capture.  cudaDeviceReset destroys the
+ * array with the device's context; the first call after it looks the
+ * address up again in the new context (make that call outside any capture
+ * too).  All calls on a device share the array: calls that overlap on the
+ * GPU race and give wrong results, so order them on one stream.  Nothing in
+ * the array needs clearing between calls.
  */
 #define FFT_POLYMUL_NOALLOC_MAX_LEN 65536
 int polymul_noalloc(const int64_t *a, int64_t na, const int64_t *b, int64_t nb, int64_t *c,

@@ -47,6 +47,18 @@ def test_binding_covers_the_header(fg):
         assert callable(getattr(fg, name))
 
 
+def test_binding_constants_match_the_header(fg):
+    # Every numeric #define of the header has the same value in the binding
+    # (FFT_POLYMUL_NOALLOC_MAX_LEN is POLYMUL_NOALLOC_MAX_LEN there), so a
+    # test that uses the binding's constant checks the library's limit.
+    text = open(HEADER).read()
+    defines = re.findall(r"^#define\s+(FFT_\w+)\s+\(?([+-]?\d+)\)?", text, flags=re.M)
+    assert len(defines) >= 15
+    for name, value in defines:
+        py_name = "POLYMUL_NOALLOC_MAX_LEN" if name == "FFT_POLYMUL_NOALLOC_MAX_LEN" else name
+        assert getattr(fg, py_name) == int(value), name
+
+
 def test_status_strings(fg):
     assert fg.fft_status_string(0) == "ok"
     for code in range(1, 7):

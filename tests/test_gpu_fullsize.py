@@ -4,11 +4,10 @@ compute one by one, plus properties that hold at any size.
 
 * 16384 x 4096 fp32: 48 sampled transforms against the recursive CT; the
   inverse returns the input for every transform.
-* one 2^26 fp32 transform (16 tones + noise): 32 sampled bins (the 16 tone
-  bins and 16 random ones) against the direct DFT of those bins -- relative
-  error at each tone bin, RMS-relative error at the noise bins, and a
-  stratified estimate of the whole vector's relative L2 error; Parseval and
-  the inverse round trip over the whole vector.
+* one 2^26 fp32 transform (16 tones + noise): the whole vector against the
+  oracle's recursive Cooley-Tukey (relative L2 error), the 16 tone bins also
+  against the direct DFT of those bins; Parseval and the inverse round trip
+  over the whole vector.
 * 8 images of 2048 x 2048 fp32: images 0 and 7 against the oracle's 2D
   transform; the inverse round trip for all 8.
 * 64 polynomial pairs of 2^20 coefficients: 4096 sampled coefficients (64 per
@@ -28,6 +27,7 @@ All floating-point bounds are the relative-L2 tolerance 1e-5 * log2(N).
 import multiprocessing as mp
 import os
 import tempfile
+import threading
 
 import numpy as np
 import pytest
@@ -87,6 +87,13 @@ def test_c3_single_2e26(fg):
     c = workloads.CONFIGS["c3"]
     n = c["n"]
     x = workloads.config_input("c3")[0]
+    x64 = x.astype(np.complex128)
+    # The oracle's recursive Cooley-Tukey of the whole vector (about half a
+    # minute of one host core; the C call releases the GIL) runs while the
+    # GPU transforms.
+    full = {}
+    worker = threading.Thread(target=lambda: full.setdefault("X", oracle.fft(x64)))
+    worker.start()
     xd = torch.from_numpy(x).cuda()
     yd = torch.empty_like(xd)
     zd = torch.empty_like(xd)
@@ -97,36 +104,31 @@ def test_c3_single_2e26(fg):
     torch.cuda.synchronize()
     y = yd.cpu().numpy().astype(np.complex128)
     z = zd.cpu().numpy().astype(np.complex128)
-    x64 = x.astype(np.complex128)
-    # Sampled bins: the 16 tone bins and 16 seeded random bins.
+    # The 16 tone bins also against the direct DFT of those bins (an
+    # independent oracle path), spread over spawned workers.
     bins, _, _ = workloads.tone_params(n, c["seed"])
-    ks = np.concatenate([bins, workloads.sample_indices(16, n, 33)])
     with tempfile.TemporaryDirectory() as td:
         path = os.path.join(td, "x.npy")
         np.save(path, x64)
-        chunks = [(path, ks[i::8]) for i in range(8)]
+        chunks = [(path, bins[i::8]) for i in range(8)]
         with mp.get_context("spawn").Pool(8) as pool:
             parts = pool.map(_bins_worker, chunks)
-    ref = np.empty(ks.size, np.complex128)
+    tone_ref = np.empty(bins.size, np.complex128)
     for i in range(8):
-        ref[i::8] = parts[i]
+        tone_ref[i::8] = parts[i]
+    worker.join()
+    ref = full["X"]
     tol = TOL32 * 26
-    err = y[ks] - ref
-    # Tone bins (magnitude N): relative error of each.
-    assert np.max(np.abs(err[:16]) / np.abs(ref[:16])) <= tol
-    # Noise bins: error against the spectrum's RMS magnitude.
-    rms = np.linalg.norm(y) / np.sqrt(n)
-    assert np.linalg.norm(err[16:]) / (np.sqrt(16) * rms) <= tol
-    # Stratified estimate of the whole transform's relative L2 error: the 16
-    # tone bins exactly, the other N - 16 bins from the 16-bin sample.
-    est = np.sum(np.abs(err[:16]) ** 2) + (n - 16) / 16 * np.sum(np.abs(err[16:]) ** 2)
-    assert np.sqrt(est) / np.linalg.norm(y) <= tol
-    # Tones: magnitude N at their bins.
-    assert np.all(np.abs(np.abs(ref[:16]) - n) < 0.01 * n)
+    # The whole vector: relative L2 error of the transform.
+    assert np.linalg.norm(y - ref) / np.linalg.norm(ref) <= tol
+    # Tone bins (magnitude N): relative error of each, against both oracle paths.
+    assert np.max(np.abs(y[bins] - tone_ref) / np.abs(tone_ref)) <= tol
+    assert np.max(np.abs(ref[bins] - tone_ref) / np.abs(tone_ref)) <= 1e-9
+    assert np.all(np.abs(np.abs(tone_ref) - n) < 0.01 * n)
     # Parseval and the round trip over the whole vector.
     ex, eX = np.sum(np.abs(x64) ** 2), np.sum(np.abs(y) ** 2) / n
-    assert abs(ex - eX) / ex <= TOL32 * 26
-    assert np.linalg.norm(z - x64) / np.linalg.norm(x64) <= 2 * TOL32 * 26
+    assert abs(ex - eX) / ex <= tol
+    assert np.linalg.norm(z - x64) / np.linalg.norm(x64) <= 2 * tol
     assert fg.fft_device_status(int(torch.cuda.current_stream().cuda_stream)) == 0
     pf.close()
     pi.close()
@@ -190,7 +192,7 @@ def test_conv1_real_signals(fg):
     assert err.max() <= TOL32 * 12
 
 
-def _any_length_full(fg, name, tol_len):
+def _any_length_full(fg, name):
     c = workloads.CONFIGS[name]
     n, batch = c["n"], c["batch"]
     x = workloads.config_input(name)
@@ -204,7 +206,7 @@ def _any_length_full(fg, name, tol_len):
     rows = np.unique(np.concatenate([workloads.sample_indices(5, batch, 71), [batch - 1]]))
     y = yd[torch.from_numpy(rows).cuda()].cpu().numpy()
     ref = np.stack([oracle.dft(x[r].astype(np.complex128)) for r in rows])
-    tol = TOL32 * int(np.log2(tol_len))
+    tol = TOL32 * int(np.log2(n))
     assert rel_rows(y, ref).max() <= tol
     assert rel_rows(zd.cpu().numpy(), x).max() <= 2 * tol
     pf.close()
@@ -214,12 +216,12 @@ def _any_length_full(fg, name, tol_len):
 def test_any1_mixed_radix_3000(fg):
     # 16384 x 3000 fp32 (mixed radix): 6 sampled rows (with the last) against
     # the direct DFT; the inverse returns every row.
-    _any_length_full(fg, "any1", 3000)
+    _any_length_full(fg, "any1")
 
 
 def test_any2_bluestein_3001(fg):
     # 16384 x 3001 fp32 (prime: Bluestein, convolution length 8192).
-    _any_length_full(fg, "any2", 8192)
+    _any_length_full(fg, "any2")
 
 
 def test_real1_r2c_c2r(fg):

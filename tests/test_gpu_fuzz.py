@@ -44,20 +44,10 @@ def draw_length(g, cap_other=3000, cap_pow2=1 << 16):
     return int(g.integers(1, cap_other + 1))
 
 
-def conv_len(n):
-    """Length whose log2 bounds the error: the Bluestein length for lengths
-    that are neither smooth nor short."""
-    m = n
-    for f in (2, 3, 5, 7):
-        while m % f == 0:
-            m //= f
-    if m == 1 or n <= 64:
-        return max(n, 2)
-    return 1 << (2 * n - 2).bit_length()
-
-
 def tol_for(dtype, n):
-    return TOL[dtype] * max(1, int(np.log2(conv_len(n))))
+    """The relative-L2 bound of a transform of n points: 1e-5 log2(n) (fp32),
+    1e-13 log2(n) (fp64), whichever algorithm the plan takes for n."""
+    return TOL[dtype] * max(1, int(np.log2(max(n, 1))))
 
 
 @pytest.mark.parametrize("case", range(CASES))
@@ -104,8 +94,7 @@ def test_fuzz(fg, case):
         torch.cuda.synchronize()
         p.close()
         ref = oracle.fftn(x.astype(np.complex128), rank, direction)
-        work = int(np.prod([conv_len(v) for v in shape]))
-        assert rel_rows(y.cpu().numpy(), ref).max() <= TOL[dtype] * max(1, int(np.log2(work))), \
+        assert rel_rows(y.cpu().numpy(), ref).max() <= tol_for(dtype, int(np.prod(shape))), \
             (shape, dtype)
     elif what == 3:                                 # convolution
         nx, nh = int(g.integers(1, 3000)), int(g.integers(1, 1500))
