@@ -4,26 +4,32 @@ process per GPU, each with its own full batch: weak scaling).
 
 Default workload (``--config c2``): 16384 transforms of 4096 fp32 complex
 points (512 MiB), a step = forward then inverse (1/N).  Inputs are larger
-than L2 (129 MB), so no flush between steps is needed.
+than L2 (129 MB), so no flush between steps is needed.  The default run also
+times the other four configurations of the same method -- one 1024-point
+transform (c1, latency), one 2^26-point transform (c3, multi-pass), 8 images
+of 2048 x 2048 (c4, 2D) and 64 polynomial products of 2^20 coefficients (c5,
+fp64) -- each in its own timed region, reported under ``configs``.
 
 Metric: effective GB/s = algorithmic HBM bytes of the step / step time,
 where the algorithmic bytes of one transform call are (HBM passes of the
 chosen plan) x 2 x (bytes of the complex array); the on-chip path makes one
 pass.  Also reported: 5 N log2 N GFLOP/s, transforms/s, the roofline of
 the dominant kernel against the measured HBM copy bandwidth, the fp64 CPU
-oracle on a bounded sample, an end-to-end figure with host buffers, and
-the SM clocks sampled during the timed region.
+oracle on a bounded sample (one core and all cores), an end-to-end figure
+with host buffers, and the SM clocks sampled during the timed region.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c1..c5]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
     python bench.py --impl reference ...   # the fp64 CPU oracle, timed alone
 """
 from __future__ import annotations
 
 import argparse
+import concurrent.futures as cf
 import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -67,23 +73,14 @@ def smooth_2357(n: int) -> bool:
 
 def planned_passes(logn: int, pass_log: int) -> int:
     """HBM passes the library plans for a 2^logn-point transform beyond the
-    on-chip length: the FFT_GB300_PASS_SPLIT / FFT_GB300_PASS_LOG tuning
-    overrides when set (as the planner reads them), else factors of at most
-    pass_log bits."""
-    split = os.environ.get("FFT_GB300_PASS_SPLIT", "")
-    try:
-        parts = [int(v) for v in split.split(",")] if split else []
-    except ValueError:
-        parts = []
-    if len(parts) >= 2 and sum(parts) == logn and all(1 <= v <= 14 for v in parts):
-        return len(parts)
-    env_log = os.environ.get("FFT_GB300_PASS_LOG", "")
-    if env_log.isdigit() and int(env_log) >= 4:
-        pass_log = min(int(env_log), 14)
+    on-chip length with factors of at most pass_log bits (its own rule; the
+    bench reads the real count from the plan it builds)."""
     return max(2, math.ceil(logn / pass_log))
 
 
-def workload_info(name: str, pass_log: int = 9):
+def workload_info(name: str, pass_log: int = 9, passes=None):
+    """Bytes, flops and units of one step.  `passes`: the HBM passes of the
+    plan actually built (its kernel count), for the multi-pass 1D kind."""
     c = config_of(name)
     n, batch = c["n"], c["batch"]
     if c["kind"] == "fft1d":
@@ -94,7 +91,10 @@ def workload_info(name: str, pass_log: int = 9):
                     transforms_per_step=directions * batch, h2d=arr, d2h=arr,
                     flops_per_step=directions * 5.0 * n * math.log2(max(n, 2)) * batch)
         if n & (n - 1) == 0:
-            passes = 1 if log2i(n) <= 14 else planned_passes(log2i(n), pass_log)
+            if log2i(n) <= 14:
+                passes = 1
+            elif passes is None:
+                passes = planned_passes(log2i(n), pass_log)
         elif smooth_2357(n) and 64 < n <= 12288:
             passes = 1    # mixed radix on chip: one read, one write
             info.update(mixed=True)
@@ -110,6 +110,10 @@ def workload_info(name: str, pass_log: int = 9):
                         + 12.0 * n)
         info.update(passes=passes, bytes_per_step=directions * (passes or 1) * 2 * arr,
                     ideal_bytes_per_step=directions * 2 * arr)
+        if n & (n - 1) == 0 and log2i(n) > 14:
+            # the survey's minimum for a transform beyond one block: a 2-pass
+            # four-step (every element read and written twice)
+            info.update(min_passes=2, min_bytes_per_step=directions * 2 * 2 * arr)
         return info
     if c["kind"] == "real":
         # R2C then C2R: samples (4 B) read and bins (8 B, n/2 + 1 per row)
@@ -239,9 +243,9 @@ KERNEL_SOURCES = {
     "c2": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_f32.cu"],
     "c3": ["fft_device.cuh", "fft_pass.cuh", "fft_pass_tma.cuh", "fft_pass_cluster.cuh",
            "fft_pass_f32.cu", "fft_plan.cu", "fft_exec.cu", "plan.h"],
-    "c4": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_f32.cu", "fft_pass.cuh",
-           "fft_pass_tma.cuh", "fft_pass_cluster.cuh", "fft_pass_f32.cu", "fft_plan.cu",
-           "fft_exec.cu", "plan.h"],
+    "c4": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_f32.cu", "fft_rows_col.cuh",
+           "rows_col_f32.cu", "fft_pass.cuh", "fft_pass_tma.cuh", "fft_pass_cluster.cuh",
+           "fft_pass_f32.cu", "fft_plan.cu", "fft_exec.cu", "plan.h"],
     "c5": ["fft_device.cuh", "fft_pass.cuh", "fft_pass_tma.cuh", "fft_pass_cluster.cuh",
            "fft_pass_f64.cu", "polymul.cu"],
     "conv1": ["fft_device.cuh", "fft_rows.cuh", "conv.cuh", "conv_f32.cu"],
@@ -289,102 +293,151 @@ def measured_peaks():
 # CPU oracle baseline (bounded sample of the same workload)
 # ---------------------------------------------------------------------------
 
-def cpu_oracle_sample(name: str, budget_s: float = 12.0):
-    """Times the fp64 oracle (recursive Cooley-Tukey; schoolbook-free fp64
-    pipeline for polymul) on a bounded sample of the workload and scales to
-    the metric's unit.  Single-threaded."""
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_units(name: str):
+    """(unit, fraction of one step's work per unit, sample description) for
+    the oracle's timed sample of a workload: `unit(k)` runs the k-th unit of
+    work on the oracle as it stands."""
     import oracle
     info = workload_info(name)
     c = config_of(name)
-    t0 = time.perf_counter()
-    done_units = 0.0  # fraction of one step's work
-    sample = ""
     if info["kind"] == "fft1d":
         n = c["n"]
+        two = info["directions"] == 2
         if n <= 1 << 16:
             x = workloads.config_input(name, scale_batch=min(c["batch"], 64)).astype(np.complex128)
             pow2 = n & (n - 1) == 0
-            fwd = oracle.fft if pow2 else oracle.dft          # any length: the direct DFT
-            k = 0
-            while time.perf_counter() - t0 < budget_s and k < x.shape[0] * 64:
-                r = x[k % x.shape[0]]
-                y = fwd(r)
-                if info["directions"] == 2:
+
+            def unit(k):
+                y = oracle.fft(x[k % x.shape[0]]) if pow2 else oracle.dft(x[k % x.shape[0]])
+                if two:
                     oracle.ifft(y) if pow2 else oracle.dft(y, +1)
-                k += 1
-            done_units = k / c["batch"]
-            sample = f"{k} of {c['batch']} transforms of N={n}" + \
-                (" (forward+inverse)" if info["directions"] == 2 else "")
-        elif n & (n - 1):
+            how = "recursive CT" if pow2 else "direct DFT"
+            return unit, 1.0 / c["batch"], \
+                f"transforms of N={n} ({how}{', forward+inverse' if two else ''}) of {c['batch']}"
+        if n & (n - 1):
             # a long length that is not a power of two: the oracle is the direct
-            # DFT; time bins of one row (O(N) each) and scale by the bins of the step
+            # DFT; units of 64 bins of one row (O(N) each)
             x = workloads.config_input(name, scale_batch=1)[0].astype(np.complex128)
-            bins = 0
-            while time.perf_counter() - t0 < budget_s and bins < n:
-                oracle.dft_bins(x, np.arange(bins, bins + 64, dtype=np.int64) % n)
-                bins += 64
-            done_units = bins / (n * c["batch"] * info["directions"])
-            sample = f"{bins} bins of one N={n} row by the direct sum, scaled to the step"
-        else:
-            # one long transform: time a 2^20 transform and scale by N log N
-            m = 1 << 20
-            x = workloads.normal_complex(m, 99, np.complex128)
-            k = 0
-            while time.perf_counter() - t0 < budget_s and k < 64:
-                oracle.fft(x)
-                k += 1
-            done_units = k * (m * log2i(m)) / (n * log2i(n))
-            sample = f"{k} transforms of N=2^20 scaled by N log2 N to N={n}"
-    elif info["kind"] == "fft2d":
+
+            def unit(k):
+                oracle.dft_bins(x, (np.arange(64, dtype=np.int64) + 64 * k) % n)
+            return unit, 64.0 / (n * c["batch"] * info["directions"]), \
+                f"blocks of 64 direct-DFT bins of one N={n} row, scaled to the step"
+        # one long transform: 2^20-point transforms scaled by N log N
+        m = 1 << 20
+        x = workloads.normal_complex(m, 99, np.complex128)
+
+        def unit(k):
+            oracle.fft(x)
+        return unit, (m * log2i(m)) / (n * log2i(n)), \
+            f"transforms of N=2^20 (recursive CT) scaled by N log2 N to N={n}"
+    if info["kind"] == "fft2d":
         n = c["n"]
         img = workloads.normal_complex((1, n, n), 4, np.complex128)[0]
-        k = 0
-        while time.perf_counter() - t0 < budget_s and k < 8:
-            X = oracle.fft2d(img)
-            oracle.fft2d(X, +1)
-            k += 1
-        done_units = k / c["batch"]
-        sample = f"{k} of {c['batch']} images {n}x{n} (forward+inverse)"
-    elif info["kind"] == "fftnd":
+
+        def unit(k):
+            oracle.fft2d(oracle.fft2d(img), +1)
+        return unit, 1.0 / c["batch"], f"images {n}x{n} (forward+inverse) of {c['batch']}"
+    if info["kind"] == "fftnd":
         vol = workloads.normal_complex((1,) + tuple(c["shape"]), c["seed"], np.complex128)
-        k = 0
-        while time.perf_counter() - t0 < budget_s and k < 4:
-            Y = oracle.fftn(vol, len(c["shape"]))
-            oracle.fftn(Y, len(c["shape"]), +1)
-            k += 1
-        done_units = k / c["batch"]
-        sample = f"{k} of {c['batch']} volumes {c['shape']} (forward+inverse)"
-    elif info["kind"] == "real":
+
+        def unit(k):
+            oracle.fftn(oracle.fftn(vol, len(c["shape"])), len(c["shape"]), +1)
+        return unit, 1.0 / c["batch"], f"volumes {c['shape']} (forward+inverse) of {c['batch']}"
+    if info["kind"] == "real":
         x = workloads.normal_real((64, c["n"]), c["seed"], np.float64)
-        k = 0
-        while time.perf_counter() - t0 < budget_s and k < 64 * 64:
+
+        def unit(k):
             oracle.irfft(oracle.rfft(x[k % 64]), c["n"])
-            k += 1
-        done_units = k / c["batch"]
-        sample = f"{k} of {c['batch']} real rows of N={c['n']} (forward+inverse)"
-    elif info["kind"] == "conv":
+        return unit, 1.0 / c["batch"], f"real rows of N={c['n']} (forward+inverse) of {c['batch']}"
+    if info["kind"] == "conv":
         x, h = workloads.conv_signals(64, c["n"], c["nh"], c["seed"])
-        k = 0
-        while time.perf_counter() - t0 < budget_s and k < 64:
-            oracle.convolve(x[k].astype(np.complex128), h.astype(np.complex128))
-            k += 1
-        done_units = k / c["batch"]
-        sample = f"{k} of {c['batch']} signals (direct sum, {c['n']} x {c['nh']} taps)"
+        h = h.astype(np.complex128)
+
+        def unit(k):
+            oracle.convolve(x[k % 64].astype(np.complex128), h)
+        return unit, 1.0 / c["batch"], \
+            f"signals (direct sum, {c['n']} x {c['nh']} taps) of {c['batch']}"
+    m = 1 << 16
+    a, b = workloads.poly_coeffs(m, 5)
+    L, Lm = info["L"], 1 << (2 * m - 1 - 1).bit_length()
+
+    def unit(k):
+        oracle.polymul_fft(a, b)
+    return unit, (Lm * log2i(Lm)) / (L * log2i(L)) / c["batch"], \
+        "fp64 FFT products of 2^16-coefficient pairs, scaled by L log2 L to 2^20"
+
+
+def cpu_oracle_sample(name: str, budget_s: float = 6.0, threads: int = 1):
+    """Times the fp64 oracle as it stands on a bounded sample of the
+    workload (about `budget_s` seconds) on `threads` host threads -- units of
+    work run concurrently, each a plain call into the oracle's C code, which
+    releases the interpreter lock -- and scales to the metric's unit."""
+    info = workload_info(name)
+    unit, frac, what = _oracle_units(name)
+    unit(0)  # first-call set-up (library load) outside the timed sample
+    done = [0] * threads
+    t0 = time.perf_counter()
+    deadline = t0 + budget_s
+
+    def worker(w):
+        k = w
+        while True:
+            unit(k)
+            done[w] += 1
+            k += threads
+            if time.perf_counter() >= deadline:
+                return
+    if threads == 1:
+        worker(0)
     else:
-        n = c["n"]
-        m = 1 << 16
-        a, b = workloads.poly_coeffs(m, 5)
-        k = 0
-        while time.perf_counter() - t0 < budget_s and k < 64:
-            oracle.polymul_fft(a, b)
-            k += 1
-        L, Lm = info["L"], 1 << (2 * m - 1 - 1).bit_length()
-        done_units = k * (Lm * log2i(Lm)) / (L * log2i(L)) / c["batch"]
-        sample = f"{k} fp64 products of 2^16-coefficient pairs, scaled by L log2 L"
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(worker, range(threads)))
     el = time.perf_counter() - t0
-    gbs = info["bytes_per_step"] * done_units / el / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
-            "seconds": round(el, 3)}
+    units = sum(done)
+    step_fraction = units * frac
+    gbs = info["bytes_per_step"] * step_fraction / el / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{units} {what}", "seconds": round(el, 3),
+            "step_fraction": step_fraction}
+
+
+def cpu_baselines(name: str, budget_s: float):
+    """The oracle on one core and on every core of the host, with the CPU
+    model; the one-core figure is the headline baseline."""
+    one = cpu_oracle_sample(name, budget_s, 1)
+    n = host_cores()
+    if n > 1:
+        allc = cpu_oracle_sample(name, budget_s, n)
+        one["all_cores"] = {k: allc[k] for k in ("value", "unit", "cores", "sample", "seconds")}
+    one["cpu_model"] = cpu_model()
+    return one
 
 
 # ---------------------------------------------------------------------------
@@ -438,113 +491,173 @@ def dist_env():
     return rank, world, local
 
 
-def run_gpu(args):
-    import torch
-    import torch.distributed as dist
+class Workload:
+    """Device buffers, plans and one step of a workload, on `stream`."""
 
-    import fft_convolution_gb300 as fg
+    def __init__(self, name, fg, torch, dev, stream):
+        self.name = name
+        c = self.c = config_of(name)
+        info = workload_info(name)
+        self.kind = info["kind"]
+        self.stream = stream
+        sh = self.sh = int(stream.cuda_stream)
+        self.plans = []
+        self.fg = fg
+        self.torch = torch
+        # Inputs smaller than L2 (129 MB): a 256 MiB buffer written before
+        # every step evicts them, so every timed call starts from HBM.
+        self.flush = torch.empty(1 << 26, dtype=torch.float32, device=dev) \
+            if info["array_bytes"] <= L2_BYTES else None
+        if info["kind"] == "conv":
+            self.xc_h, self.hc_h = workloads.conv_signals(c["batch"], c["n"], c["nh"], c["seed"])
+            self.xc_d = torch.from_numpy(self.xc_h).to(dev)
+            self.hc_d = torch.from_numpy(self.hc_h).to(dev)
+            ny = c["n"] + c["nh"] - 1
+            self.yc_d = torch.empty(c["batch"], ny, dtype=torch.float32, device=dev)
+            self.kernels_per_step = fg.fft_convolve_num_kernels(
+                c["n"], c["nh"], c["batch"], 0, fg.FFT_CONV_REAL, fg.FFT_C2C_F32)
+        elif info["kind"] == "polymul":
+            self.a_h, self.b_h = workloads.poly_coeffs((c["batch"], c["n"]), c["seed"])
+            self.a_d, self.b_d = torch.from_numpy(self.a_h).to(dev), torch.from_numpy(self.b_h).to(dev)
+            self.c_d = torch.empty(c["batch"], 2 * c["n"] - 1, dtype=torch.int64, device=dev)
+            self.kernels_per_step = fg.polymul_num_kernels(c["n"], c["n"])
+        elif info["kind"] == "real":
+            self.x_h = sized_input(name, c)
+            self.x_d = torch.from_numpy(self.x_h).to(dev)
+            n, batch = c["n"], c["batch"]
+            self.X_d = torch.empty(batch, n // 2 + 1, dtype=torch.complex64, device=dev)
+            self.y_d = torch.empty_like(self.x_d)
+            self.plans = [fg.Plan(n, batch, 1, fg.FFT_FORWARD, fg.FFT_REAL_F32),
+                          fg.Plan(n, batch, 1, fg.FFT_INVERSE, fg.FFT_REAL_F32)]
+            self.kernels_per_step = sum(p.num_kernels for p in self.plans)
+        else:
+            self.x_h = sized_input(name, c)
+            self.x_d = torch.from_numpy(self.x_h).to(dev)
+            self.y_d = torch.empty_like(self.x_d)
+            self.z_d = torch.empty_like(self.x_d)
+            dims = 2 if info["kind"] == "fft2d" else 1
+            shape = tuple(c["shape"]) if info["kind"] == "fftnd" else None
+            self.plans = [fg.Plan(c["n"], c["batch"], dims, fg.FFT_FORWARD, fg.FFT_C2C_F32,
+                                  shape=shape)]
+            if info["directions"] == 2:
+                self.plans.append(fg.Plan(c["n"], c["batch"], dims, fg.FFT_INVERSE,
+                                          fg.FFT_C2C_F32, shape=shape))
+            self.kernels_per_step = sum(p.num_kernels for p in self.plans)
+        # The HBM passes of the plan actually built (multi-pass 1D: one per kernel).
+        passes = None
+        if info["kind"] == "fft1d" and c["n"] & (c["n"] - 1) == 0 and log2i(c["n"]) > 14:
+            passes = self.plans[0].num_kernels
+        self.info = workload_info(name, passes=passes)
 
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local)
-    name = args.config
-    c = config_of(name)
-    info = workload_info(name)
+    def step(self, events=None):
+        """One step; events[0..2] (optional) bracket its launches: [0]..[1]
+        the first (dominant) call, [1]..[2] the second.  Inputs smaller than
+        L2 are preceded by an L2 flush (outside the brackets)."""
+        fg, sh, st = self.fg, self.sh, self.stream
+        if self.flush is not None:
+            with self.torch.cuda.stream(st):
+                self.flush.zero_()
+        if events is not None:
+            events[0].record(st)
+        if self.kind == "conv":
+            rc = [fg.fft_convolve(self.xc_d.data_ptr(), self.c["n"], self.hc_d.data_ptr(),
+                                  self.c["nh"], self.yc_d.data_ptr(), self.c["batch"], 0,
+                                  fg.FFT_CONV_REAL, fg.FFT_C2C_F32, sh)]
+        elif self.kind == "polymul":
+            rc = [fg.polymul_batched(self.a_d.data_ptr(), self.c["n"], self.b_d.data_ptr(),
+                                     self.c["n"], self.c_d.data_ptr(), self.c["batch"], sh)]
+        elif self.kind == "real":
+            rc = [fg.fft_exec(self.plans[0].handle, self.x_d.data_ptr(), self.X_d.data_ptr(), sh)]
+        else:
+            rc = [fg.fft_exec(self.plans[0].handle, self.x_d.data_ptr(), self.y_d.data_ptr(), sh)]
+        if events is not None:
+            events[1].record(st)
+        if self.kind == "real":
+            rc.append(fg.fft_exec(self.plans[1].handle, self.X_d.data_ptr(), self.y_d.data_ptr(),
+                                  sh))
+        elif self.kind not in ("conv", "polymul") and len(self.plans) == 2:
+            rc.append(fg.fft_exec(self.plans[1].handle, self.y_d.data_ptr(), self.z_d.data_ptr(),
+                                  sh))
+        if events is not None:
+            events[2].record(st)
+        assert all(r == 0 for r in rc), [fg.fft_status_string(r) for r in rc]
+
+    def e2e_step_fn(self, torch, chunks):
+        """One end-to-end step through the host-buffer entry points (pinned
+        host input -> device, the transforms, device -> pinned host output),
+        and the number of chunks the batch streams through in."""
+        fg, sh, c = self.fg, self.sh, self.c
+        chunk = max(1, c["batch"] // chunks)
+        if self.kind in ("fft1d", "fft2d", "fftnd", "real"):
+            h_in = torch.from_numpy(self.x_h).pin_memory()
+            h_out = torch.empty_like(h_in).pin_memory()
+            dev_b = self.X_d if self.kind == "real" else self.y_d
+            plans = self.plans
+
+            def f():
+                plans[0].chain_host(plans[1:], h_in, h_out, self.x_d, dev_b, chunk, self.stream)
+            return f, chunk
+        if self.kind == "conv":
+            hx = torch.from_numpy(self.xc_h).pin_memory()
+            hy = torch.empty(self.yc_d.shape, dtype=torch.float32).pin_memory()
+
+            def f():
+                rc = fg.fft_convolve_host(hx.data_ptr(), c["n"], self.hc_d.data_ptr(), c["nh"],
+                                          hy.data_ptr(), c["batch"], 0, fg.FFT_CONV_REAL,
+                                          fg.FFT_C2C_F32, self.xc_d.data_ptr(),
+                                          self.yc_d.data_ptr(), chunk, sh)
+                assert rc == 0, fg.fft_status_string(rc)
+            return f, chunk
+        ha, hb = torch.from_numpy(self.a_h).pin_memory(), torch.from_numpy(self.b_h).pin_memory()
+        hc = torch.empty(self.c_d.shape, dtype=torch.int64).pin_memory()
+
+        def f():
+            rc = fg.polymul_batched_host(ha.data_ptr(), c["n"], hb.data_ptr(), c["n"],
+                                         hc.data_ptr(), c["batch"], self.a_d.data_ptr(),
+                                         self.b_d.data_ptr(), self.c_d.data_ptr(), chunk, sh)
+            assert rc == 0, fg.fft_status_string(rc)
+        return f, chunk
+
+    def close(self):
+        for p in self.plans:
+            p.close()
+
+
+def graph_latency_us(w: Workload, torch, replays: int = 20, per_graph: int = 256) -> float:
+    """Device time per transform of `per_graph` back-to-back forward calls
+    captured in one CUDA graph (no host enqueue between them), averaged over
+    `replays` replays timed with one pair of events."""
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device=w.x_d.device)
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=cap):
+        sh = int(torch.cuda.current_stream().cuda_stream)
+        for _ in range(per_graph):
+            rc = w.fg.fft_exec(w.plans[0].handle, w.x_d.data_ptr(), w.y_d.data_ptr(), sh)
+            assert rc == 0, w.fg.fft_status_string(rc)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(replays):
+        g.replay()
+    e1.record()
+    e1.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (replays * per_graph)
+    del g
+    return us
+
+
+def measure(name, args, fg, torch, dev, world, barrier, with_cpu):
+    """Times `args.steps` steps of workload `name` after `args.warmup`
+    untimed ones (clocks sampled over an untimed soak that runs straight
+    into the timed region) and returns the JSON fields of its line."""
     stream = torch.cuda.Stream(device=dev)
-    sh = int(stream.cuda_stream)
-
-    # Inputs: seeded on the host, resident in HBM before timing.
-    if info["kind"] == "conv":
-        xc_h, hc_h = workloads.conv_signals(c["batch"], c["n"], c["nh"], c["seed"])
-        xc_d, hc_d = torch.from_numpy(xc_h).to(dev), torch.from_numpy(hc_h).to(dev)
-        ny = c["n"] + c["nh"] - 1
-        yc_d = torch.empty(c["batch"], ny, dtype=torch.float32, device=dev)
-        plans = []
-
-        def step(events=None):
-            if events is not None:
-                events[0].record(stream)
-            rc = fg.fft_convolve(xc_d.data_ptr(), c["n"], hc_d.data_ptr(), c["nh"],
-                                 yc_d.data_ptr(), c["batch"], 0, fg.FFT_CONV_REAL,
-                                 fg.FFT_C2C_F32, sh)
-            if events is not None:
-                events[1].record(stream)
-            assert rc == 0, fg.fft_status_string(rc)
-        kernels_per_step = fg.fft_convolve_num_kernels(c["n"], c["nh"], c["batch"], 0,
-                                                       fg.FFT_CONV_REAL, fg.FFT_C2C_F32)
-    elif info["kind"] == "polymul":
-        a_h, b_h = workloads.poly_coeffs((c["batch"], c["n"]), c["seed"])
-        a_d, b_d = torch.from_numpy(a_h).to(dev), torch.from_numpy(b_h).to(dev)
-        c_d = torch.empty(c["batch"], 2 * c["n"] - 1, dtype=torch.int64, device=dev)
-        plans = []
-
-        def step(events=None):
-            with torch.cuda.stream(stream):
-                if events is not None:
-                    events[0].record(stream)
-                rc = fg.polymul_batched(a_d.data_ptr(), c["n"], b_d.data_ptr(), c["n"],
-                                        c_d.data_ptr(), c["batch"], sh)
-                if events is not None:
-                    events[1].record(stream)
-            assert rc == 0, fg.fft_status_string(rc)
-        kernels_per_step = fg.polymul_num_kernels(c["n"], c["n"])
-    elif info["kind"] == "real":
-        x_h = sized_input(name, c)
-        x_d = torch.from_numpy(x_h).to(dev)
-        n, batch = c["n"], c["batch"]
-        X_d = torch.empty(batch, n // 2 + 1, dtype=torch.complex64, device=dev)
-        y_d = torch.empty_like(x_d)
-        pf = fg.Plan(n, batch, 1, fg.FFT_FORWARD, fg.FFT_REAL_F32)
-        pi = fg.Plan(n, batch, 1, fg.FFT_INVERSE, fg.FFT_REAL_F32)
-        plans = [pf, pi]
-
-        def step(events=None):
-            if events is not None:
-                events[0].record(stream)
-            r0 = fg.fft_exec(pf.handle, x_d.data_ptr(), X_d.data_ptr(), sh)
-            if events is not None:
-                events[1].record(stream)
-            r1 = fg.fft_exec(pi.handle, X_d.data_ptr(), y_d.data_ptr(), sh)
-            if events is not None:
-                events[2].record(stream)
-            assert r0 == 0 and r1 == 0, (fg.fft_status_string(r0), fg.fft_status_string(r1))
-        kernels_per_step = pf.num_kernels + pi.num_kernels
-    else:
-        x_h = sized_input(name, c)
-        x_d = torch.from_numpy(x_h).to(dev)
-        y_d = torch.empty_like(x_d)
-        z_d = torch.empty_like(x_d)
-        dims = 2 if info["kind"] == "fft2d" else 1
-        n, batch = c["n"], c["batch"]
-        shape = tuple(c["shape"]) if info["kind"] == "fftnd" else None
-        pf = fg.Plan(n, batch, dims, fg.FFT_FORWARD, fg.FFT_C2C_F32, shape=shape)
-        plans = [pf]
-        if info["directions"] == 2:
-            pi = fg.Plan(n, batch, dims, fg.FFT_INVERSE, fg.FFT_C2C_F32, shape=shape)
-            plans.append(pi)
-
-        def step(events=None):
-            rcs = []
-            if events is not None:
-                events[0].record(stream)
-            rcs.append(fg.fft_exec(pf.handle, x_d.data_ptr(), y_d.data_ptr(), sh))
-            if events is not None:
-                events[1].record(stream)
-            if len(plans) == 2:
-                rcs.append(fg.fft_exec(plans[1].handle, y_d.data_ptr(), z_d.data_ptr(), sh))
-                if events is not None:
-                    events[2].record(stream)
-            assert all(r == 0 for r in rcs), [fg.fft_status_string(r) for r in rcs]
-        kernels_per_step = sum(p.num_kernels for p in plans)
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
+    w = Workload(name, fg, torch, dev, stream)
+    info, c = w.info, w.c
     for _ in range(args.warmup):
-        step()
+        w.step()
     torch.cuda.synchronize(dev)
 
     # Clock sampling: nvidia-smi samples every 100 ms, longer than most timed
@@ -552,14 +665,13 @@ def run_gpu(args):
     # steps (>= args.clock_soak seconds of load) that leads straight into
     # the timed region; the clocks reported are those of the GPU under this
     # load.
-    nev = 3
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
-    clocks = ClockSampler(local)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     t_soak = time.perf_counter()
     while time.perf_counter() - t_soak < args.clock_soak:
         for _ in range(4):
-            step()
+            w.step()
         torch.cuda.synchronize(dev)
 
     # Timed region.
@@ -569,120 +681,89 @@ def run_gpu(args):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for k in range(args.steps):
-        step(ev[k])
+        w.step(ev[k])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     clk = clocks.stop()
     ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     ms_step = ms_total / args.steps
+    if w.flush is not None:
+        # The step's own time, without the L2 flush before it.
+        ms_step = max_over_ranks(statistics.mean(e[0].elapsed_time(e[2]) for e in ev), world,
+                                 dev)
 
-    # Per-launch durations of the dominant kernel (the forward transform;
-    # for 1-kernel plans that is one launch per exec).
+    # Per-launch durations of the dominant call (the forward transform).
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    inv_ms = [e[1].elapsed_time(e[2]) for e in ev] if info["kind"] in ("fft1d", "fft2d", "fftnd",
-                                                                        "real") and \
-        info["directions"] == 2 else []
+    inv_ms = [e[1].elapsed_time(e[2]) for e in ev] \
+        if info["kind"] in ("fft1d", "fft2d", "fftnd", "real") and info["directions"] == 2 else []
 
-    # End-to-end through the host-buffer entry point: pinned host input ->
-    # device, transforms, device -> pinned host output, every step.
+    # End-to-end through the host-buffer entry points, every step.
     e2e = None
-    if info["kind"] in ("fft1d", "fft2d", "fftnd", "real") and not args.no_e2e:
-        h_in = torch.from_numpy(x_h).pin_memory()
-        h_out = torch.empty_like(h_in).pin_memory()
-        e2e_steps = max(5, min(args.steps, 10))
-        # Chunks of the batch stream through the device: uploads, transforms
-        # and downloads of different chunks overlap (fft_exec_host_chain).
-        chunk = max(1, c["batch"] // args.e2e_chunks)
-        # Samples in x_d, spectra in X_d for the real round trip.
-        dev_b = X_d if info["kind"] == "real" else y_d
-
-        def e2e_step():
-            plans[0].chain_host(plans[1:], h_in, h_out, x_d, dev_b, chunk, stream)
-        t = time_host_steps(e2e_step, stream, e2e_steps)
+    if not args.no_e2e:
+        f, chunk = w.e2e_step_fn(torch, args.e2e_chunks)
+        nsteps = 5 if info["kind"] == "polymul" else max(5, min(args.steps, 10))
+        t = time_host_steps(f, stream, nsteps)
         e2e_ms = t["median_ms"]
-        e2e = {"value": info["bytes_per_step"] * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": info["h2d"], "d2h_bytes_per_step": info["d2h"],
-               "ms_per_step": round(e2e_ms, 4), "ms_mean": round(t["mean_ms"], 4),
-               "ms_min": round(t["min_ms"], 4), "timed_steps": e2e_steps,
-               "chunk_transforms": chunk}
-    elif info["kind"] == "conv" and not args.no_e2e:
-        hx = torch.from_numpy(xc_h).pin_memory()
-        hy = torch.empty(yc_d.shape, dtype=torch.float32).pin_memory()
-        chunk = max(1, c["batch"] // args.e2e_chunks)
-
-        def e2e_step():
-            # Chunks of rows stream through the device (fft_convolve_host).
-            rc = fg.fft_convolve_host(hx.data_ptr(), c["n"], hc_d.data_ptr(), c["nh"],
-                                      hy.data_ptr(), c["batch"], 0, fg.FFT_CONV_REAL,
-                                      fg.FFT_C2C_F32, xc_d.data_ptr(), yc_d.data_ptr(), chunk, sh)
-            assert rc == 0, fg.fft_status_string(rc)
-        t = time_host_steps(e2e_step, stream, max(5, min(args.steps, 10)))
-        e2e_ms = t["median_ms"]
-        e2e = {"value": info["bytes_per_step"] * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": info["h2d"], "d2h_bytes_per_step": info["d2h"],
-               "ms_per_step": round(e2e_ms, 4), "ms_mean": round(t["mean_ms"], 4),
-               "ms_min": round(t["min_ms"], 4), "timed_steps": t["steps"]}
-    elif info["kind"] == "polymul" and not args.no_e2e:
-        ha, hb = torch.from_numpy(a_h).pin_memory(), torch.from_numpy(b_h).pin_memory()
-        hc = torch.empty(c_d.shape, dtype=torch.int64).pin_memory()
-
-        chunk = max(1, c["batch"] // args.e2e_chunks)
-
-        def e2e_step():
-            # Chunks of pairs stream through the device (polymul_batched_host).
-            rc = fg.polymul_batched_host(ha.data_ptr(), c["n"], hb.data_ptr(), c["n"],
-                                         hc.data_ptr(), c["batch"], a_d.data_ptr(),
-                                         b_d.data_ptr(), c_d.data_ptr(), chunk, sh)
-            assert rc == 0, fg.fft_status_string(rc)
-        t = time_host_steps(e2e_step, stream, 5, warmup=2)
-        e2e_ms = t["median_ms"]
-        e2e = {"value": info["bytes_per_step"] * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": info["h2d"], "d2h_bytes_per_step": info["d2h"],
-               "ms_per_step": round(e2e_ms, 4), "ms_mean": round(t["mean_ms"], 4),
-               "ms_min": round(t["min_ms"], 4), "timed_steps": t["steps"]}
+        e2e = {"value": round(info["bytes_per_step"] * world / (e2e_ms * 1e-3) / 1e9, 2),
+               "unit": "GB/s", "h2d_bytes_per_step": info["h2d"],
+               "d2h_bytes_per_step": info["d2h"], "ms_per_step": round(e2e_ms, 4),
+               "ms_mean": round(t["mean_ms"], 4), "ms_min": round(t["min_ms"], 4),
+               "timed_steps": t["steps"], "chunk": chunk}
 
     peak, peak_kind = measured_peaks()
     value = whole_job_value(info["bytes_per_step"], world, ms_step)
-
+    dom_ms = statistics.mean(fwd_ms)
+    kps = w.kernels_per_step
     if info["kind"] == "conv":
-        dom_ms = statistics.mean(fwd_ms)
         per_launch_bytes = info["bytes_per_step"]
-        dom_name = "fft_convolve (filter spectrum + fused convolution, %d kernels)" % kernels_per_step
+        dom_name = "fft_convolve (filter spectrum + fused convolution, %d kernels)" % kps
     elif info["kind"] == "polymul":
-        dom_ms = statistics.mean(fwd_ms)
         per_launch_bytes = info["bytes_per_step"]
-        dom_name = "polymul (whole fused pipeline, %d kernels)" % kernels_per_step
+        dom_name = "polymul (whole fused pipeline, %d kernels)" % kps
     elif info["kind"] == "real":
-        dom_ms = statistics.mean(fwd_ms)
         per_launch_bytes = info["bytes_per_step"] / 2
         dom_name = ("r2c_rows_kernel<float,%d>" % log2i(c["n"] // 2)) if info["passes"] == 1 \
-            else "forward real plan (%d kernels)" % plans[0].num_kernels
+            else "forward real plan (%d kernels)" % w.plans[0].num_kernels
     else:
-        dom_ms = statistics.mean(fwd_ms)
         per_launch_bytes = info["bytes_per_step"] / info["directions"]
         dom_name = ("fft_rows_kernel<float,%d,-1>" % log2i(c["n"])) if info["passes"] == 1 and \
-            info["kind"] == "fft1d" else "forward plan (%d kernels)" % plans[0].num_kernels
+            info["kind"] == "fft1d" else "forward plan (%d kernels)" % w.plans[0].num_kernels
         if info.get("mixed"):
             dom_name = "mixed_rows_kernel<float,-1> (N=%d)" % c["n"]
         if info.get("four_step"):
-            dom_name = "forward four-step plan (%d kernels, N=%d)" % (plans[0].num_kernels, c["n"])
+            dom_name = "forward four-step plan (%d kernels, N=%d)" % (w.plans[0].num_kernels,
+                                                                      c["n"])
     achieved = per_launch_bytes / (dom_ms * 1e-3) / 1e9
     tr = committed_traffic(name)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": tr["traffic_bytes_per_launch"] if tr else None,
                 "kernel": dom_name, "peak_source": peak_kind,
+                "bytes_per_launch": per_launch_bytes,
                 "launch_ms": round(dom_ms, 4),
                 "inverse_launch_ms": round(statistics.mean(inv_ms), 4) if inv_ms else None}
+    if info.get("min_bytes_per_step"):
+        # Against the survey's 2-pass minimum for this length, next to the
+        # chosen plan's own pass count.
+        mb = info["min_bytes_per_step"] / info["directions"]
+        roofline.update(min_passes=info["min_passes"], min_bytes_per_launch=mb,
+                        frac_vs_min_passes=round(mb / (dom_ms * 1e-3) / 1e9 / peak, 4))
     if info["kind"] == "polymul":
-        # Bound by the FP64 pipe: flops of the transforms run (5 M log2 M each) per pipeline
-        # launch against the GB300's nominal 1.25 TFLOP/s FP64 (an FMA probe measured 1.19).
+        # Bound by the FP64 pipe.  Two flop counts per pipeline launch: the
+        # transforms the pipeline runs (one of length L for a + ib, one of
+        # length L/2 for the real product: 5 M log2 M each) and the method's
+        # count (three length-L transforms), against the GB300's nominal
+        # 1.25 TFLOP/s FP64 (an FMA probe on this part measured 1.19).
         fl = info["fp64_flops_per_step"]
         tf = fl / (dom_ms * 1e-3) / 1e12
+        mfl = info["flops_per_step"]
+        mtf = mfl / (dom_ms * 1e-3) / 1e12
         roofline.update(bound="alu", achieved=round(tf, 4), peak=1.25, unit="TFLOP/s",
                         frac=round(tf / 1.25, 4), flops_per_launch=fl,
-                        peak_source="nominal FP64 (1.25 TFLOP/s); measured FMA probe 1.19",
+                        method_flops_per_launch=mfl, method_achieved=round(mtf, 4),
+                        method_frac=round(mtf / 1.25, 4),
+                        peak_source="nominal FP64 (1.25 TFLOP/s); FMA probe measured 1.19",
                         hbm_achieved_gbs=round(achieved, 1))
     if info.get("bluestein_m") and info["passes"] == 1:
         # Two length-M transforms per row of n points: the fused Bluestein kernel is bound by
@@ -697,40 +778,103 @@ def run_gpu(args):
                         % (log2i(info["bluestein_m"]), info["bluestein_m"]),
                         hbm_achieved_gbs=round(achieved, 1),
                         flops_per_launch=flops)
-
-    line = {
+    fields = {
         "metric": metric_name(info["kind"]),
         "value": round(value, 2),
         "unit": "GB/s",
-        "n_gpus": world,
+        "ms_per_step": round(ms_step, 4),
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
         "dtype": "f64" if info["kind"] == "polymul" else "f32",
-        "data": "synthetic (seeded)",
-        "config": {"workload": workload_label(name), "l2": "inputs larger than L2, no flush",
-                   "hbm_passes": info["passes"], "parallelism": f"replicas x{world}"},
+        "config": config_dict(name, info, world),
         "hbm_frac": round(value / world / peak, 4),
         "ideal_1pass_frac": round(info["ideal_bytes_per_step"] / (ms_step * 1e-3) / 1e9 / peak, 4),
         "gflops": round(info["flops_per_step"] * world / (ms_step * 1e-3) / 1e9, 1),
         "transforms_per_s": round(info["transforms_per_step"] * world / (ms_step * 1e-3), 1),
-        "gpu_launches": kernels_per_step * args.steps,
+        "gpu_launches": kps * args.steps,
         "roofline": roofline,
         "e2e": e2e,
         "clocks": clk,
-        "clock_soak_s": args.clock_soak,
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(name)
+    if name == "c1" and not SIZE_OVERRIDE:
+        # Latency of one 1024-point transform: the step time above brackets
+        # the host's enqueue of each call (ctypes + launch); the device time
+        # per transform comes from back-to-back calls replayed from a graph.
+        dev_us = graph_latency_us(w, torch)
+        fields["latency"] = {"cold_l2_call_us": round(ms_step * 1e3, 3),
+                             "cold_l2_call_how": "events around each call (host enqueue "
+                                                 "included), L2 flushed before it",
+                             "device_us_per_transform": round(dev_us, 3),
+                             "device_how": "256 back-to-back forward calls captured in one CUDA "
+                                           "graph, 20 replays between one pair of events (warm "
+                                           "L2)"}
+    if with_cpu:
+        fields["cpu_baseline"] = cpu_baselines(name, args.cpu_seconds)
+    w.close()
+    return fields
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import fft_convolution_gb300 as fg
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    head = measure(args.config, args, fg, torch, dev, world, barrier, with_cpu)
+    line = {
+        "metric": head["metric"],
+        "value": head["value"],
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": head["dtype"],
+        "data": "synthetic (seeded)",
+    }
+    line.update({k: v for k, v in head.items() if k not in line})
+    line["clock_soak_s"] = args.clock_soak
+    extras = [] if args.no_extra_configs or args.config != "c2" or SIZE_OVERRIDE else \
+        [c for c in EXTRA_CONFIGS if c != args.config]
+    if extras:
+        line["configs"] = {}
+        for nm in extras:
+            line["configs"][nm] = measure(nm, args, fg, torch, dev, world, barrier, with_cpu)
+        # Launches of every timed region of this run (headline and configs).
+        line["gpu_launches_all_configs"] = line["gpu_launches"] + sum(
+            e["gpu_launches"] for e in line["configs"].values())
     if rank == 0:
         print(json.dumps(line), flush=True)
-    for p in plans:
-        p.close()
     if world > 1:
         dist.destroy_process_group()
+
+
+# The other configurations of the method, timed by the default run beside
+# the c2 headline.
+EXTRA_CONFIGS = ("c1", "c3", "c4", "c5")
+
+
+L2_BYTES = 129e6
+
+
+def config_dict(name: str, info: dict, world: int) -> dict:
+    return {"workload": workload_label(name), "l2": "inputs larger than L2, no flush"
+            if info["array_bytes"] > L2_BYTES else "L2 flushed (256 MiB written) before every "
+            "timed step", "hbm_passes": info["passes"], "parallelism": f"replicas x{world}"}
 
 
 def sized_input(name: str, c: dict):
@@ -752,6 +896,8 @@ def metric_name(kind: str) -> str:
         return "batched FFT convolution effective GB/s"
     if kind == "real":
         return "batched real FFT (R2C + C2R) effective GB/s"
+    if kind == "polymul":
+        return "batched FFT polynomial multiplication effective GB/s (int64 in and out)"
     return "batched C2C FFT effective GB/s"
 
 
@@ -790,6 +936,10 @@ def workload_label(name: str) -> str:
 # ---------------------------------------------------------------------------
 
 def run_reference(args):
+    """The fp64 CPU oracle as it stands, on every host core: each step is a
+    bounded sample (about --ref-step-seconds) of the workload's work, and
+    the line reports the rate over the sampled work, the sampled fraction of
+    a full step, and the wall time actually spent."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
@@ -797,18 +947,22 @@ def run_reference(args):
     oracle.build()
     name = args.config
     info = workload_info(name)
+    cores = host_cores()
 
     def one_step():
-        return cpu_oracle_sample(name, budget_s=args.ref_step_seconds)
+        return cpu_oracle_sample(name, budget_s=args.ref_step_seconds, threads=cores)
+    t_all = time.perf_counter()
     for _ in range(args.warmup):
         one_step()
-    vals, secs, last = [], 0.0, None
+    t0 = time.perf_counter()
+    done, secs, last = 0.0, 0.0, None
     for _ in range(args.steps):
         last = one_step()
-        vals.append(last["value"])
+        done += last["step_fraction"]
         secs += last["seconds"]
-    value = statistics.mean(vals)
-    ms_step = 1e3 * info["bytes_per_step"] / (value * 1e9)
+    wall = time.perf_counter() - t0
+    value = info["bytes_per_step"] * done / secs / 1e9
+    ms_step = 1e3 * secs / args.steps
     line = {
         "impl": "reference",
         "metric": metric_name(info["kind"]),
@@ -817,14 +971,21 @@ def run_reference(args):
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
+        # Wall time of one timed (sampled) step; the sampled work is
+        # `sample_fraction` of a full step.
         "ms_per_step": round(ms_step, 2),
+        "sample_fraction": float(f"{done / args.steps:.4g}"),
+        "extrapolated": {"ms_per_full_step": round(ms_step * args.steps / done, 2)
+                         if done > 0 else None},
+        "wall_s": {"timed": round(wall, 2), "total": round(time.perf_counter() - t_all, 2)},
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded)",
-        "config": {"workload": workload_label(name), "l2": "n/a (CPU)"},
-        "cpu_baseline": {"value": float(f"{value:.4g}"), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "config": config_dict(name, info, world),
+        "cpu_baseline": {"value": float(f"{value:.4g}"), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "cpu_model": cpu_model(),
                          "sample": last["sample"] + " per step"},
         "e2e": {"value": float(f"{value:.4g}"), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -840,6 +1001,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", choices=sorted(workloads.CONFIGS), default="c2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="time only --config (the default c2 run also times c1, c3, c4, c5)")
+    ap.add_argument("--cpu-seconds", type=float, default=5.0,
+                    help="seconds of oracle work per CPU-baseline sample (one core, all cores)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=16,
                     help="batch chunks streamed through the device by the end-to-end pipeline")

@@ -37,6 +37,14 @@ FFT_REAL_F64 = 3
 FFT_CONV_COMPLEX = 0
 FFT_CONV_REAL = 1
 
+FFT_OPT_PASS_LOG = 1
+FFT_OPT_PASS_SPLIT = 2
+FFT_OPT_NO_TMA = 3
+FFT_OPT_NO_CLUSTER = 4
+FFT_OPT_CLUSTER_LOG_MIN = 5
+FFT_OPT_ND_ROWS_T = 6
+FFT_OPT_COL_RADIX_LOG = 7
+
 # Every symbol the header declares, with its ctypes signature.
 _VP, _I64, _INT, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
@@ -61,6 +69,7 @@ SIGNATURES = {
     "fft_device_status": (_INT, [_VP]),
     "fft_debug_wait_timeout": (_INT, [_I64, _VP]),
     "fft_debug_cluster_timeout": (_INT, [_VP, _I64, _VP]),
+    "fft_debug_set_option": (_INT, [_INT, _I64]),
     "fft_last_status": (_INT, []),
     "fft_status_string": (ctypes.c_char_p, [_INT]),
     "fft_last_cuda_error": (ctypes.c_char_p, []),
@@ -200,6 +209,21 @@ def fft_debug_wait_timeout(polls: int, stream: int) -> int:
 
 def fft_debug_cluster_timeout(data_ptr: int, polls: int, stream: int) -> int:
     return int(_lib.fft_debug_cluster_timeout(data_ptr, polls, stream))
+
+
+def fft_debug_set_option(option: int, value: int) -> int:
+    """Test / tuning hook: force one planning or launch choice (FFT_OPT_*);
+    value < 0 restores the library's own choice."""
+    return int(_lib.fft_debug_set_option(option, value))
+
+
+def pass_split_value(factors) -> int:
+    """FFT_OPT_PASS_SPLIT value of a list of per-pass factors (log2), first
+    pass first."""
+    v = 0
+    for k, f in enumerate(factors):
+        v |= int(f) << (4 * k)
+    return v
 
 
 def fft_device_status(stream: int) -> int:

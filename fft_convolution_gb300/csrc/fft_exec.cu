@@ -40,9 +40,6 @@ struct Schedule {
     ++count;
     return dry ? cudaSuccess : launch_pass(p->dtype, p->direction, a, in, out, st);
   }
-  int tile_cols(int log_l) const {
-    return p->dtype == FFT_C2C_F32 ? pass_tile_cols_f32(log_l) : pass_tile_cols_f64(log_l);
-  }
 
   // 2D / 3D: rows (the contiguous side) on chip, then every other axis as
   // an in-place column pass (stride = the product of the inner sides), from
@@ -86,26 +83,37 @@ struct Schedule {
 
   cudaError_t run_nd(const char *in, char *out) {
     if (p->nd_rows_t) return run_nd_rows_t(in, out);
-    const size_t tbytes = (size_t)p->elems * elem();
-    const size_t budget = l2_group_bytes();
-    long long g = budget ? (long long)(budget / tbytes) : batch;
-    if (g < 1) g = 1;
-    for (long long b0 = 0; b0 < batch; b0 += g) {
-      const long long nb = batch - b0 < g ? batch - b0 : g;
-      const size_t off = (size_t)b0 * tbytes;
-      cudaError_t e = rows(in + off, out + off, nb * (p->elems >> p->logn));
-      if (e != cudaSuccess) return e;
-      int inner = p->logn;  // log2 of the stride of the next axis
-      for (int k = p->rank - 2; k >= 0; --k) {
-        const int l = p->shape_log[k];
-        if (l > 0) {
-          const int log_block = l + inner;  // one column block: L * stride elements
-          PassArgs a{log_block, l, inner, 0, nb * (p->elems >> log_block), {}};
-          e = pass(a, out + off, out + off);
-          if (e != cudaSuccess) return e;
-        }
-        inner += l;
+    // Out of place with long columns: the row pass also takes the first
+    // radix-R stage of the column transform (fft_rows_col.cuh), and the
+    // column pass then has on-chip length H / R over columns R W apart.
+    const int logr = in != out ? p->col_radix_log : 0;
+    cudaError_t e;
+    if (logr > 0) {
+      const int logh = p->shape_log[p->rank - 2];
+      ++count;
+      e = dry ? cudaSuccess
+              : (p->dtype == FFT_C2C_F32 ? launch_rows_col_f32 : launch_rows_col_f64)(
+                    p->logn, logr, p->direction, in, out, logh,
+                    batch * (p->elems >> (p->logn + logh)), st);
+    } else {
+      e = rows(in, out, batch * (p->elems >> p->logn));
+    }
+    if (e != cudaSuccess) return e;
+    int inner = p->logn;  // log2 of the stride of the next axis
+    for (int k = p->rank - 2; k >= 0; --k) {
+      int l = p->shape_log[k];
+      int stride_log = inner;
+      if (k == p->rank - 2 && logr > 0) {  // the rest of the folded column transform
+        l -= logr;
+        stride_log += logr;
       }
+      if (l > 0) {
+        const int log_block = l + stride_log;  // one column block: L * stride elements
+        PassArgs a{log_block, l, stride_log, 0, batch * (p->elems >> log_block)};
+        e = pass(a, out, out);
+        if (e != cudaSuccess) return e;
+      }
+      inner += p->shape_log[k];
     }
     return cudaSuccess;
   }
@@ -133,7 +141,7 @@ struct Schedule {
       const long long outer = batch * (total / (L * stride));
       if (p->axis_pass[k]) {
         const int l = ilog2_exact(L), inner = ilog2_exact(stride);
-        PassArgs a{l + inner, l, inner, 0, outer, {}};
+        PassArgs a{l + inner, l, inner, 0, outer};
         e = pass(a, out, out);
       } else if (p->axis_plan[k]) {
         // [outer][L][stride] -> ws [outer][stride][L], transform, and back.
@@ -195,7 +203,7 @@ struct Schedule {
     const char *src = k_begin == 0 ? in : (k_begin % 2 == 1 ? ws : out);
     for (int k = k_begin; k < p->npasses; ++k) {
       char *dst = (k == p->npasses - 1) ? out : (k % 2 == 0 ? ws : out);
-      PassArgs a{p->logn, p->pass_log[k], log_m, 1, batch, {}};
+      PassArgs a{p->logn, p->pass_log[k], log_m, 1, batch};
       cudaError_t e = pass(a, src, dst);
       if (e != cudaSuccess) return e;
       src = dst;
@@ -204,64 +212,7 @@ struct Schedule {
     return cudaSuccess;
   }
 
-  // Passes 0 and 1 of one transform fused through L2.  Pass-1 butterfly
-  // q*L0 + p (q < Q = N/(L0 L1)) reads exactly the outputs of the pass-0
-  // butterflies q + u*Q (u < L1), so for a group of G consecutive q both
-  // passes close over G*L0*L1 elements: run pass 0 for the group (its
-  // output stays in L2), then pass 1 for the group, group after group.
-  // Returns false (nothing launched) when the sizes do not allow it.
-  bool fused_01(const char *in, char *out, char *ws, cudaError_t *err) {
-    const int l0 = p->pass_log[0], l1 = p->pass_log[1];
-    const long long L0 = 1LL << l0, L1 = 1LL << l1;
-    const long long Q = 1LL << (p->logn - l0 - l1);
-    const long long C0 = tile_cols(l0), C1 = tile_cols(l1);
-    long long G = (long long)(l2_group_bytes() / ((size_t)L0 * L1 * elem()));
-    if (G < C0) G = C0;
-    while (G & (G - 1)) G &= G - 1;  // power of two
-    if (C0 <= 0 || C1 <= 0 || Q < C0 || G > Q || Q % G || (G * L0) % C1) return false;
-    for (long long q0 = 0; q0 < Q; q0 += G) {
-      PassArgs a0{p->logn, l0, 0, 1, 1, {q0 / C0, G / C0, Q / C0, L1}};
-      *err = pass(a0, in, ws);
-      if (*err != cudaSuccess) return true;
-      PassArgs a1{p->logn, l1, l0, 1, 1, {q0 * L0 / C1, G * L0 / C1, 0, 1}};
-      *err = pass(a1, ws, out);
-      if (*err != cudaSuccess) return true;
-    }
-    *err = cudaSuccess;
-    return true;
-  }
-
-  cudaError_t run_multi(const char *in, char *out) {
-    const size_t tbytes = (size_t)p->n * elem();
-    const size_t budget = l2_group_bytes();
-    if (budget == 0) return run_passes(in, out, ws, batch, 0);
-    if (tbytes <= budget) {
-      // Whole transforms fit in L2: all passes of one group, then the next.
-      long long g = (long long)(budget / tbytes);
-      if (g < 1) g = 1;
-      for (long long b0 = 0; b0 < batch; b0 += g) {
-        const long long nb = batch - b0 < g ? batch - b0 : g;
-        const size_t off = (size_t)b0 * tbytes;
-        cudaError_t e = run_passes(in + off, out + off, ws + off, nb, 0);
-        if (e != cudaSuccess) return e;
-      }
-      return cudaSuccess;
-    }
-    // Larger than L2: fuse the first two passes through L2 when the result
-    // may not overwrite the input early (out of place) and there is a pass
-    // left to run after them.
-    if (in != out && p->npasses >= 3) {
-      bool fused = true;
-      for (long long b = 0; b < batch && fused; ++b) {
-        const size_t off = (size_t)b * tbytes;
-        cudaError_t e = cudaSuccess;
-        fused = fused_01(in + off, out + off, ws + off, &e);
-        if (e != cudaSuccess) return e;
-      }
-      if (fused) return run_passes(in, out, ws, batch, 2);
-    }
-    return run_passes(in, out, ws, batch, 0);
-  }
+  cudaError_t run_multi(const char *in, char *out) { return run_passes(in, out, ws, batch, 0); }
 
   cudaError_t run(const void *in, void *out) {
     const char *i = static_cast<const char *>(in);

@@ -203,6 +203,22 @@ int fft_device_status(void *stream) {
 
 int fft_last_status(void) { return g_status; }
 
+int fft_debug_set_option(int option, int64_t value) {
+  if (value < 0) return set_option(option, -1) ? FFT_OK : FFT_ERR_INVALID_ARG;
+  bool ok;
+  switch (option) {
+    case FFT_OPT_PASS_LOG: ok = value >= 4 && value <= kPassMaxLogF32; break;
+    case FFT_OPT_PASS_SPLIT: ok = value > 0 && value < (1LL << (4 * kMaxPasses)); break;
+    case FFT_OPT_NO_TMA:
+    case FFT_OPT_NO_CLUSTER:
+    case FFT_OPT_ND_ROWS_T: ok = value <= 1; break;
+    case FFT_OPT_CLUSTER_LOG_MIN: ok = value >= 11 && value <= 13; break;
+    case FFT_OPT_COL_RADIX_LOG: ok = value <= 3; break;
+    default: ok = false;
+  }
+  return ok && set_option(option, value) ? FFT_OK : FFT_ERR_INVALID_ARG;
+}
+
 const char *fft_status_string(int status) {
   switch (status) {
     case FFT_OK: return "ok";

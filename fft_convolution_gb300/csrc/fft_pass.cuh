@@ -73,9 +73,6 @@ template <typename V> struct StoreComplex {
   }
 };
 
-// Which tiles a launch covers.  Block r of a transform takes tile
-// tile_lo + (r mod tile_run) + (r / tile_run) * tile_jump; a launch over all
-// tiles has tile_lo = 0, tile_run = grid_per_batch, tile_jump = 0.
 // Optional two-level table of the inter-pass twiddles W_{L m}^e for this
 // pass's direction: W^e = hi[e >> lo_bits] * lo[e & (2^lo_bits - 1)].
 // Used where sincospi is expensive (fp64); lo == nullptr computes them.
@@ -92,11 +89,8 @@ struct PassGeom {
   int log_n;
   int log_m;
   int twiddle;
-  long long grid_per_batch;  // tiles per transform in this launch
-  long long tile_lo;
-  long long tile_run;
-  long long tile_jump;
-  long long total;  // grid_per_batch * batch: the tiles of the launch
+  long long grid_per_batch;  // tiles per transform
+  long long total;           // grid_per_batch * batch: the tiles of the launch
 };
 
 // Persistent: each block fills the stage-twiddle table once, then walks
@@ -120,9 +114,8 @@ __global__ void __launch_bounds__(PassConfig<T, LOGL>::THREADS, PassConfig<T, LO
   __syncthreads();
 
   for (long long blk = blockIdx.x; blk < g.total; blk += gridDim.x) {
-    const long long r = blk % g.grid_per_batch;
+    const long long tile = blk % g.grid_per_batch;
     const long long b = blk / g.grid_per_batch;
-    const long long tile = g.tile_lo + r % g.tile_run + (r / g.tile_run) * g.tile_jump;
     const long long i = tile * C + c;
     const bool active = i < cols;
 
@@ -197,7 +190,7 @@ template <typename T, int LOGL> long long pass_tiles(int log_n) {
 
 template <typename T, int LOGL, int DIR, class Load, class Store>
 cudaError_t launch_pass_t(Load load, Store store, int log_n, int log_m, int twiddle,
-                          long long batch, cudaStream_t st, const TileSet *subset = nullptr,
+                          long long batch, cudaStream_t st,
                           TwiddleTables<vec2_t<T>> tt = {nullptr, nullptr, 0, 0}) {
   using C = PassConfig<T, LOGL>;
   auto kern = fft_pass_kernel<T, LOGL, DIR, Load, Store>;
@@ -207,14 +200,7 @@ cudaError_t launch_pass_t(Load load, Store store, int log_n, int log_m, int twid
     if (e != cudaSuccess) return e;
   }
   const long long tiles = pass_tiles<T, LOGL>(log_n);
-  PassGeom g{log_n, log_m, twiddle, tiles, 0, tiles, 0, 0};
-  if (subset) {
-    g.grid_per_batch = subset->runs * subset->run;
-    g.tile_lo = subset->lo;
-    g.tile_run = subset->run;
-    g.tile_jump = subset->jump;
-  }
-  g.total = g.grid_per_batch * batch;
+  PassGeom g{log_n, log_m, twiddle, tiles, tiles * batch};
   if (g.total <= 0) return cudaErrorInvalidConfiguration;
   // Persistent grid: as many blocks as fit on the device at once.
   static std::atomic<int> occupancy[64];
@@ -244,17 +230,14 @@ cudaError_t dispatch_pass(const PassArgs &a, const void *in, void *out, cudaStre
     if (a.log_l == LOGL) {
       using V = vec2_t<T>;
       const long long n = 1LL << a.log_n;
-      if (a.subset.runs == 0) {
-        cudaError_t e = launch_pass_cluster_t<T, LOGL, DIR>(in, out, a.log_n, a.log_m,
-                                                            a.twiddle, a.batch, st);
-        if (e != cudaErrorNotSupported) return e;
-        e = launch_pass_tma_t<T, LOGL, DIR>(in, out, a.log_n, a.log_m, a.twiddle, a.batch, st);
-        if (e != cudaErrorNotSupported) return e;
-      }
+      cudaError_t e = launch_pass_cluster_t<T, LOGL, DIR>(in, out, a.log_n, a.log_m, a.twiddle,
+                                                          a.batch, st);
+      if (e != cudaErrorNotSupported) return e;
+      e = launch_pass_tma_t<T, LOGL, DIR>(in, out, a.log_n, a.log_m, a.twiddle, a.batch, st);
+      if (e != cudaErrorNotSupported) return e;
       return launch_pass_t<T, LOGL, DIR>(LoadComplex<V>{static_cast<const V *>(in), n},
                                          StoreComplex<V>{static_cast<V *>(out), n}, a.log_n,
-                                         a.log_m, a.twiddle, a.batch, st,
-                                         a.subset.runs > 0 ? &a.subset : nullptr);
+                                         a.log_m, a.twiddle, a.batch, st);
     }
     return dispatch_pass<T, DIR, MAXLOG, LOGL + 1>(a, in, out, st);
   }

@@ -284,10 +284,7 @@ __global__ void __launch_bounds__(ClusterConfig<T, LOGL>::THREADS,
   if (tid < C * R) bulk_wait_all();
 }
 
-inline bool cluster_disabled() {
-  const char *e = getenv("FFT_GB300_NO_CLUSTER");
-  return e && *e && *e != '0';
-}
+inline bool cluster_disabled() { return option(FFT_OPT_NO_CLUSTER) == 1; }
 
 // Shortest on-chip length (log2) that takes the cluster kernel.  Measured
 // on GB300 (fp32 2D transforms, column pass on clusters vs one block per
@@ -295,20 +292,16 @@ inline bool cluster_disabled() {
 // vs 0.572 ms, 8192^2 1.31 vs 2.29 ms: columns of 4096 and more.  A 2^26
 // transform as two cluster passes of 2^13 (0.85 ms) stays slower than
 // three single-block passes of 2^9 (0.61 ms), so the 1D planner keeps its
-// short passes.  FFT_GB300_CLUSTER_LOG_MIN (11 .. 13) overrides it for tests.
+// short passes.  FFT_OPT_CLUSTER_LOG_MIN (11 .. 13) overrides it for tests.
 inline int cluster_min_log() {
-  const char *e = getenv("FFT_GB300_CLUSTER_LOG_MIN");
-  if (e && *e) {
-    const int v = atoi(e);
-    if (v >= 11 && v <= 13) return v;
-  }
-  return 12;
+  const long long v = option(FFT_OPT_CLUSTER_LOG_MIN);
+  return v >= 11 && v <= 13 ? (int)v : 12;
 }
 
 // Launches the cluster pass kernel, or returns cudaErrorNotSupported
 // (nothing launched) when the shape does not suit it: on-chip length
 // outside cluster_min_log() .. 2^13, fewer columns than one tile, output
-// blocks shorter than a tile, FFT_GB300_NO_CLUSTER set, no driver entry
+// blocks shorter than a tile, FFT_OPT_NO_CLUSTER set, no driver entry
 // point, or no cluster fits the device.
 template <typename T, int LOGL, int DIR>
 cudaError_t launch_pass_cluster_t(const void *in, void *out, int log_n, int log_m, int twiddle,

@@ -10,19 +10,6 @@ cudaError_t launch_pass_f32(int dir, const PassArgs &a, const void *in, void *ou
   return dispatch_pass<float, +1, kPassMaxLogF32>(a, in, out, st);
 }
 
-namespace {
-template <int LOGL = 1> int tile_cols(int log_l) {
-  if constexpr (LOGL > kPassMaxLogF32) {
-    return 0;
-  } else {
-    if (log_l == LOGL) return PassConfig<float, LOGL>::C;
-    return tile_cols<LOGL + 1>(log_l);
-  }
-}
-}  // namespace
-
-int pass_tile_cols_f32(int log_l) { return tile_cols(log_l); }
-
 // Test hook: one in-place pass of on-chip length 2^13 over 2^15 points (one
 // tile, one cluster of 8 blocks) in which block 1's tile load never
 // completes; every wait gives up after `polls` polls.

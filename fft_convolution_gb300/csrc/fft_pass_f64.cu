@@ -10,17 +10,4 @@ cudaError_t launch_pass_f64(int dir, const PassArgs &a, const void *in, void *ou
   return dispatch_pass<double, +1, kPassMaxLogF64>(a, in, out, st);
 }
 
-namespace {
-template <int LOGL = 1> int tile_cols(int log_l) {
-  if constexpr (LOGL > kPassMaxLogF64) {
-    return 0;
-  } else {
-    if (log_l == LOGL) return PassConfig<double, LOGL>::C;
-    return tile_cols<LOGL + 1>(log_l);
-  }
-}
-}  // namespace
-
-int pass_tile_cols_f64(int log_l) { return tile_cols(log_l); }
-
 }  // namespace fftgb

@@ -298,10 +298,7 @@ inline EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-inline bool tma_disabled() {
-  const char *e = getenv("FFT_GB300_NO_TMA");
-  return e && *e && *e != '0';
-}
+inline bool tma_disabled() { return option(FFT_OPT_NO_TMA) == 1; }
 
 // Multiprocessors of the current device (cached per device).
 inline int sm_count() {
@@ -317,7 +314,7 @@ inline int sm_count() {
 // Launches the TMA pass kernel, or returns cudaErrorNotSupported (nothing
 // launched) when the shape does not suit it: tiles narrower than 2 columns
 // (16-byte TMA rows), fewer columns than one tile, output blocks shorter than
-// a tile, FFT_GB300_NO_TMA set, or no driver entry point.
+// a tile, FFT_OPT_NO_TMA set, or no driver entry point.
 template <typename T, int LOGL, int DIR>
 cudaError_t launch_pass_tma_t(const void *in, void *out, int log_n, int log_m, int twiddle,
                               long long batch, cudaStream_t st) {

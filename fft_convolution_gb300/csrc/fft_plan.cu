@@ -85,58 +85,48 @@ int cuda_fail(cudaError_t e) {
   return e == cudaErrorMemoryAllocation ? FFT_ERR_ALLOC : FFT_ERR_CUDA;
 }
 
+// Process-wide test / tuning options (fft_debug_set_option); -1 = the
+// library's own choice.
+static std::atomic<long long> g_options[kNumOptions] = {
+    {-1}, {-1}, {-1}, {-1}, {-1}, {-1}, {-1}, {-1}};
+
+long long option(int which) {
+  return which > 0 && which < kNumOptions ? g_options[which].load(std::memory_order_relaxed) : -1;
+}
+
+bool set_option(int which, long long value) {
+  if (which <= 0 || which >= kNumOptions) return false;
+  g_options[which].store(value < 0 ? -1 : value, std::memory_order_relaxed);
+  return true;
+}
+
 // Largest on-chip factor (log2) per HBM pass of a long 1D transform.  The
 // default 9 keeps every pass tile at 64 KB with 16 (fp32) / 8 (fp64)
-// contiguous columns; FFT_GB300_PASS_LOG overrides it (4 .. 14 fp32,
-// 4 .. 13 fp64) for tuning.
+// contiguous columns (FFT_OPT_PASS_LOG overrides it).
 int pass_log_limit(int dtype) {
-  int lim = 9;
-  const char *env = getenv("FFT_GB300_PASS_LOG");
-  if (env && *env) {
-    int v = atoi(env);
-    if (v >= 4) lim = v;
-  }
+  const long long v = option(FFT_OPT_PASS_LOG);
+  const int lim = v >= 4 ? (int)v : 9;
   const int hard = dtype == FFT_C2C_F32 ? kPassMaxLogF32 : kPassMaxLogF64;
   return lim > hard ? hard : lim;
 }
 
-// FFT_GB300_PASS_SPLIT = "a,b[,c...]" (tuning and tests): the passes of a
-// multi-pass transform of 2^logn points, first pass first, when the factors
-// add up to logn and each is within 1 .. the pass kernels' limit.  Returns
-// the number of passes, or 0 (no override, or one that does not apply).
+// FFT_OPT_PASS_SPLIT: the passes of a multi-pass transform of 2^logn
+// points, first pass first (4 bits each), when the factors add up to logn
+// and each is within 1 .. the pass kernels' limit.  Returns the number of
+// passes, or 0 (no override, or one that does not apply).
 static int pass_split_override(int logn, int dtype, int *split) {
-  const char *env = getenv("FFT_GB300_PASS_SPLIT");
-  if (!env || !*env) return 0;
+  long long v = option(FFT_OPT_PASS_SPLIT);
+  if (v <= 0) return 0;
   const int hard = dtype == FFT_C2C_F32 ? kPassMaxLogF32 : kPassMaxLogF64;
   int count = 0, sum = 0;
-  const char *s = env;
-  while (*s) {
-    char *end = nullptr;
-    const long v = strtol(s, &end, 10);
-    if (end == s || v < 1 || v > hard || count == kMaxPasses) return 0;
-    split[count++] = (int)v;
-    sum += (int)v;
-    s = end;
-    if (*s == ',') ++s;
-    else if (*s) return 0;
+  while (v > 0) {
+    const int f = (int)(v & 15);
+    v >>= 4;
+    if (f < 1 || f > hard || count == kMaxPasses) return 0;
+    split[count++] = f;
+    sum += f;
   }
   return count >= 2 && sum == logn ? count : 0;
-}
-
-// Bytes of data an L2-grouped schedule keeps in flight between two
-// dependent kernels so that the second finds the first's output in L2.
-// Measured on GB300, grouping 2D images (32 MiB) or fusing the first two
-// passes of a 2^26 transform by 32 MiB groups is slower than whole-array
-// passes (more, smaller launches with partial last waves), so grouping is
-// off by default (0) and FFT_GB300_L2_BYTES turns it on for tuning.
-size_t l2_group_bytes() {
-  size_t v = 0;
-  const char *env = getenv("FFT_GB300_L2_BYTES");
-  if (env && *env) {
-    long long x = atoll(env);
-    if (x > 0) v = (size_t)x;
-  }
-  return v;
 }
 
 }  // namespace fftgb
@@ -456,7 +446,7 @@ static fft_plan *plan_any_length(int64_t n, int64_t batch, int direction, int dt
 // (256^2 x 512: 0.163 vs 0.170 ms; 128x256x256 x 4: 0.253 vs 0.264;
 // 256^3 x 2: 0.249 vs 0.264), slower for longer sides (2048^2 x 8: 0.240 vs
 // 0.209; 512^2 x 128: 0.188 vs 0.175; 32x512^2 x 4: 0.306 vs 0.263) and for
-// shorter ones (64^3 x 256: 0.649 vs 0.540).  FFT_GB300_ND_ROWS_T=0 / 1
+// shorter ones (64^3 x 256: 0.649 vs 0.540).  FFT_OPT_ND_ROWS_T = 0 / 1
 // forces the choice (sides 2^4 .. the transposed-store limit) for tuning.
 static int nd_rows_t_wanted(int rank, const int *logs, int dtype) {
   const int lim = dtype == FFT_C2C_F32 ? rows_t_max_log_f32() : rows_t_max_log_f64();
@@ -465,8 +455,8 @@ static int nd_rows_t_wanted(int rank, const int *logs, int dtype) {
     if (logs[k] < 4 || logs[k] > lim) ok = 0;
     if (logs[k] < 7 || logs[k] > 8) preferred = 0;
   }
-  const char *env = getenv("FFT_GB300_ND_ROWS_T");
-  if (env && *env) return ok && atoi(env) != 0;
+  const long long forced = option(FFT_OPT_ND_ROWS_T);
+  if (forced >= 0) return ok && forced != 0;
   return ok && preferred;
 }
 
@@ -591,7 +581,7 @@ fft_plan *fft_plan_create(int64_t n, int64_t batch, int dims, int direction, int
   }
   // Stockham passes over HBM: logn split into nearly equal factors of at
   // most pass_log_limit bits, larger factors first (or the split
-  // FFT_GB300_PASS_SPLIT names).
+  // FFT_OPT_PASS_SPLIT names).
   int split[kMaxPasses];
   int P = pass_split_override(logn, dtype, split);
   if (P == 0) {
@@ -679,6 +669,24 @@ fft_plan *fft_plan_create_nd(int rank, const int64_t *shape, int64_t batch, int 
   p->batch = batch;
   p->direction = direction;
   p->dtype = dtype;
+  // Columns of 1024 or 2048 points: fold the first radix-R stage (R = 2, 4)
+  // of the column transform into the row pass so that the column pass
+  // transforms 512-point columns of R times wider rows (out-of-place
+  // execution only), where the row pass keeps blocks of at most 512
+  // threads.  Measured on GB300 (fp32, forward + inverse, ms): 1024^2 x 32
+  // 0.404 unfolded, 0.366 R = 2, 0.382 R = 4; 2048^2 x 8 0.427 unfolded,
+  // 0.441 R = 2, 0.420 R = 4, 0.503 R = 8 (and 0.444 with R = 4 split over
+  // a cluster of two 256-thread blocks); 4096^2 x 2 keeps its cluster column
+  // pass (0.530 unfolded, 0.531 R = 8).
+  if (!p->nd_rows_t) {
+    const int logh = logs[rank - 2], logw = logs[rank - 1];
+    const long long forced = option(FFT_OPT_COL_RADIX_LOG);
+    int logr = 0;
+    if (forced >= 0) logr = (int)forced;
+    else if ((logh == 10 || logh == 11) && logw >= 4 && (logh - 9) + logw - 4 <= 9) logr = logh - 9;
+    if (logr >= 1 && logr < logh && rows_col_supported(dtype == FFT_C2C_F64, logw, logr))
+      p->col_radix_log = logr;
+  }
   if (p->nd_rows_t) {
     p->ws_stride = (size_t)p->elems * (dtype == FFT_C2C_F32 ? 8 : 16);
     p->workspace_bytes = (size_t)batch * p->ws_stride;

@@ -9,6 +9,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "fft_gb300.h"
+
 namespace fftgb {
 
 // Largest transform one thread block holds on chip: 2^14 complex fp32 or
@@ -29,6 +31,13 @@ unsigned long long context_id();
 struct DeviceOnce {
   std::atomic<unsigned long long> ctx[64];
 };
+
+// Process-wide test / tuning options of fft_debug_set_option (FFT_OPT_*
+// in the public header; fft_plan.cu): the current value, -1 for the
+// library's own choice.
+constexpr int kNumOptions = 8;
+long long option(int which);
+bool set_option(int which, long long value);
 
 // Sets a kernel's dynamic shared-memory limit once per device and context
 // (the attribute belongs to the context).  `done` is the calling launcher's
@@ -64,14 +73,21 @@ cudaError_t launch_rows_f32(int logn, int dir, const void *in, void *out, long l
 cudaError_t launch_rows_f64(int logn, int dir, const void *in, void *out, long long batch,
                             cudaStream_t st);
 
-// A subset of a pass's tiles: `runs` runs of `run` consecutive tiles, run k
-// starting at tile lo + k * jump.  runs = 0 means every tile.
-struct TileSet {
-  long long lo;
-  long long run;
-  long long jump;
-  long long runs;
-};
+// Row pass of 2D / 3D transforms with the first radix-2^logr stage of the
+// column transform folded in (rows_col_*.cu): `planes` H x W planes
+// (H = 2^log_h, W = 2^logw), out of place; the column pass that follows
+// runs with on-chip length H / 2^logr over columns at stride 2^logr W.
+// cudaErrorInvalidValue outside rows_col_supported().
+cudaError_t launch_rows_col_f32(int logw, int logr, int dir, const void *in, void *out, int log_h,
+                                long long planes, cudaStream_t st);
+cudaError_t launch_rows_col_f64(int logw, int logr, int dir, const void *in, void *out, int log_h,
+                                long long planes, cudaStream_t st);
+inline bool rows_col_supported(bool f64, int logw, int logr) {
+  if (logw < 8 || logw > (f64 ? 11 : 12) || logr < 1 || logr > 3) return false;
+  if ((1 << (logw + logr - 4)) > 1024) return false;  // threads per block
+  const long long smem = (1LL << logr) * (((1LL << logw) * 17) / 16) * (f64 ? 16 : 8);
+  return logr < 3 || smem <= 200 * 1024;
+}
 
 // One pass of a transform that does not fit on chip, or the column pass of
 // a 2D transform (fft_pass_*.cu).  The data of each of `batch` transforms is
@@ -79,20 +95,14 @@ struct TileSet {
 // length 2^log_l, each over the elements i + u * 2^(log_n - log_l),
 // u < 2^log_l, and is the radix-2^log_l Stockham stage whose previous block
 // length is 2^log_m.  With twiddle != 0 input u of butterfly i is first
-// multiplied by W_{2^(log_l+log_m)}^{(i mod 2^log_m) u}.  `subset` limits
-// the launch to some of the pass's tiles.
+// multiplied by W_{2^(log_l+log_m)}^{(i mod 2^log_m) u}.
 struct PassArgs {
   int log_n;
   int log_l;
   int log_m;
   int twiddle;
   long long batch;
-  TileSet subset;
 };
-// Columns (consecutive butterflies) one block of the pass kernel takes for an
-// on-chip length 2^log_l (fft_pass_*.cu).
-int pass_tile_cols_f32(int log_l);
-int pass_tile_cols_f64(int log_l);
 cudaError_t launch_pass_f32(int dir, const PassArgs &a, const void *in, void *out,
                             cudaStream_t st);
 cudaError_t launch_pass_f64(int dir, const PassArgs &a, const void *in, void *out,

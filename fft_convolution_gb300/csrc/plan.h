@@ -55,9 +55,8 @@ int cuda_fail(cudaError_t e);
 
 inline bool misaligned(const void *p) { return ((uintptr_t)p & 15u) != 0; }
 
-// Tuning limits (environment overrides; fft_plan.cu).
+// Largest on-chip factor (log2) per HBM pass of a long 1D plan (fft_plan.cu).
 int pass_log_limit(int dtype);
-size_t l2_group_bytes();
 
 inline cudaError_t launch_rows(int dtype, int logn, int dir, const void *in, void *out,
                                long long batch, cudaStream_t st) {
@@ -113,6 +112,9 @@ struct fft_plan {
   int axis_pass[3];
   // KIND_ND with every axis as on-chip rows stored transposed (nd_rows_t).
   int nd_rows_t;
+  // KIND_ND, out of place: log2 of the radix of the column transform's first
+  // stage folded into the row pass (0: rows, then a full column pass).
+  int col_radix_log;
 };
 
 namespace fftgb {

@@ -110,7 +110,7 @@ cudaError_t poly_pass(int log_l, Load load, Store store, int log_n, int log_m, l
   } else {
     if (log_l == LOGL)
       return launch_pass_t<double, LOGL, DIR>(load, store, log_n, log_m, /*twiddle=*/1, batch,
-                                              st, nullptr, tt);
+                                              st, tt);
     return poly_pass<DIR, Load, Store, LOGL + 1>(log_l, load, store, log_n, log_m, batch, st,
                                                  tt);
   }

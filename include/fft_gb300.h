@@ -393,10 +393,41 @@ int fft_debug_wait_timeout(int64_t polls, void *stream);
  * (1 .. 2^22).  That block's wait runs out; the whole cluster sees its
  * flag, leaves together, and the device status word reads
  * FFT_ERR_DEVICE_TIMEOUT (fft_device_status).  Returns FFT_ERR_UNSUPPORTED
- * when the cluster kernel is switched off (FFT_GB300_NO_CLUSTER).  Faults
+ * when the cluster kernel is switched off (FFT_OPT_NO_CLUSTER).  Faults
  * nothing.  No counterpart on the source pages.
  */
 int fft_debug_cluster_timeout(void *data, int64_t polls, void *stream);
+
+/*
+ * fft_debug_set_option -- test and tuning hook (not part of the transform
+ * API; no transform needs it): sets one process-wide choice that the
+ * planner and the pass launchers otherwise make themselves, so that tests
+ * can run every schedule on small shapes and kernels can be compared.  A
+ * plan reads the planning options when it is created; the launch options
+ * apply to every later launch.  `value` < 0 restores the library's own
+ * choice.  Nothing in the library reads the process environment.  Returns
+ * FFT_OK, or FFT_ERR_INVALID_ARG for an unknown option or a value out of
+ * its range (the option is then unchanged).  Not thread-safe with respect
+ * to plans being created or launched at the same time.
+ */
+#define FFT_OPT_PASS_LOG 1        /* planning: largest on-chip factor (log2, 4 .. 14 fp32,
+                                     4 .. 13 fp64) per HBM pass of a long 1D transform;
+                                     own choice 9 */
+#define FFT_OPT_PASS_SPLIT 2      /* planning: the passes of a long 1D transform, one factor
+                                     (log2, 1 .. 14) per 4 bits, first pass in the lowest;
+                                     used when they add up to log2 N */
+#define FFT_OPT_NO_TMA 3          /* launch: 1 = every pass by the plain-load kernel */
+#define FFT_OPT_NO_CLUSTER 4      /* launch: 1 = no thread-block-cluster passes */
+#define FFT_OPT_CLUSTER_LOG_MIN 5 /* launch: shortest on-chip length (log2, 11 .. 13) that
+                                     takes the cluster pass; own choice 12 */
+#define FFT_OPT_ND_ROWS_T 6       /* planning: 2D / 3D of power-of-two sides as rows with
+                                     transposed stores (1) or rows + column passes (0);
+                                     own choice by shape */
+#define FFT_OPT_COL_RADIX_LOG 7   /* planning: 2D / 3D, out of place: log2 of the radix of the
+                                     column transform's first stage folded into the row pass
+                                     (0 = none, 1 .. 3); own choice log2(H / 512) for columns
+                                     of 1024 .. 4096 points */
+int fft_debug_set_option(int option, int64_t value);
 
 /* Last status recorded on this host thread by a call that returns a
  * pointer (fft_plan_create). */

@@ -34,3 +34,21 @@ def fg_lib():
     build_library()
     import fft_convolution_gb300
     return fft_convolution_gb300
+
+
+@pytest.fixture
+def opt(fg_lib):
+    """Forces library choices through the test hook fft_debug_set_option for
+    one test: opt("PASS_SPLIT", "12,10"), opt("NO_CLUSTER", 1), ...; the
+    library's own choices are restored afterwards."""
+    used = []
+
+    def set_option(name, value):
+        code = getattr(fg_lib, "FFT_OPT_" + name)
+        if name == "PASS_SPLIT" and isinstance(value, str):
+            value = fg_lib.pass_split_value(int(v) for v in value.split(","))
+        assert fg_lib.fft_debug_set_option(code, int(value)) == fg_lib.FFT_OK, (name, value)
+        used.append(code)
+    yield set_option
+    for code in used:
+        fg_lib.fft_debug_set_option(code, -1)

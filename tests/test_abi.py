@@ -97,13 +97,31 @@ def test_on_chip_plans_need_no_device(fg, n, dims, dtype, kernels):
     fg.fft_plan_destroy(h)
 
 
-def test_2d_l2_grouping_kernel_count(fg, monkeypatch):
-    # With an L2 budget of one 32 MiB image, 3 images run as 3 groups of
-    # (row kernel, column pass).
-    monkeypatch.setenv("FFT_GB300_L2_BYTES", str(32 << 20))
-    h = fg._lib.fft_plan_create(2048, 3, 2, -1, 0)
-    assert fg.fft_plan_num_kernels(h) == 6
-    fg.fft_plan_destroy(h)
+def test_debug_set_option_checks(fg):
+    # The test / tuning hook validates its arguments and restores defaults
+    # with a negative value.
+    assert fg.fft_debug_set_option(99, 1) == fg.FFT_ERR_INVALID_ARG
+    assert fg.fft_debug_set_option(0, 1) == fg.FFT_ERR_INVALID_ARG
+    assert fg.fft_debug_set_option(fg.FFT_OPT_PASS_LOG, 3) == fg.FFT_ERR_INVALID_ARG
+    assert fg.fft_debug_set_option(fg.FFT_OPT_CLUSTER_LOG_MIN, 10) == fg.FFT_ERR_INVALID_ARG
+    assert fg.fft_debug_set_option(fg.FFT_OPT_COL_RADIX_LOG, 4) == fg.FFT_ERR_INVALID_ARG
+    assert fg.fft_debug_set_option(fg.FFT_OPT_NO_TMA, 2) == fg.FFT_ERR_INVALID_ARG
+    for code in range(1, 8):
+        assert fg.fft_debug_set_option(code, -1) == fg.FFT_OK
+    assert fg.pass_split_value([9, 9, 8]) == 9 | 9 << 4 | 8 << 8
+
+
+def test_2d_folded_column_radix_keeps_two_kernels(fg, opt):
+    # 2048 x 2048: rows (with the column transform's first radix-4 stage)
+    # and one column pass, with or without the fold; no workspace either way.
+    for logr in (-1, 0, 1, 2, 3):
+        if logr >= 0:
+            opt("COL_RADIX_LOG", logr)
+        h = fg._lib.fft_plan_create(2048, 3, 2, -1, 0)
+        assert h
+        assert fg.fft_plan_num_kernels(h) == 2
+        assert fg.fft_plan_workspace_bytes(h) == 0
+        fg.fft_plan_destroy(h)
 
 
 def test_exec_argument_checks(fg):

@@ -77,7 +77,7 @@ def test_c2c_guards(fg, n, batch, dtype, direction):
 
 @pytest.mark.parametrize("shape,batch", [((64, 64), 3), ((16, 32), 5), ((4, 16, 32), 2),
                                          ((2, 1, 256), 3), ((30, 50), 3), ((3, 5, 7), 2),
-                                         ((1 << 15, 4), 1)])
+                                         ((1 << 15, 4), 1), ((2048, 256), 2), ((2, 1024, 256), 1)])
 def test_nd_guards(fg, shape, batch):
     x = workloads.normal_complex((batch,) + shape, 9100, np.complex64)
     for direction in (-1, 1):

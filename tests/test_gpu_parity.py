@@ -114,41 +114,21 @@ def test_multipass_forward_inverse(fg, dtype, logn):
 
 
 @pytest.mark.parametrize("passlog", [5, 7, 9, 13])
-def test_multipass_factorisations(fg, monkeypatch, passlog):
+def test_multipass_factorisations(fg, opt, passlog):
     # The same 2^18 transform split into 2, 3 or 4 passes.
-    monkeypatch.setenv("FFT_GB300_PASS_LOG", str(passlog))
+    opt("PASS_LOG", passlog)
     n = 1 << 18
     x = workloads.uniform_complex((1, n), 31, np.complex64)
     y = run_plan(fg, x, n, 1, 1, fg.FFT_FORWARD, F32)
     assert rel_rows(y, oracle.fft(x.astype(np.complex128))).max() <= tol(F32, n)
 
 
-@pytest.mark.parametrize("dtype,logn,budget", [
-    (F32, 22, 1 << 20),   # passes 8,7,7: four L2 groups of the fused first two passes
-    (F32, 20, 1 << 19),   # passes 7,7,6: one group
-    (F64, 20, 1 << 20),   # passes 7,7,6 fp64: two groups
-])
-def test_multipass_fused_l2_groups(fg, monkeypatch, dtype, logn, budget):
-    # A transform larger than the L2 budget runs its first two passes group
-    # by group through L2 (out of place), or all passes in turn (in place).
-    monkeypatch.setenv("FFT_GB300_L2_BYTES", str(budget))
-    n = 1 << logn
-    x = workloads.normal_complex((1, n), 4000 + logn, NP[dtype])
-    ref = oracle.fft(x.astype(np.complex128))
-    y = run_plan(fg, x, n, 1, 1, fg.FFT_FORWARD, dtype)
-    assert rel_rows(y, ref).max() <= tol(dtype, n)
-    y2 = run_plan(fg, x, n, 1, 1, fg.FFT_FORWARD, dtype, inplace=True)
-    assert rel_rows(y2, ref).max() <= tol(dtype, n)
-    z = run_plan(fg, y, n, 1, 1, fg.FFT_INVERSE, dtype)
-    assert rel_rows(z, x.astype(np.complex128)).max() <= 2 * tol(dtype, n)
-
-
 @pytest.mark.parametrize("dims,dtype,logn", [(1, F32, 18), (1, F32, 22), (1, F64, 17),
                                               (2, F32, 11), (2, F64, 9)])
-def test_lsu_pass_kernel(fg, monkeypatch, dims, dtype, logn):
+def test_lsu_pass_kernel(fg, opt, dims, dtype, logn):
     # The pass kernel with plain loads/stores (what runs when the TMA path
     # does not apply) on shapes that normally take the TMA path.
-    monkeypatch.setenv("FFT_GB300_NO_TMA", "1")
+    opt("NO_TMA", 1)
     n = 1 << logn
     shape = (1, n) if dims == 1 else (1, n, n)
     x = workloads.normal_complex(shape, 5000 + logn, NP[dtype])
@@ -171,9 +151,9 @@ def test_lsu_pass_kernel(fg, monkeypatch, dims, dtype, logn):
     (F64, 21, "11,10", 1),
     (F64, 20, "8,12", 2),
 ])
-def test_cluster_passes(fg, monkeypatch, dtype, logn, split, batch):
-    monkeypatch.setenv("FFT_GB300_PASS_SPLIT", split)
-    monkeypatch.setenv("FFT_GB300_CLUSTER_LOG_MIN", "11")  # clusters of 2 as well
+def test_cluster_passes(fg, opt, dtype, logn, split, batch):
+    opt("PASS_SPLIT", split)
+    opt("CLUSTER_LOG_MIN", 11)  # clusters of 2 as well
     n = 1 << logn
     x = workloads.normal_complex((batch, n), 6000 + logn, NP[dtype])
     ref = oracle.fft(x.astype(np.complex128))
@@ -187,12 +167,12 @@ def test_cluster_passes(fg, monkeypatch, dtype, logn, split, batch):
 
 
 @pytest.mark.parametrize("split", ["13,11", "11,13", "12,12", "8,8,8"])
-def test_cluster_pass_splits_2e24(fg, monkeypatch, split):
+def test_cluster_pass_splits_2e24(fg, opt, split):
     # One 2^24 transform split into cluster passes of 2^11 .. 2^13 points
     # (and, for comparison, into single-block passes), against the oracle at
     # every bin, forward and inverse.
-    monkeypatch.setenv("FFT_GB300_PASS_SPLIT", split)
-    monkeypatch.setenv("FFT_GB300_CLUSTER_LOG_MIN", "11")
+    opt("PASS_SPLIT", split)
+    opt("CLUSTER_LOG_MIN", 11)
     n = 1 << 24
     x = workloads.normal_complex((1, n), 6100, np.complex64)
     y = run_plan(fg, x, n, 1, 1, fg.FFT_FORWARD, F32)
@@ -201,10 +181,10 @@ def test_cluster_pass_splits_2e24(fg, monkeypatch, split):
     assert rel_rows(z, x.astype(np.complex128)).max() <= 2 * tol(F32, n)
 
 
-def test_cluster_pass_disabled_fallback(fg, monkeypatch):
-    # FFT_GB300_NO_CLUSTER: the same split runs on the single-block kernels.
-    monkeypatch.setenv("FFT_GB300_PASS_SPLIT", "12,10")
-    monkeypatch.setenv("FFT_GB300_NO_CLUSTER", "1")
+def test_cluster_pass_disabled_fallback(fg, opt):
+    # FFT_OPT_NO_CLUSTER: the same split runs on the single-block kernels.
+    opt("PASS_SPLIT", "12,10")
+    opt("NO_CLUSTER", 1)
     n = 1 << 22
     x = workloads.uniform_complex((1, n), 6200, np.complex64)
     y = run_plan(fg, x, n, 1, 1, fg.FFT_FORWARD, F32)
@@ -214,25 +194,6 @@ def test_cluster_pass_disabled_fallback(fg, monkeypatch):
 def test_device_status_clear_after_transforms(fg):
     # No bounded in-kernel wait ran out during the transforms above.
     assert fg.fft_device_status(stream()) == 0
-
-
-def test_multipass_batch_groups(fg, monkeypatch):
-    # Transforms that fit the L2 budget run all their passes group by group.
-    monkeypatch.setenv("FFT_GB300_L2_BYTES", str(2 * (1 << 16) * 8))
-    n, batch = 1 << 16, 5
-    x = workloads.uniform_complex((batch, n), 77, np.complex64)
-    y = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, F32)
-    assert rel_rows(y, oracle.fft(x.astype(np.complex128))).max() <= tol(F32, n)
-
-
-def test_2d_l2_groups(fg, monkeypatch):
-    monkeypatch.setenv("FFT_GB300_L2_BYTES", str(256 * 256 * 8))  # one image per group
-    n, batch = 256, 5
-    x = workloads.normal_complex((batch, n, n), 78, np.complex64)
-    y = run_plan(fg, x, n, batch, 2, fg.FFT_FORWARD, F32)
-    assert rel_rows(y, oracle.fft2d(x.astype(np.complex128))).max() <= tol(F32, n * n)
-    y2 = run_plan(fg, x, n, batch, 2, fg.FFT_FORWARD, F32, inplace=True)
-    assert rel_rows(y2, oracle.fft2d(x.astype(np.complex128))).max() <= tol(F32, n * n)
 
 
 # --- 2D -----------------------------------------------------------------------
@@ -283,12 +244,42 @@ def test_nd_forward_inverse(fg, dtype, shape):
     pi.close()
 
 
+# Columns of 1024 points or more, out of place: the row pass also takes the
+# first radix-R stage of the column transform (R = H / 512) and the column
+# pass transforms 512-point columns R W apart.  In place the plan keeps rows
+# plus a full column pass; both schedules are checked against the oracle.
+@pytest.mark.parametrize("dtype,shape,batch", [
+    (F32, (1024, 256), 3), (F32, (2048, 256), 2), (F64, (2048, 256), 2), (F32, (4096, 256), 1),
+    (F64, (4096, 256), 1), (F32, (2048, 2048), 2), (F32, (4096, 1024), 1), (F32, (1024, 4096), 1),
+    (F64, (1024, 2048), 1), (F32, (2, 1024, 256), 2), (F64, (4, 2048, 512), 1)])
+def test_nd_folded_column_radix(fg, dtype, shape, batch):
+    x = workloads.normal_complex((batch,) + shape, 3600 + sum(shape), NP[dtype])
+    npts = int(np.prod(shape))
+    p = fg.Plan(0, batch, direction=fg.FFT_FORWARD, dtype=dtype, shape=shape)
+    pi = fg.Plan(0, batch, direction=fg.FFT_INVERSE, dtype=dtype, shape=shape)
+    assert p.num_kernels == len(shape)
+    xd = torch.from_numpy(x).cuda()
+    yd, zd = torch.empty_like(xd), torch.empty_like(xd)
+    p.exec(xd, yd)
+    pi.exec(yd, zd)
+    torch.cuda.synchronize()
+    ref = oracle.fftn(x.astype(np.complex128), len(shape))
+    assert rel_rows(yd.cpu().numpy(), ref).max() <= tol(dtype, npts)
+    assert rel_rows(zd.cpu().numpy(), x).max() <= 2 * tol(dtype, npts)
+    assert np.array_equal(xd.cpu().numpy(), x)          # input untouched
+    p.exec(xd, xd)                                      # in place: rows + column pass
+    torch.cuda.synchronize()
+    assert rel_rows(xd.cpu().numpy(), ref).max() <= tol(dtype, npts)
+    p.close()
+    pi.close()
+
+
 @pytest.mark.parametrize("dtype", [F32, F64])
 @pytest.mark.parametrize("shape", [(8192, 2), (2048, 4), (4096, 8)])
-def test_nd_columns_single_block(fg, monkeypatch, dtype, shape):
-    # Long columns on the single-block pass kernels (FFT_GB300_NO_CLUSTER);
+def test_nd_columns_single_block(fg, opt, dtype, shape):
+    # Long columns on the single-block pass kernels (FFT_OPT_NO_CLUSTER);
     # fp64 columns of 8192 compute their stage twiddles (no shared table).
-    monkeypatch.setenv("FFT_GB300_NO_CLUSTER", "1")
+    opt("NO_CLUSTER", 1)
     x = workloads.normal_complex((2,) + shape, 3550 + sum(shape), NP[dtype])
     p = fg.Plan(0, 2, direction=fg.FFT_FORWARD, dtype=dtype, shape=shape)
     y = p.exec(torch.from_numpy(x).cuda())
@@ -308,16 +299,16 @@ def test_nd_large_3d(fg):
 
 
 # Every axis as on-chip rows with transposed stores: the default when every
-# side is 128 or 256, forced here (FFT_GB300_ND_ROWS_T=1) on other sides
+# side is 128 or 256, forced here (FFT_OPT_ND_ROWS_T = 1) on other sides
 # too; out of place and in place (rank 3 in place ends with a copy).
 @pytest.mark.parametrize("dtype,shape,force", [
     (F32, (128, 256), False), (F32, (256, 256), False), (F32, (128, 128, 256), False),
     (F32, (64, 32), True), (F32, (16, 1024), True), (F32, (4096, 16), True),
     (F32, (32, 16, 64), True), (F64, (256, 128), False), (F64, (64, 4096), True), (F64, (64, 8192), True),
     (F64, (16, 32, 64), True)])
-def test_nd_rows_transposed(fg, monkeypatch, dtype, shape, force):
+def test_nd_rows_transposed(fg, opt, dtype, shape, force):
     if force:
-        monkeypatch.setenv("FFT_GB300_ND_ROWS_T", "1")
+        opt("ND_ROWS_T", 1)
     batch = 3
     x = workloads.normal_complex((batch,) + shape, 3700 + sum(shape), NP[dtype])
     p = fg.Plan(0, batch, direction=fg.FFT_FORWARD, dtype=dtype, shape=shape)

@@ -66,20 +66,11 @@ def test_reference_arm_under_torchrun_prints_once():
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
 
 
-def test_planned_passes_follow_the_planner(monkeypatch):
-    # The HBM pass count bench.py reports mirrors the planner: factors of at
-    # most 9 bits by default, or the FFT_GB300_PASS_SPLIT / _PASS_LOG
-    # overrides when they apply.
+def test_planned_passes_follow_the_planner():
+    # The HBM pass count bench.py assumes before a plan exists mirrors the
+    # planner's own rule: factors of at most 9 bits, at least two passes.
     import bench
-    monkeypatch.delenv("FFT_GB300_PASS_SPLIT", raising=False)
-    monkeypatch.delenv("FFT_GB300_PASS_LOG", raising=False)
     assert bench.planned_passes(26, 9) == 3
     assert bench.planned_passes(15, 9) == 2
     assert bench.planned_passes(30, 9) == 4
-    monkeypatch.setenv("FFT_GB300_PASS_SPLIT", "13,13")
-    assert bench.planned_passes(26, 9) == 2
-    monkeypatch.setenv("FFT_GB300_PASS_SPLIT", "13,12")      # does not add up to 26: ignored
-    assert bench.planned_passes(26, 9) == 3
-    monkeypatch.delenv("FFT_GB300_PASS_SPLIT")
-    monkeypatch.setenv("FFT_GB300_PASS_LOG", "13")
-    assert bench.planned_passes(26, 9) == 2
+    assert bench.planned_passes(18, 13) == 2
