@@ -254,6 +254,7 @@ KERNEL_SOURCES = {
     "any3": ["fft_device.cuh", "mixed.cuh", "mixed_f32.cu", "transpose.cu", "fft_plan.cu", "fft_exec.cu", "plan.h"],
     "real1": ["fft_device.cuh", "fft_rows.cuh", "real.cuh", "real_f32.cu"],
     "nd1": ["fft_device.cuh", "fft_rows.cuh", "fft_rows_t.cuh", "rows_t_f32.cu", "fft_plan.cu", "fft_exec.cu", "plan.h"],
+    "rows512": ["fft_device.cuh", "fft_rows.cuh", "fft_warp.cuh", "fft_rows_f32.cu"],
 }
 
 
@@ -825,6 +826,11 @@ def run_gpu(args):
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
+    for item in args.option:
+        name, _, value = item.partition("=")
+        code = getattr(fg, "FFT_OPT_" + name.strip().upper())
+        rc = fg.fft_debug_set_option(code, int(value))
+        assert rc == 0, f"option {item}: {fg.fft_status_string(rc)}"
 
     def barrier():
         if world > 1:
@@ -871,10 +877,16 @@ EXTRA_CONFIGS = ("c1", "c3", "c4", "c5")
 L2_BYTES = 129e6
 
 
+OPTIONS = []  # --option NAME=VALUE items of this run
+
+
 def config_dict(name: str, info: dict, world: int) -> dict:
-    return {"workload": workload_label(name), "l2": "inputs larger than L2, no flush"
-            if info["array_bytes"] > L2_BYTES else "L2 flushed (256 MiB written) before every "
-            "timed step", "hbm_passes": info["passes"], "parallelism": f"replicas x{world}"}
+    d = {"workload": workload_label(name), "l2": "inputs larger than L2, no flush"
+         if info["array_bytes"] > L2_BYTES else "L2 flushed (256 MiB written) before every "
+         "timed step", "hbm_passes": info["passes"], "parallelism": f"replicas x{world}"}
+    if OPTIONS:
+        d["library_options"] = list(OPTIONS)
+    return d
 
 
 def sized_input(name: str, c: dict):
@@ -928,6 +940,8 @@ def workload_label(name: str) -> str:
         return "1D C2C forward+inverse, N=3001 prime (Bluestein, M=8192 on chip), batch 16384, fp32"
     if name == "nd1":
         return "3D C2C forward+inverse, 128x256x256, batch 4, fp32 (256 MiB)"
+    if name == "rows512":
+        return "1D C2C forward+inverse, N=512, batch 131072, fp32 (512 MiB)"
     return f"polymul, {c['batch']} pairs of 2^20 int64 coefficients, fp64 transforms of 2^21"
 
 
@@ -1011,11 +1025,15 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=3.0)
     ap.add_argument("--clock-soak", type=float, default=0.6,
                     help="seconds of untimed load sampled for clocks before the timed region")
+    ap.add_argument("--option", action="append", default=[], metavar="NAME=VALUE",
+                    help="force a library choice through its test hook before planning, e.g. "
+                         "ROWS_SHFL=1 or COL_RADIX_LOG=0 (kernel comparisons; recorded in config)")
     ap.add_argument("--n", type=int, default=None,
                     help="override the transform length (small profiling cases)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the batch (small profiling cases)")
     args = ap.parse_args()
+    OPTIONS.extend(args.option)
     if args.n is not None:
         SIZE_OVERRIDE["n"] = args.n
     if args.batch is not None:

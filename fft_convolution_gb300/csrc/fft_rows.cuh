@@ -11,6 +11,7 @@
 #pragma once
 
 #include "fft_device.cuh"
+#include "fft_warp.cuh"
 #include "internal.h"
 
 namespace fftgb {
@@ -96,13 +97,63 @@ cudaError_t launch_rows_t(const void *in, void *out, long long batch, cudaStream
                             static_cast<vec2_t<T> *>(out), batch);
 }
 
+// 512-point transforms with the warp-shuffle exchange of fft_warp.cuh: one
+// warp per transform, 8 per block, no shared memory (selected by
+// FFT_OPT_ROWS_SHFL; the shared-memory engine above is the default).
+template <typename T, int DIR>
+__global__ void __launch_bounds__(256) fft_rows_warp_kernel(const vec2_t<T> *in, vec2_t<T> *out,
+                                                           long long batch) {
+  using V = vec2_t<T>;
+  const int lane = threadIdx.x & 31;
+  const long long tr = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (tr >= batch) return;  // whole warps leave together
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  V x[16];
+  const V *src = in + tr * 512;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) x[r] = src[lane + 32 * r];
+  asm volatile("griddepcontrol.launch_dependents;");
+  fft512_warp<DIR>(x, lane);
+  V *dst = out + tr * 512 + (lane >> 1) + 256 * (lane & 1);
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    V v = x[c];
+    if constexpr (DIR > 0) v = c_scale(v, (T)(1.0 / 512));
+    dst[16 * c] = v;
+  }
+}
+
+template <typename T, int DIR>
+cudaError_t launch_rows_warp_t(const void *in, void *out, long long batch, cudaStream_t st) {
+  const long long grid = (batch + 7) / 8;
+  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fft_rows_warp_kernel<T, DIR>,
+                            static_cast<const vec2_t<T> *>(in), static_cast<vec2_t<T> *>(out),
+                            batch);
+}
+
 template <typename T, int DIR, int LOGN = 0>
 cudaError_t dispatch_rows(int logn, const void *in, void *out, long long batch,
                           cudaStream_t st) {
   if constexpr (LOGN > RowsMaxLog<T>::value) {
     return cudaErrorInvalidValue;
   } else {
-    if (logn == LOGN) return launch_rows_t<T, LOGN, DIR>(in, out, batch, st);
+    if (logn == LOGN) {
+      if constexpr (LOGN == 9) {
+        if (option(FFT_OPT_ROWS_SHFL) == 1) return launch_rows_warp_t<T, DIR>(in, out, batch, st);
+      }
+      return launch_rows_t<T, LOGN, DIR>(in, out, batch, st);
+    }
     return dispatch_rows<T, DIR, LOGN + 1>(logn, in, out, batch, st);
   }
 }

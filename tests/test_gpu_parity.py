@@ -138,6 +138,22 @@ def test_lsu_pass_kernel(fg, opt, dims, dtype, logn):
     assert rel_rows(y, ref).max() <= tol(dtype, npts)
 
 
+# 512-point transforms with the warp-shuffle exchange (FFT_OPT_ROWS_SHFL): one
+# warp per transform, four register/lane bit swaps by __shfl_xor_sync and a
+# final 2-point butterfly across lane pairs; ragged batches against the
+# oracle, forward and inverse, in place and out of place.
+@pytest.mark.parametrize("dtype", [F32, F64])
+@pytest.mark.parametrize("batch", [1, 7, 8, 61])
+def test_rows_warp_shuffle_512(fg, opt, dtype, batch):
+    opt("ROWS_SHFL", 1)
+    n = 512
+    x = workloads.normal_complex((batch, n), 3900 + batch, NP[dtype])
+    y = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, dtype)
+    assert rel_rows(y, oracle.fft(x.astype(np.complex128))).max() <= tol(dtype, n)
+    z = run_plan(fg, y, n, batch, 1, fg.FFT_INVERSE, dtype, inplace=True)
+    assert rel_rows(z, oracle.ifft(y.astype(np.complex128))).max() <= tol(dtype, n)
+
+
 # --- passes whose on-chip length (2^11 .. 2^13) is split over a cluster --------
 
 @pytest.mark.parametrize("dtype,logn,split,batch", [

@@ -31,6 +31,10 @@ Workloads (sizes and distributions):
   normal; 3D forward then inverse.
 * ``real1``: 32768 real fp32 rows of 8192 samples (1 GiB), standard normal;
   half spectrum (R2C) then back (C2R).
+* ``rows512``: 131072 transforms of 512 points (512 MiB fp32 complex), re and
+  im i.i.d. standard normal; forward then inverse (the shape on which the
+  shared-memory and warp-shuffle exchanges of the on-chip engine are
+  compared).
 """
 from __future__ import annotations
 
@@ -48,6 +52,7 @@ CONFIGS = {
     "any3": dict(kind="fft1d", n=100000, batch=1024, dtype="f32", seed=11),
     "nd1": dict(kind="fftnd", n=256, shape=(128, 256, 256), batch=4, dtype="f32", seed=8),
     "real1": dict(kind="real", n=8192, batch=32768, dtype="f32", seed=9),
+    "rows512": dict(kind="fft1d", n=512, batch=131072, dtype="f32", seed=12),
 }
 
 
@@ -161,7 +166,7 @@ def config_input(name: str, scale_batch: int | None = None):
         return poly_coeffs((batch, c["n"]), c["seed"])
     if name == "conv1":
         return conv_signals(batch, c["n"], c["nh"], c["seed"])
-    if name in ("any1", "any2", "any3"):
+    if name in ("any1", "any2", "any3", "rows512"):
         return normal_complex((batch, c["n"]), c["seed"])
     if name == "nd1":
         return normal_complex((batch,) + tuple(c["shape"]), c["seed"])
