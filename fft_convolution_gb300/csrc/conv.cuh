@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(ConvRowsBounds<T, LOGN>::THREADS,
 #pragma unroll
   for (int w = 0; w < P::E; ++w)
     x[w] = active ? src(r, t + w * P::TP) : make_c<V>((T)0, (T)0);
-  fft_on_chip<LOGN, -1>(x, t, sm);
+  fft_on_chip<LOGN, -1, false, false>(x, t, sm);  // data came from global memory
 
   if constexpr (MODE == 0) {
     if (active) {

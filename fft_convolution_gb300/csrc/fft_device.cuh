@@ -271,7 +271,7 @@ __device__ __forceinline__ void stage_store(const V *x, int t, const SmemView<V>
   }
 }
 
-template <int LOGL, int K, int DIR, bool TABLE, typename V>
+template <int LOGL, int K, int DIR, bool TABLE, bool SYNC_FIRST, typename V>
 __device__ __forceinline__ void run_stages(V *x, int t, const SmemView<V> &sm, const V *tw) {
   using P = StagePlan<LOGL>;
   if constexpr (K < P::NS) {
@@ -283,11 +283,13 @@ __device__ __forceinline__ void run_stages(V *x, int t, const SmemView<V> &sm, c
     }
     stage_compute<R, P::E, P::TP, LOGM, DIR, TABLE>(x, t, TABLE ? tw + P::tw_offset(K) : tw);
     if constexpr (K + 1 < P::NS) {
-      __syncthreads();  // everyone has read the previous stage's data
+      // Everyone has read the previous stage's data (for the first stage:
+      // whatever the caller last read from this shared memory).
+      if constexpr (K > 0 || SYNC_FIRST) __syncthreads();
       stage_store<R, P::E, P::TP, LOGM>(x, t, sm);
       __syncthreads();  // this stage's data is complete
     }
-    run_stages<LOGL, K + 1, DIR, TABLE>(x, t, sm, tw);
+    run_stages<LOGL, K + 1, DIR, TABLE, SYNC_FIRST>(x, t, sm, tw);
   }
 }
 
@@ -296,10 +298,13 @@ __device__ __forceinline__ void run_stages(V *x, int t, const SmemView<V> &sm, c
 // its DFT (natural order).  Every thread of the block must call this the
 // same number of times (it contains __syncthreads when L > 16).  With
 // TABLE, the stage twiddles come from `tw` (filled by fill_twiddle_table).
-template <int LOGL, int DIR, bool TABLE = false, typename V>
+// SYNC_FIRST = false drops the barrier before the first stage's shared-memory
+// writes: for callers that have not read `sm` since their last barrier (a
+// transform loaded from global memory, or from `sm` before a barrier).
+template <int LOGL, int DIR, bool TABLE = false, bool SYNC_FIRST = true, typename V>
 __device__ __forceinline__ void fft_on_chip(V *x, int t, const SmemView<V> &sm,
                                             const V *tw = nullptr) {
-  run_stages<LOGL, 0, DIR, TABLE>(x, t, sm, tw);
+  run_stages<LOGL, 0, DIR, TABLE, SYNC_FIRST>(x, t, sm, tw);
 }
 
 // Fills the stage-twiddle table of an on-chip transform of length 2^LOGL

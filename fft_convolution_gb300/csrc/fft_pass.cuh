@@ -147,7 +147,9 @@ __global__ void __launch_bounds__(PassConfig<T, LOGL>::THREADS, PassConfig<T, LO
     }
 
     const SmemView<V> sm{smem + c, C};
-    fft_on_chip<LOGL, DIR, Cfg::TABLE>(x, t, sm, Cfg::TABLE ? twt : nullptr);
+    // The previous tile's shared-memory reads ended before the barrier at the
+    // end of the loop: the first stage needs no barrier of its own.
+    fft_on_chip<LOGL, DIR, Cfg::TABLE, false>(x, t, sm, Cfg::TABLE ? twt : nullptr);
 
     if constexpr (DIR > 0) {
 #pragma unroll

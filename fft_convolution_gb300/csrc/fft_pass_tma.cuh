@@ -187,28 +187,44 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
   __syncthreads();
   if (Cfg::NBUF == 2 && tid == 0 && blockIdx.x < g.total_tiles) issue_load(blockIdx.x, 0);
 
+  static_assert(C <= 32, "the threads that issue bulk stores are in warp 0");
   int k = 0;
   for (long long tile = blockIdx.x; tile < g.total_tiles; tile += gridDim.x, ++k) {
     const int s = Cfg::NBUF == 2 ? (k & 1) : 0;
     V *const cur = buf0 + s * Cfg::BUF_ELEMS;
     const long long next = tile + gridDim.x;
-    // The previous tile's stores (issued by threads < C) have left its
-    // buffer, and every thread is done with it.
-    if (tid < C) bulk_wait_read_all();
-    __syncthreads();
+    // The buffer the next load lands in last held the previous tile's
+    // output: every thread finished staging it before the previous
+    // iteration's last barrier, and only its bulk stores (issued by threads
+    // < C, all in warp 0) may still be reading it.  So warp 0 alone waits
+    // for them before thread 0 issues the load.
     bool prefetched = false;
-    if (tid == 0) {
-      if (Cfg::NBUF == 2) {
-        if (next < g.total_tiles) {
-          issue_load(next, s ^ 1);
-          prefetched = true;
+    if (tid < 32) {
+      if (tid < C) bulk_wait_read_all();
+      __syncwarp();
+      if (tid == 0) {
+        if (Cfg::NBUF == 2) {
+          if (next < g.total_tiles) {
+            issue_load(next, s ^ 1);
+            prefetched = true;
+          }
+        } else {
+          issue_load(tile, 0);
         }
-      } else {
-        issue_load(tile, 0);
       }
     }
     const uint32_t parity = Cfg::NBUF == 2 ? (uint32_t)(k >> 1) & 1u : (uint32_t)k & 1u;
     const bool ok = mbar_wait(&bar[s], parity);
+
+    const long long b = tile / g.tiles_per_batch;
+    const long long i = (tile % g.tiles_per_batch) * C + c;
+    // Read even when the wait ran out (the values are then stale but the
+    // addresses are the tile's own): the barrier below also carries the
+    // verdict.
+    V x[P::E];
+#pragma unroll
+    for (int w = 0; w < P::E; ++w) x[w] = cur[(t + w * P::TP) * C + c];
+    // The tile is in registers; buffer s becomes the exchange space.
     if (__syncthreads_or(!ok)) {
       if (tid == 0) {
         atomicExch(status, kDeviceErrorTimeout);
@@ -217,21 +233,16 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
       }
       break;
     }
-
-    const long long b = tile / g.tiles_per_batch;
-    const long long i = (tile % g.tiles_per_batch) * C + c;
-    V x[P::E];
-#pragma unroll
-    for (int w = 0; w < P::E; ++w) x[w] = cur[(t + w * P::TP) * C + c];
     if (g.twiddle && g.log_m > 0) {
       const long long p = i & ((1LL << g.log_m) - 1);
       const int log_lm = g.log_m + LOGL;
       apply_geometric<P::E>(x, twiddle<DIR>(p * t, log_lm, T()),
                             twiddle<DIR>(p * P::TP, log_lm, T()));
     }
-    __syncthreads();  // the tile is in registers; buffer s becomes the exchange space
 
-    fft_on_chip<LOGL, DIR, true>(x, t, SmemView<V>{cur + c, C}, twt);
+    // No barrier before the first stage's writes: every thread's reads of
+    // buffer s happened before the barrier above.
+    fft_on_chip<LOGL, DIR, true, false>(x, t, SmemView<V>{cur + c, C}, twt);
     if constexpr (DIR > 0) {
 #pragma unroll
       for (int w = 0; w < P::E; ++w) x[w] = c_scale(x[w], (T)(1.0 / L));

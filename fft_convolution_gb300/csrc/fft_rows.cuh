@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(RowsConfig<T, LOGN>::THREADS)
   asm volatile("griddepcontrol.launch_dependents;");
 
   const SmemView<V> sm{smem + f * P::SMEM_ELEMS, 1};
-  fft_on_chip<LOGN, DIR>(x, t, sm);
+  fft_on_chip<LOGN, DIR, false, false>(x, t, sm);  // data came from global memory
 
   if (active) {
     V *dst = out + tr * P::L;

@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(RowsColConfig<T, LOGW, LOGR>::THREADS)
   asm volatile("griddepcontrol.launch_dependents;");
 
   const SmemView<V> sm{smem + j * Cfg::SE, 1};
-  fft_on_chip<LOGW, DIR>(x, t, sm);
+  fft_on_chip<LOGW, DIR, false, false>(x, t, sm);  // data came from global memory
 
   // Row j's spectrum into its shared-memory row for the cross-row step.
   __syncthreads();  // the last on-chip exchange has been read

@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(RowsTConfig<T, LOGN>::THREADS)
   }
   asm volatile("griddepcontrol.launch_dependents;");
 
-  fft_on_chip<LOGN, DIR>(x, t, SmemView<V>{smem + f * P::SMEM_ELEMS, 1});
+  fft_on_chip<LOGN, DIR, false, false>(x, t, SmemView<V>{smem + f * P::SMEM_ELEMS, 1});
 
   // Stage as [column][row of the block], then store F rows' values of one
   // column together.

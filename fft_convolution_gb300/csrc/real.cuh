@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(RealRowsConfig<T, LOGH>::THREADS, RealRowsBoun
     for (int w = 0; w < P::E; ++w) x[w] = make_c<V>((T)0, (T)0);
   }
   const SmemView<V> sm{smem + f * C::ELEMS, 1};
-  fft_on_chip<LOGH, -1>(x, t, sm);
+  fft_on_chip<LOGH, -1, false, false>(x, t, sm);  // data came from global memory
 
   // x[w] = Z_k, k = t + w TP.  Mirror through shared memory.
   __syncthreads();
