@@ -218,6 +218,23 @@ template <typename V> struct SmemView {
   __device__ __forceinline__ void st(int idx, V v) const { base[pad16(idx) * stride] = v; }
 };
 
+// Shared-memory view of one of 8 interleaved fp32 columns (or 4 fp64): each
+// position is a 64-byte row of the C columns, so a warp touches 4 positions
+// and two of them share each 128-byte row of banks.  Positions whose index
+// differs by an even number land in the same half of that row (the radix-2
+// stage's writes at 2i + v hit one half four times), so the position is
+// stored at idx ^ ((idx >> 1) & 1): the half is then the parity of bits 0
+// and 1, which splits every stage pattern of these transforms (four
+// consecutive positions; 2i + v for four consecutive i; pairs 32 apart)
+// two and two.  No padding: L slots per column.
+template <typename V> struct SwzView {
+  V *base;
+  int stride;
+  __device__ __forceinline__ static int swz(int idx) { return idx ^ ((idx >> 1) & 1); }
+  __device__ __forceinline__ V ld(int idx) const { return base[swz(idx) * stride]; }
+  __device__ __forceinline__ void st(int idx, V v) const { base[swz(idx) * stride] = v; }
+};
+
 // One radix-R Stockham stage on the registers of thread t.  x[w] holds
 // element t + w*TP of the stage input.  Butterfly s (< E/R) is
 // i = t + s*TP; its inputs are x[s + u*(E/R)] and its outputs go back to the
@@ -257,8 +274,8 @@ __device__ __forceinline__ void stage_compute(V *x, int t, const V *tw) {
 
 // Write the outputs of stage (R, m) to shared memory at their Stockham
 // positions q*R*m + p + v*m (i = q*m + p).
-template <int R, int E, int TP, int LOGM, typename V>
-__device__ __forceinline__ void stage_store(const V *x, int t, const SmemView<V> &sm) {
+template <int R, int E, int TP, int LOGM, typename V, class View>
+__device__ __forceinline__ void stage_store(const V *x, int t, const View &sm) {
   constexpr int S = E / R;
   constexpr int M = 1 << LOGM;
 #pragma unroll
@@ -271,8 +288,8 @@ __device__ __forceinline__ void stage_store(const V *x, int t, const SmemView<V>
   }
 }
 
-template <int LOGL, int K, int DIR, bool TABLE, bool SYNC_FIRST, typename V>
-__device__ __forceinline__ void run_stages(V *x, int t, const SmemView<V> &sm, const V *tw) {
+template <int LOGL, int K, int DIR, bool TABLE, bool SYNC_FIRST, typename V, class View>
+__device__ __forceinline__ void run_stages(V *x, int t, const View &sm, const V *tw) {
   using P = StagePlan<LOGL>;
   if constexpr (K < P::NS) {
     constexpr int R = P::radix(K);
@@ -301,9 +318,9 @@ __device__ __forceinline__ void run_stages(V *x, int t, const SmemView<V> &sm, c
 // SYNC_FIRST = false drops the barrier before the first stage's shared-memory
 // writes: for callers that have not read `sm` since their last barrier (a
 // transform loaded from global memory, or from `sm` before a barrier).
-template <int LOGL, int DIR, bool TABLE = false, bool SYNC_FIRST = true, typename V>
-__device__ __forceinline__ void fft_on_chip(V *x, int t, const SmemView<V> &sm,
-                                            const V *tw = nullptr) {
+template <int LOGL, int DIR, bool TABLE = false, bool SYNC_FIRST = true, typename V,
+          class View = SmemView<V>>
+__device__ __forceinline__ void fft_on_chip(V *x, int t, const View &sm, const V *tw = nullptr) {
   run_stages<LOGL, 0, DIR, TABLE, SYNC_FIRST>(x, t, sm, tw);
 }
 

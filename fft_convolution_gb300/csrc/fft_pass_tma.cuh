@@ -115,7 +115,10 @@ template <typename T, int LOGL> struct TmaConfig {
   // the banks; at least 2 for fp32, so every column starts 16-byte aligned.
   static constexpr int PAD = 32 / C >= 2 ? 32 / C : (sizeof(T) == 4 ? 2 : 1);
   static constexpr int RS = L + PAD;
-  static constexpr int RAW_EX = PassConfig<T, LOGL>::ROW_ELEMS * C;  // exchange
+  // Exchange layout: 64-byte rows of C columns take the swizzled view
+  // (SwzView, L slots per column), other widths the padded one.
+  static constexpr bool SWIZZLE = C * sizeof(V) == 64;
+  static constexpr int RAW_EX = SWIZZLE ? L * C : PassConfig<T, LOGL>::ROW_ELEMS * C;
   static constexpr int RAW_ELEMS = RAW_EX > C * RS ? RAW_EX : C * RS;
   static constexpr int MIN_BLOCKS = THREADS >= 1024 ? 1 : (THREADS >= 512 ? 2 : (THREADS >= 256 ? 3 : 4));
   static constexpr int BUF_ELEMS =
@@ -242,7 +245,10 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
 
     // No barrier before the first stage's writes: every thread's reads of
     // buffer s happened before the barrier above.
-    fft_on_chip<LOGL, DIR, true, false>(x, t, SmemView<V>{cur + c, C}, twt);
+    if constexpr (Cfg::SWIZZLE)
+      fft_on_chip<LOGL, DIR, true, false>(x, t, SwzView<V>{cur + c, C}, twt);
+    else
+      fft_on_chip<LOGL, DIR, true, false>(x, t, SmemView<V>{cur + c, C}, twt);
     if constexpr (DIR > 0) {
 #pragma unroll
       for (int w = 0; w < P::E; ++w) x[w] = c_scale(x[w], (T)(1.0 / L));
