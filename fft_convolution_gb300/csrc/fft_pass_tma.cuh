@@ -126,10 +126,16 @@ template <typename T, int LOGL> struct TmaConfig {
   // Stage-twiddle table shared by the block's columns (rounded to 128 B).
   static constexpr int TW_ELEMS =
       ((P::TW_ELEMS * (int)sizeof(V) + 127) / 128) * 128 / (int)sizeof(V);
-  // Two buffers (prefetch the next tile while computing this one) when that
-  // still leaves room for three blocks per SM; otherwise one buffer, and the
-  // overlap comes from the other blocks on the SM.
-  static constexpr int NBUF = 2 * BUF_ELEMS * sizeof(V) <= 76 * 1024 ? 2 : 1;
+  // Buffers per block: the loads run NBUF - 1 tiles ahead of the
+  // computation.  Three (two tiles in flight) when that leaves room for two
+  // blocks per SM, else two when three blocks still fit, else one (the
+  // overlap then comes from the other blocks on the SM).  Measured on GB300
+  // (fp32, ms): 2^26 transform 0.570 with two buffers at three blocks per SM,
+  // 0.542 with three at two blocks, 0.831 with four at one block; 8 x 2048^2
+  // forward + inverse 0.415, 0.397, 0.487.
+  static constexpr int NBUF = 3 * BUF_ELEMS * sizeof(V) <= 110 * 1024
+                                  ? 3
+                                  : (2 * BUF_ELEMS * sizeof(V) <= 76 * 1024 ? 2 : 1);
   static constexpr size_t SMEM =
       256 + (size_t)TW_ELEMS * sizeof(V) + NBUF * (size_t)BUF_ELEMS * sizeof(V);
 };
@@ -181,43 +187,48 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
                   k * Cfg::ROWS_PER_BOX, (int)b);
   };
 
+  constexpr int NB = Cfg::NBUF;
+  static_assert(NB >= 1 && NB <= 15, "one mbarrier per buffer in the first 128 bytes");
   if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+#pragma unroll
+    for (int j = 0; j < NB; ++j) mbar_init(&bar[j], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   fill_twiddle_table<LOGL, DIR>(twt, tid, Cfg::THREADS);
   __syncthreads();
-  if (Cfg::NBUF == 2 && tid == 0 && blockIdx.x < g.total_tiles) issue_load(blockIdx.x, 0);
+  // With NB buffers the loads run NB - 1 tiles ahead of the computation:
+  // tile k of this block lives in buffer k mod NB.
+  if (NB > 1 && tid == 0) {
+#pragma unroll
+    for (int j = 0; j + 1 < NB; ++j) {
+      const long long tj = blockIdx.x + (long long)j * gridDim.x;
+      if (tj < g.total_tiles) issue_load(tj, j);
+    }
+  }
 
   static_assert(C <= 32, "the threads that issue bulk stores are in warp 0");
   int k = 0;
   for (long long tile = blockIdx.x; tile < g.total_tiles; tile += gridDim.x, ++k) {
-    const int s = Cfg::NBUF == 2 ? (k & 1) : 0;
+    const int s = k % NB;
     V *const cur = buf0 + s * Cfg::BUF_ELEMS;
-    const long long next = tile + gridDim.x;
-    // The buffer the next load lands in last held the previous tile's
-    // output: every thread finished staging it before the previous
-    // iteration's last barrier, and only its bulk stores (issued by threads
-    // < C, all in warp 0) may still be reading it.  So warp 0 alone waits
-    // for them before thread 0 issues the load.
-    bool prefetched = false;
+    const long long ahead = tile + (long long)(NB - 1) * gridDim.x;
+    // The buffer the next load lands in, (k - 1) mod NB, last held the
+    // previous tile's output: every thread finished staging it before the
+    // previous iteration's last barrier, and only its bulk stores (issued by
+    // threads < C, all in warp 0) may still be reading it.  So warp 0 alone
+    // waits for them before thread 0 issues the load.
     if (tid < 32) {
       if (tid < C) bulk_wait_read_all();
       __syncwarp();
       if (tid == 0) {
-        if (Cfg::NBUF == 2) {
-          if (next < g.total_tiles) {
-            issue_load(next, s ^ 1);
-            prefetched = true;
-          }
+        if (NB > 1) {
+          if (ahead < g.total_tiles) issue_load(ahead, (k + NB - 1) % NB);
         } else {
           issue_load(tile, 0);
         }
       }
     }
-    const uint32_t parity = Cfg::NBUF == 2 ? (uint32_t)(k >> 1) & 1u : (uint32_t)k & 1u;
-    const bool ok = mbar_wait(&bar[s], parity);
+    const bool ok = mbar_wait(&bar[s], (uint32_t)(k / NB) & 1u);
 
     const long long b = tile / g.tiles_per_batch;
     const long long i = (tile % g.tiles_per_batch) * C + c;
@@ -231,8 +242,11 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
     if (__syncthreads_or(!ok)) {
       if (tid == 0) {
         atomicExch(status, kDeviceErrorTimeout);
-        // Let the prefetch issued above land before the block exits.
-        if (prefetched) mbar_wait(&bar[s ^ 1], (uint32_t)((k + 1) >> 1) & 1u);
+        // Let the loads issued ahead land before the block exits.
+#pragma unroll
+        for (int j = 1; j < NB; ++j)
+          if (tile + (long long)j * gridDim.x < g.total_tiles)
+            mbar_wait(&bar[(k + j) % NB], (uint32_t)((k + j) / NB) & 1u);
       }
       break;
     }
