@@ -288,8 +288,25 @@ __device__ __forceinline__ void stage_store(const V *x, int t, const View &sm) {
   }
 }
 
-template <int LOGL, int K, int DIR, bool TABLE, bool SYNC_FIRST, typename V, class View>
-__device__ __forceinline__ void run_stages(V *x, int t, const View &sm, const V *tw) {
+// Barriers between the stages: the whole block (default), or a named
+// barrier of the `count` threads that share one transform (bar.sync id,
+// count), so that several independent transforms in a block do not wait
+// for one another.
+struct BlockSync {
+  __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+struct GroupSync {
+  int id;     // 1 .. 15 (0 is the block-wide barrier)
+  int count;  // threads of the group, a multiple of 32
+  __device__ __forceinline__ void operator()() const {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+  }
+};
+
+template <int LOGL, int K, int DIR, bool TABLE, bool SYNC_FIRST, typename V, class View,
+          class Sync = BlockSync>
+__device__ __forceinline__ void run_stages(V *x, int t, const View &sm, const V *tw,
+                                           Sync sync = Sync()) {
   using P = StagePlan<LOGL>;
   if constexpr (K < P::NS) {
     constexpr int R = P::radix(K);
@@ -302,11 +319,11 @@ __device__ __forceinline__ void run_stages(V *x, int t, const View &sm, const V 
     if constexpr (K + 1 < P::NS) {
       // Everyone has read the previous stage's data (for the first stage:
       // whatever the caller last read from this shared memory).
-      if constexpr (K > 0 || SYNC_FIRST) __syncthreads();
+      if constexpr (K > 0 || SYNC_FIRST) sync();
       stage_store<R, P::E, P::TP, LOGM>(x, t, sm);
-      __syncthreads();  // this stage's data is complete
+      sync();  // this stage's data is complete
     }
-    run_stages<LOGL, K + 1, DIR, TABLE, SYNC_FIRST>(x, t, sm, tw);
+    run_stages<LOGL, K + 1, DIR, TABLE, SYNC_FIRST>(x, t, sm, tw, sync);
   }
 }
 
@@ -319,9 +336,10 @@ __device__ __forceinline__ void run_stages(V *x, int t, const View &sm, const V 
 // writes: for callers that have not read `sm` since their last barrier (a
 // transform loaded from global memory, or from `sm` before a barrier).
 template <int LOGL, int DIR, bool TABLE = false, bool SYNC_FIRST = true, typename V,
-          class View = SmemView<V>>
-__device__ __forceinline__ void fft_on_chip(V *x, int t, const View &sm, const V *tw = nullptr) {
-  run_stages<LOGL, 0, DIR, TABLE, SYNC_FIRST>(x, t, sm, tw);
+          class View = SmemView<V>, class Sync = BlockSync>
+__device__ __forceinline__ void fft_on_chip(V *x, int t, const View &sm, const V *tw = nullptr,
+                                            Sync sync = Sync()) {
+  run_stages<LOGL, 0, DIR, TABLE, SYNC_FIRST>(x, t, sm, tw, sync);
 }
 
 // Fills the stage-twiddle table of an on-chip transform of length 2^LOGL

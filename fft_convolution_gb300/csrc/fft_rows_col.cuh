@@ -34,6 +34,11 @@ namespace {
 
 template <typename T, int LOGW, int LOGR> struct RowsColConfig {
   using P = StagePlan<LOGW>;
+  // Four or more rows of whole warps synchronise by named barriers (ids
+  // 1 .. R).  Measured on GB300 (fp32, forward + inverse): 8 x 2048^2 with
+  // R = 4 0.398 -> 0.392 ms; 32 x 1024^2 with R = 2 0.352 -> 0.383 ms, so
+  // two-row blocks keep the block-wide barrier.
+  static constexpr bool GROUP_SYNC = P::TP % 32 == 0 && LOGR >= 2 && (1 << LOGR) <= 15;
   static constexpr int R = 1 << LOGR;
   static constexpr int THREADS = R * P::TP;
   static constexpr int SE = P::SMEM_ELEMS > P::L + P::L / 16 ? P::SMEM_ELEMS : P::L + P::L / 16;
@@ -71,13 +76,21 @@ __global__ void __launch_bounds__(RowsColConfig<T, LOGW, LOGR>::THREADS)
   asm volatile("griddepcontrol.launch_dependents;");
 
   const SmemView<V> sm{smem + j * Cfg::SE, 1};
-  fft_on_chip<LOGW, DIR, false, false>(x, t, sm);  // data came from global memory
-
+  // Each row's transform synchronises only its own TP threads (named
+  // barrier 1 + j), so the R rows of a block proceed independently until
+  // the cross-row step.  The data came from global memory.
+  if constexpr (Cfg::GROUP_SYNC) {
+    const GroupSync gsync{1 + j, P::TP};
+    fft_on_chip<LOGW, DIR, false, false>(x, t, sm, static_cast<const V *>(nullptr), gsync);
+    gsync();  // the row's last on-chip exchange has been read
+  } else {
+    fft_on_chip<LOGW, DIR, false, false>(x, t, sm);
+    __syncthreads();
+  }
   // Row j's spectrum into its shared-memory row for the cross-row step.
-  __syncthreads();  // the last on-chip exchange has been read
 #pragma unroll
   for (int w = 0; w < P::E; ++w) sm.st(t + w * P::TP, x[w]);
-  __syncthreads();
+  __syncthreads();  // every row's spectrum is in place
 
   // W_H^{a d}, d < R (conjugate for the inverse).
   V tw[R];
