@@ -14,7 +14,8 @@
 // applying the stage twiddles (read from a per-plan table of the forward
 // roots, conjugated for the inverse), running the radix-R DFT in registers
 // and storing the R outputs.  Radices 2, 4, 8, 16 use the power-of-two
-// register DFTs; 3, 5, 7 pair x_u with x_{R-u}:
+// register DFTs, 15 the prime-factor split into 3 and 5 (dft15); 3, 5, 7
+// pair x_u with x_{R-u}:
 //   X_v = x_0 + sum_{u<=(R-1)/2} [(x_u + x_{R-u}) cos(2 pi uv/R)
 //                                 + DIR i (x_u - x_{R-u}) sin(2 pi uv/R)],
 // and X_{R-v} the same with the sine term negated.
@@ -81,8 +82,36 @@ template <int R, int DIR, typename V> __device__ __forceinline__ void dft_odd(V 
   }
 }
 
+// In-register DFT of length 15 = 3 * 5 by the prime-factor mapping (the
+// factors are coprime, so no twiddles sit between the two sub-transforms):
+// with u = (5 n1 + 3 n2) mod 15 and v = (10 k1 + 6 k2) mod 15,
+//   u v = 5 n1 k1 + 3 n2 k2 (mod 15)   (10 = 5 * (5^-1 mod 3), 6 = 3 * (3^-1 mod 5)),
+// so X_v = sum_{n2} W_5^{n2 k2} sum_{n1} W_3^{n1 k1} x_u: five 3-point DFTs,
+// then three 5-point DFTs, the index maps being register renaming only.
+template <int DIR, typename V> __device__ __forceinline__ void dft15(V *x) {
+  V a[5][3];
+#pragma unroll
+  for (int n2 = 0; n2 < 5; ++n2)
+#pragma unroll
+    for (int n1 = 0; n1 < 3; ++n1) a[n2][n1] = x[(5 * n1 + 3 * n2) % 15];
+#pragma unroll
+  for (int n2 = 0; n2 < 5; ++n2) dft_odd<3, DIR>(a[n2]);
+  V b[3][5];
+#pragma unroll
+  for (int k1 = 0; k1 < 3; ++k1)
+#pragma unroll
+    for (int n2 = 0; n2 < 5; ++n2) b[k1][n2] = a[n2][k1];
+#pragma unroll
+  for (int k1 = 0; k1 < 3; ++k1) dft_odd<5, DIR>(b[k1]);
+#pragma unroll
+  for (int k1 = 0; k1 < 3; ++k1)
+#pragma unroll
+    for (int k2 = 0; k2 < 5; ++k2) x[(10 * k1 + 6 * k2) % 15] = b[k1][k2];
+}
+
 template <int R, int DIR, typename V> __device__ __forceinline__ void dft_any(V *x) {
   if constexpr (R == 3 || R == 5 || R == 7) dft_odd<R, DIR>(x);
+  else if constexpr (R == 15) dft15<DIR>(x);
   else dft_reg<R, DIR>(x);
 }
 
@@ -154,6 +183,7 @@ __device__ __forceinline__ void mixed_stage_any(const V *src, V *dst, const Mixe
     case 5: mixed_stage<5, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
     case 7: mixed_stage<7, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
     case 8: mixed_stage<8, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
+    case 15: mixed_stage<15, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
     default: mixed_stage<16, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
   }
 }
@@ -206,6 +236,7 @@ __device__ __forceinline__ void mixed_first_stage_any(const V *g, V *dst, const 
     case 5: mixed_first_stage<5, DIR>(g, dst, ms, rows); break;
     case 7: mixed_first_stage<7, DIR>(g, dst, ms, rows); break;
     case 8: mixed_first_stage<8, DIR>(g, dst, ms, rows); break;
+    case 15: mixed_first_stage<15, DIR>(g, dst, ms, rows); break;
     default: mixed_first_stage<16, DIR>(g, dst, ms, rows); break;
   }
 }
