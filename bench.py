@@ -550,38 +550,50 @@ class Workload:
             passes = self.plans[0].num_kernels
         self.info = workload_info(name, passes=passes)
 
+    def call(self, which: int):
+        """The step's first (0: the dominant forward call) or second (1:
+        the inverse, where the workload has one) library call."""
+        fg, sh = self.fg, self.sh
+        if which == 0:
+            if self.kind == "conv":
+                rc = fg.fft_convolve(self.xc_d.data_ptr(), self.c["n"], self.hc_d.data_ptr(),
+                                     self.c["nh"], self.yc_d.data_ptr(), self.c["batch"], 0,
+                                     fg.FFT_CONV_REAL, fg.FFT_C2C_F32, sh)
+            elif self.kind == "polymul":
+                rc = fg.polymul_batched(self.a_d.data_ptr(), self.c["n"], self.b_d.data_ptr(),
+                                        self.c["n"], self.c_d.data_ptr(), self.c["batch"], sh)
+            elif self.kind == "real":
+                rc = fg.fft_exec(self.plans[0].handle, self.x_d.data_ptr(), self.X_d.data_ptr(), sh)
+            else:
+                rc = fg.fft_exec(self.plans[0].handle, self.x_d.data_ptr(), self.y_d.data_ptr(), sh)
+        elif self.kind == "real":
+            rc = fg.fft_exec(self.plans[1].handle, self.X_d.data_ptr(), self.y_d.data_ptr(), sh)
+        else:
+            rc = fg.fft_exec(self.plans[1].handle, self.y_d.data_ptr(), self.z_d.data_ptr(), sh)
+        assert rc == 0, fg.fft_status_string(rc)
+
+    def has_second(self) -> bool:
+        return self.kind == "real" or (self.kind not in ("conv", "polymul") and len(self.plans) == 2)
+
     def step(self, events=None):
-        """One step; events[0..2] (optional) bracket its launches: [0]..[1]
-        the first (dominant) call, [1]..[2] the second.  Inputs smaller than
-        L2 are preceded by an L2 flush (outside the brackets)."""
-        fg, sh, st = self.fg, self.sh, self.stream
+        """One step.  Inputs smaller than L2 are preceded by an L2 flush,
+        and then events[0..2] (which such workloads pass) bracket the calls:
+        [0]..[1] the first, [1]..[2] the second.  Other workloads are timed
+        without events between their calls (an event recorded between two
+        launches keeps the second from starting while the first drains)."""
+        st = self.stream
         if self.flush is not None:
             with self.torch.cuda.stream(st):
                 self.flush.zero_()
         if events is not None:
             events[0].record(st)
-        if self.kind == "conv":
-            rc = [fg.fft_convolve(self.xc_d.data_ptr(), self.c["n"], self.hc_d.data_ptr(),
-                                  self.c["nh"], self.yc_d.data_ptr(), self.c["batch"], 0,
-                                  fg.FFT_CONV_REAL, fg.FFT_C2C_F32, sh)]
-        elif self.kind == "polymul":
-            rc = [fg.polymul_batched(self.a_d.data_ptr(), self.c["n"], self.b_d.data_ptr(),
-                                     self.c["n"], self.c_d.data_ptr(), self.c["batch"], sh)]
-        elif self.kind == "real":
-            rc = [fg.fft_exec(self.plans[0].handle, self.x_d.data_ptr(), self.X_d.data_ptr(), sh)]
-        else:
-            rc = [fg.fft_exec(self.plans[0].handle, self.x_d.data_ptr(), self.y_d.data_ptr(), sh)]
+        self.call(0)
         if events is not None:
             events[1].record(st)
-        if self.kind == "real":
-            rc.append(fg.fft_exec(self.plans[1].handle, self.X_d.data_ptr(), self.y_d.data_ptr(),
-                                  sh))
-        elif self.kind not in ("conv", "polymul") and len(self.plans) == 2:
-            rc.append(fg.fft_exec(self.plans[1].handle, self.y_d.data_ptr(), self.z_d.data_ptr(),
-                                  sh))
+        if self.has_second():
+            self.call(1)
         if events is not None:
             events[2].record(st)
-        assert all(r == 0 for r in rc), [fg.fft_status_string(r) for r in rc]
 
     def e2e_step_fn(self, torch, chunks):
         """One end-to-end step through the host-buffer entry points (pinned
@@ -675,14 +687,15 @@ def measure(name, args, fg, torch, dev, world, barrier, with_cpu):
             w.step()
         torch.cuda.synchronize(dev)
 
-    # Timed region.
+    # Timed region: the steps alone between one pair of events (workloads
+    # smaller than L2 flush it before each step, outside per-call events).
     barrier()
     torch.cuda.synchronize(dev)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for k in range(args.steps):
-        w.step(ev[k])
+        w.step(ev[k] if w.flush is not None else None)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -693,11 +706,22 @@ def measure(name, args, fg, torch, dev, world, barrier, with_cpu):
         # The step's own time, without the L2 flush before it.
         ms_step = max_over_ranks(statistics.mean(e[0].elapsed_time(e[2]) for e in ev), world,
                                  dev)
-
-    # Per-launch durations of the dominant call (the forward transform).
-    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    inv_ms = [e[1].elapsed_time(e[2]) for e in ev] \
-        if info["kind"] in ("fft1d", "fft2d", "fftnd", "real") and info["directions"] == 2 else []
+        fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+        inv_ms = [e[1].elapsed_time(e[2]) for e in ev] if w.has_second() else []
+    else:
+        # Average duration of each call of the step: the same number of
+        # back-to-back launches of that call alone, between one pair of
+        # events on the launching stream.
+        def timed_calls(which):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                w.call(which)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            return [e0.elapsed_time(e1) / args.steps]
+        fwd_ms = timed_calls(0)
+        inv_ms = timed_calls(1) if w.has_second() else []
 
     # End-to-end through the host-buffer entry points, every step.
     e2e = None
