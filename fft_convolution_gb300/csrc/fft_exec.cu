@@ -100,6 +100,7 @@ struct Schedule {
     }
     if (e != cudaSuccess) return e;
     int inner = p->logn;  // log2 of the stride of the next axis
+    int after_pass = 0;   // the previous kernel was a pass (not the row kernel)
     for (int k = p->rank - 2; k >= 0; --k) {
       int l = p->shape_log[k];
       int stride_log = inner;
@@ -109,9 +110,12 @@ struct Schedule {
       }
       if (l > 0) {
         const int log_block = l + stride_log;  // one column block: L * stride elements
-        PassArgs a{log_block, l, stride_log, 0, batch * (p->elems >> log_block)};
+        // The first column pass follows the row kernel; a later one (3D)
+        // follows a pass and may overlap its tail.
+        PassArgs a{log_block, l, stride_log, 0, batch * (p->elems >> log_block), after_pass};
         e = pass(a, out, out);
         if (e != cudaSuccess) return e;
+        after_pass = 1;
       }
       inner += p->shape_log[k];
     }
@@ -203,7 +207,7 @@ struct Schedule {
     const char *src = k_begin == 0 ? in : (k_begin % 2 == 1 ? ws : out);
     for (int k = k_begin; k < p->npasses; ++k) {
       char *dst = (k == p->npasses - 1) ? out : (k % 2 == 0 ? ws : out);
-      PassArgs a{p->logn, p->pass_log[k], log_m, 1, batch};
+      PassArgs a{p->logn, p->pass_log[k], log_m, 1, batch, k > 0 ? 1 : 0};
       cudaError_t e = pass(a, src, dst);
       if (e != cudaSuccess) return e;
       src = dst;

@@ -218,7 +218,7 @@ cudaError_t launch_pass_t(Load load, Store store, int log_n, int log_m, int twid
 
 template <typename T, int LOGL, int DIR>
 cudaError_t launch_pass_tma_t(const void *in, void *out, int log_n, int log_m, int twiddle,
-                              long long batch, cudaStream_t st);
+                              long long batch, cudaStream_t st, int overlap = 0);
 template <typename T, int LOGL, int DIR>
 cudaError_t launch_pass_cluster_t(const void *in, void *out, int log_n, int log_m, int twiddle,
                                   long long batch, cudaStream_t st, int debug_fail = 0,
@@ -235,7 +235,8 @@ cudaError_t dispatch_pass(const PassArgs &a, const void *in, void *out, cudaStre
       cudaError_t e = launch_pass_cluster_t<T, LOGL, DIR>(in, out, a.log_n, a.log_m, a.twiddle,
                                                           a.batch, st);
       if (e != cudaErrorNotSupported) return e;
-      e = launch_pass_tma_t<T, LOGL, DIR>(in, out, a.log_n, a.log_m, a.twiddle, a.batch, st);
+      e = launch_pass_tma_t<T, LOGL, DIR>(in, out, a.log_n, a.log_m, a.twiddle, a.batch, st,
+                                          a.overlap);
       if (e != cudaErrorNotSupported) return e;
       return launch_pass_t<T, LOGL, DIR>(LoadComplex<V>{static_cast<const V *>(in), n},
                                          StoreComplex<V>{static_cast<V *>(out), n}, a.log_n,

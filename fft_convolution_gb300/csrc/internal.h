@@ -95,13 +95,19 @@ inline bool rows_col_supported(bool f64, int logw, int logr) {
 // length 2^log_l, each over the elements i + u * 2^(log_n - log_l),
 // u < 2^log_l, and is the radix-2^log_l Stockham stage whose previous block
 // length is 2^log_m.  With twiddle != 0 input u of butterfly i is first
-// multiplied by W_{2^(log_l+log_m)}^{(i mod 2^log_m) u}.
+// multiplied by W_{2^(log_l+log_m)}^{(i mod 2^log_m) u}.  overlap != 0
+// lets the TMA pass kernel start while the previous kernel on the stream
+// drains (programmatic dependent launch): set only after another pass,
+// whose persistent grid leaves no room for the new blocks until it
+// retires -- after a kernel of many short waves the new persistent blocks
+// would sit on SM resources that kernel still needs.
 struct PassArgs {
   int log_n;
   int log_l;
   int log_m;
   int twiddle;
   long long batch;
+  int overlap = 0;
 };
 cudaError_t launch_pass_f32(int dir, const PassArgs &a, const void *in, void *out,
                             cudaStream_t st);
