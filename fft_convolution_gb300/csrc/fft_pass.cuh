@@ -89,8 +89,9 @@ struct PassGeom {
   int log_n;
   int log_m;
   int twiddle;
-  long long grid_per_batch;  // tiles per transform
+  long long grid_per_batch;  // tiles per transform (a power of two)
   long long total;           // grid_per_batch * batch: the tiles of the launch
+  int log_gpb;               // log2(grid_per_batch)
 };
 
 // Persistent: each block fills the stage-twiddle table once, then walks
@@ -114,8 +115,8 @@ __global__ void __launch_bounds__(PassConfig<T, LOGL>::THREADS, PassConfig<T, LO
   __syncthreads();
 
   for (long long blk = blockIdx.x; blk < g.total; blk += gridDim.x) {
-    const long long tile = blk % g.grid_per_batch;
-    const long long b = blk / g.grid_per_batch;
+    const long long tile = blk & (g.grid_per_batch - 1);
+    const long long b = blk >> g.log_gpb;
     const long long i = tile * C + c;
     const bool active = i < cols;
 
@@ -202,7 +203,9 @@ cudaError_t launch_pass_t(Load load, Store store, int log_n, int log_m, int twid
     if (e != cudaSuccess) return e;
   }
   const long long tiles = pass_tiles<T, LOGL>(log_n);
-  PassGeom g{log_n, log_m, twiddle, tiles, tiles * batch};
+  int log_gpb = 0;
+  while ((1LL << log_gpb) < tiles) ++log_gpb;
+  PassGeom g{log_n, log_m, twiddle, tiles, tiles * batch, log_gpb};
   if (g.total <= 0) return cudaErrorInvalidConfiguration;
   // Persistent grid: as many blocks as fit on the device at once.
   static std::atomic<int> occupancy[64];

@@ -149,8 +149,8 @@ __global__ void __launch_bounds__(ClusterConfig<T, LOGL>::THREADS,
   const bool failing = g.debug_fail == r + 1;
   const uint32_t limit = failing && g.poll_limit ? g.poll_limit : 1u << 22;
   auto issue_load = [&](long long tile) {
-    const long long b = tile / g.tiles_per_batch;
-    const long long i0 = (tile % g.tiles_per_batch) * C;
+    const long long b = tile >> g.log_tpb;
+    const long long i0 = (tile & (g.tiles_per_batch - 1)) * C;
     mbar_expect_tx(&bar[0], Cfg::TILE_BYTES);
 #pragma unroll
     for (int kb = 0; kb < LP / Cfg::BOX_IN; ++kb)
@@ -170,8 +170,8 @@ __global__ void __launch_bounds__(ClusterConfig<T, LOGL>::THREADS,
 
   int k = 0;
   for (long long tile = cluster; tile < g.total_tiles; tile += nclusters, ++k) {
-    const long long b = tile / g.tiles_per_batch;
-    const long long i0 = (tile % g.tiles_per_batch) * C;
+    const long long b = tile >> g.log_tpb;
+    const long long i0 = (tile & (g.tiles_per_batch - 1)) * C;
     const long long next = tile + nclusters;
     const bool ok = mbar_wait(&bar[0], (uint32_t)k & 1u, limit);
     const int bad = __syncthreads_or(!ok);
@@ -376,7 +376,7 @@ cudaError_t launch_pass_cluster_t(const void *in, void *out, int log_n, int log_
       resident[dev].store(ncl, std::memory_order_release);
     }
     TmaGeom g{log_n, log_m, twiddle, cols / Cfg::C, (cols / Cfg::C) * batch, debug_fail,
-              poll_limit};
+              poll_limit, log2_pow2(cols / Cfg::C)};
     long long clusters = ncl < g.total_tiles ? ncl : g.total_tiles;
     cfg.gridDim = dim3((unsigned)(clusters * Cfg::R));
     return cudaLaunchKernelEx(&cfg, kern, tin, tout, static_cast<vec2_t<T> *>(out), g,

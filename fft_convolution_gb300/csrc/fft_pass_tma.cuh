@@ -151,7 +151,15 @@ struct TmaGeom {
   // (and issues no copy); its waits give up after poll_limit polls.
   int debug_fail;
   unsigned poll_limit;
+  int log_tpb;  // log2(tiles_per_batch): tile counts are powers of two
 };
+
+// log2 of a power of two (host).
+inline int log2_pow2(long long v) {
+  int l = 0;
+  while ((1LL << l) < v) ++l;
+  return l;
+}
 
 template <typename T, int LOGL, int DIR>
 __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL>::MIN_BLOCKS)
@@ -177,8 +185,8 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
   const long long cols = 1LL << (g.log_n - LOGL);
 
   auto issue_load = [&](long long tile, int s) {
-    const long long b = tile / g.tiles_per_batch;
-    const long long i0 = (tile % g.tiles_per_batch) * C;
+    const long long b = tile >> g.log_tpb;
+    const long long i0 = (tile & (g.tiles_per_batch - 1)) * C;
     V *dst = buf0 + s * Cfg::BUF_ELEMS;
     mbar_expect_tx(&bar[s], Cfg::TILE_BYTES);
 #pragma unroll
@@ -238,8 +246,8 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
     }
     const bool ok = mbar_wait(&bar[s], (uint32_t)(k / NB) & 1u);
 
-    const long long b = tile / g.tiles_per_batch;
-    const long long i = (tile % g.tiles_per_batch) * C + c;
+    const long long b = tile >> g.log_tpb;
+    const long long i = (tile & (g.tiles_per_batch - 1)) * C + c;
     // Read even when the wait ran out (the values are then stale but the
     // addresses are the tile's own): the barrier below also carries the
     // verdict.
@@ -287,7 +295,7 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
       fence_async_smem();
       __syncthreads();
       if (tid < C) {
-        V *dst = out_linear + b * (1LL << g.log_n) + ((tile % g.tiles_per_batch) * C + tid) * L;
+        V *dst = out_linear + b * (1LL << g.log_n) + ((tile & (g.tiles_per_batch - 1)) * C + tid) * L;
         bulk_store(dst, cur + tid * RS, (uint32_t)(L * sizeof(V)));
         bulk_commit();
       }
@@ -300,7 +308,7 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
       if (tid == 0) {
         const long long m = 1LL << g.log_m;
         const long long q = i >> g.log_m;  // same for the whole tile (C <= m)
-        const long long p0 = (tile % g.tiles_per_batch) * C & (m - 1);
+        const long long p0 = (tile & (g.tiles_per_batch - 1)) * C & (m - 1);
 #pragma unroll
         for (int kb = 0; kb < Cfg::BOXES; ++kb)
           tma_store_4d(&tout, cur + kb * Cfg::ROWS_PER_BOX * C, (int)(2 * p0),
@@ -401,7 +409,8 @@ cudaError_t launch_pass_tma_t(const void *in, void *out, int log_n, int log_m, i
     static DeviceOnce attr_set;
     const cudaError_t attr = smem_limit_once((const void *)kern, Cfg::SMEM, attr_set);
     if (attr != cudaSuccess) return attr;
-    TmaGeom g{log_n, log_m, twiddle, cols / Cfg::C, (cols / Cfg::C) * batch, 0, 0};
+    TmaGeom g{log_n, log_m, twiddle, cols / Cfg::C, (cols / Cfg::C) * batch, 0, 0,
+              log2_pow2(cols / Cfg::C)};
     static std::atomic<int> occupancy[64];
     const int per_sm = blocks_per_sm_once((const void *)kern, Cfg::THREADS, Cfg::SMEM, occupancy);
     long long grid = (long long)sms * (per_sm > 0 ? per_sm : 1);
