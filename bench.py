@@ -852,8 +852,12 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     for item in args.option:
         name, _, value = item.partition("=")
-        code = getattr(fg, "FFT_OPT_" + name.strip().upper())
-        rc = fg.fft_debug_set_option(code, int(value))
+        name = name.strip().upper()
+        code = getattr(fg, "FFT_OPT_" + name)
+        # PASS_SPLIT takes the per-pass factors, first pass first: 13,13
+        v = fg.pass_split_value(int(f) for f in value.split(",")) \
+            if name == "PASS_SPLIT" and "," in value else int(value)
+        rc = fg.fft_debug_set_option(code, v)
         assert rc == 0, f"option {item}: {fg.fft_status_string(rc)}"
 
     def barrier():
@@ -1051,7 +1055,8 @@ def main():
                     help="seconds of untimed load sampled for clocks before the timed region")
     ap.add_argument("--option", action="append", default=[], metavar="NAME=VALUE",
                     help="force a library choice through its test hook before planning, e.g. "
-                         "ROWS_SHFL=1 or COL_RADIX_LOG=0 (kernel comparisons; recorded in config)")
+                         "ROWS_SHFL=1, COL_RADIX_LOG=0 or PASS_SPLIT=13,13 (kernel comparisons; "
+                         "recorded in config)")
     ap.add_argument("--n", type=int, default=None,
                     help="override the transform length (small profiling cases)")
     ap.add_argument("--batch", type=int, default=None,
