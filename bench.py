@@ -544,11 +544,33 @@ class Workload:
                 self.plans.append(fg.Plan(c["n"], c["batch"], dims, fg.FFT_INVERSE,
                                           fg.FFT_C2C_F32, shape=shape))
             self.kernels_per_step = sum(p.num_kernels for p in self.plans)
+        self.check_shapes()
         # The HBM passes of the plan actually built (multi-pass 1D: one per kernel).
         passes = None
         if info["kind"] == "fft1d" and c["n"] & (c["n"] - 1) == 0 and log2i(c["n"]) > 14:
             passes = self.plans[0].num_kernels
         self.info = workload_info(name, passes=passes)
+
+    def check_shapes(self):
+        """Host-side check, before any launch, that every device buffer holds
+        what the plans and calls of this workload read and write."""
+        c = self.c
+        if self.kind == "conv":
+            ok = tuple(self.xc_d.shape) == (c["batch"], c["n"]) and \
+                tuple(self.yc_d.shape) == (c["batch"], c["n"] + c["nh"] - 1)
+        elif self.kind == "polymul":
+            ok = tuple(self.a_d.shape) == (c["batch"], c["n"]) == tuple(self.b_d.shape) and \
+                tuple(self.c_d.shape) == (c["batch"], 2 * c["n"] - 1)
+        elif self.kind == "real":
+            ok = tuple(self.x_d.shape) == (c["batch"], c["n"]) and \
+                tuple(self.X_d.shape) == (c["batch"], c["n"] // 2 + 1)
+        else:
+            per = c["n"] * c["n"] if self.kind == "fft2d" else \
+                int(np.prod(c["shape"])) if self.kind == "fftnd" else c["n"]
+            ok = self.x_d.numel() == c["batch"] * per and \
+                self.y_d.numel() == self.x_d.numel() == self.z_d.numel()
+        if not ok:
+            raise ValueError(f"{self.name}: input buffers do not match the plan's sizes")
 
     def call(self, which: int):
         """The step's first (0: the dominant forward call) or second (1:
@@ -927,7 +949,9 @@ def sized_input(name: str, c: dict):
     if c["kind"] == "fft2d":
         return workloads.normal_complex((c["batch"], c["n"], c["n"]), c["seed"])
     if name == "c3":
-        return workloads.tones_plus_noise(c["n"], c["seed"]).reshape(1, -1)
+        # one tones-plus-noise row per transform of the (possibly reduced) batch
+        return np.stack([workloads.tones_plus_noise(c["n"], c["seed"] + r)
+                         for r in range(c["batch"])])
     return workloads.normal_complex((c["batch"], c["n"]), c["seed"])
 
 
