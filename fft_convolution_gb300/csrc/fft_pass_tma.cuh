@@ -116,8 +116,10 @@ template <typename T, int LOGL> struct TmaConfig {
   static constexpr int PAD = 32 / C >= 2 ? 32 / C : (sizeof(T) == 4 ? 2 : 1);
   static constexpr int RS = L + PAD;
   // Exchange layout: 64-byte rows of C columns take the swizzled view
-  // (SwzView, L slots per column), other widths the padded one.
-  static constexpr bool SWIZZLE = C * sizeof(V) == 64;
+  // (SwzView, L slots per column) when the transform starts with a radix-2
+  // stage (whose writes land at 2i + v: the pattern the swizzle balances);
+  // other tiles the padded one (which balances a first stage's 16i + v).
+  static constexpr bool SWIZZLE = C * sizeof(V) == 64 && P::R0 == 2;
   static constexpr int RAW_EX = SWIZZLE ? L * C : PassConfig<T, LOGL>::ROW_ELEMS * C;
   static constexpr int RAW_ELEMS = RAW_EX > C * RS ? RAW_EX : C * RS;
   static constexpr int MIN_BLOCKS = THREADS >= 1024 ? 1 : (THREADS >= 512 ? 2 : (THREADS >= 256 ? 3 : 4));
