@@ -258,7 +258,12 @@ __global__ void __launch_bounds__(kMixedThreads, sizeof(T) == 4 ? 4 : 2)
   // output), the last stage to global memory.  (Persistent blocks
   // prefetching the next rows into a third buffer measured slower: one
   // block fewer per SM.)
+  // Programmatic dependent launch, as the row kernel: wait for the
+  // previous kernel before the first stage reads global memory; the next
+  // kernel may be scheduled once this block has its data on chip.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   mixed_first_stage_any<DIR>(in + row0 * ms.N, cur, ms, rows);
+  asm volatile("griddepcontrol.launch_dependents;");
   __syncthreads();
   const int S = ms.nstages;  // >= 2 for every planned length (N > 64, R <= 16)
   for (int k = 1; k < S - 1; ++k) {
@@ -287,10 +292,18 @@ cudaError_t mixed_exec_t(const void *in, void *out, long long batch, const Mixed
   const long long grid = (batch + ms.F - 1) / ms.F;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const T scale = dir < 0 ? (T)1 : (T)(1.0 / ms.N);
-  kern<<<(unsigned)grid, kMixedThreads, smem, st>>>(static_cast<const V *>(in),
-                                                    static_cast<V *>(out), batch, ms,
-                                                    static_cast<const V *>(tw), scale);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kMixedThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<const V *>(in), static_cast<V *>(out), batch,
+                            ms, static_cast<const V *>(tw), scale);
 }
 
 }  // namespace

@@ -99,6 +99,10 @@ __global__ void __launch_bounds__(RealRowsConfig<T, LOGH>::THREADS, RealRowsBoun
   const long long r = (long long)blockIdx.x * C::F + f;
   const bool active = r < batch;
 
+  // Programmatic dependent launch, as the row kernel: wait for the
+  // previous kernel before reading, let the next one be scheduled once
+  // this block holds its data.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   V x[P::E];
   if (active) {
     const V *src = in + r * H;
@@ -108,6 +112,7 @@ __global__ void __launch_bounds__(RealRowsConfig<T, LOGH>::THREADS, RealRowsBoun
 #pragma unroll
     for (int w = 0; w < P::E; ++w) x[w] = make_c<V>((T)0, (T)0);
   }
+  asm volatile("griddepcontrol.launch_dependents;");
   const SmemView<V> sm{smem + f * C::ELEMS, 1};
   fft_on_chip<LOGH, -1, false, false>(x, t, sm);  // data came from global memory
 
@@ -155,6 +160,7 @@ __global__ void __launch_bounds__(RealRowsConfig<T, LOGH>::THREADS, RealRowsBoun
   const bool active = r < batch;
   const SmemView<V> sm{smem + f * C::ELEMS, 1};
 
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // as in r2c_rows_kernel
   V x[P::E];
   if (active) {
     const V *src = in + r * (H + 1);
@@ -174,6 +180,7 @@ __global__ void __launch_bounds__(RealRowsConfig<T, LOGH>::THREADS, RealRowsBoun
 #pragma unroll
     for (int w = 0; w < P::E; ++w) x[w] = make_c<V>((T)0, (T)0);
   }
+  asm volatile("griddepcontrol.launch_dependents;");
   __syncthreads();
   // Z_k = 2E_k + i (2 O_k), 2 O_k = W_N^{-k} (X_k - conj(X_{H-k})) (the
   // factor 1/2 joins 1/H at the store).
@@ -207,9 +214,17 @@ cudaError_t launch_real_rows_t(const void *in, void *out, long long batch, cudaS
   }
   const long long grid = (batch + C::F - 1) / C::F;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)grid, C::THREADS, C::SMEM, st>>>(static_cast<const V *>(in),
-                                                     static_cast<V *>(out), batch);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<const V *>(in), static_cast<V *>(out), batch);
 }
 
 template <typename T, bool FWD, int LOGH = 0>
