@@ -45,6 +45,7 @@ FFT_OPT_CLUSTER_LOG_MIN = 5
 FFT_OPT_ND_ROWS_T = 6
 FFT_OPT_COL_RADIX_LOG = 7
 FFT_OPT_ROWS_SHFL = 8
+FFT_OPT_PASS_SHFL = 9
 
 # Every symbol the header declares, with its ctypes signature.
 _VP, _I64, _INT, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t

@@ -212,7 +212,8 @@ int fft_debug_set_option(int option, int64_t value) {
     case FFT_OPT_NO_TMA:
     case FFT_OPT_NO_CLUSTER:
     case FFT_OPT_ND_ROWS_T:
-    case FFT_OPT_ROWS_SHFL: ok = value <= 1; break;
+    case FFT_OPT_ROWS_SHFL:
+    case FFT_OPT_PASS_SHFL: ok = value <= 1; break;
     case FFT_OPT_CLUSTER_LOG_MIN: ok = value >= 11 && value <= 13; break;
     case FFT_OPT_COL_RADIX_LOG: ok = value <= 3; break;
     default: ok = false;

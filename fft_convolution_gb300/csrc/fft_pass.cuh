@@ -219,7 +219,7 @@ cudaError_t launch_pass_t(Load load, Store store, int log_n, int log_m, int twid
   return cudaGetLastError();
 }
 
-template <typename T, int LOGL, int DIR>
+template <typename T, int LOGL, int DIR, bool SHFL = false>
 cudaError_t launch_pass_tma_t(const void *in, void *out, int log_n, int log_m, int twiddle,
                               long long batch, cudaStream_t st, int overlap = 0);
 template <typename T, int LOGL, int DIR>

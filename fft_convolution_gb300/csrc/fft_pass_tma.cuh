@@ -22,7 +22,10 @@
 
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "fft_pass.cuh"
+#include "fft_warp.cuh"
 
 namespace fftgb {
 
@@ -93,7 +96,9 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <typename T, int LOGL> struct TmaConfig {
+// SHFL: the warp-shuffle variant of the 512-point fp32 pass (one warp per
+// column, fft512_warp; see the kernel).
+template <typename T, int LOGL, bool SHFL = false> struct TmaConfig {
   using P = StagePlan<LOGL>;
   using V = vec2_t<T>;
   static constexpr int L = P::L;
@@ -120,14 +125,27 @@ template <typename T, int LOGL> struct TmaConfig {
   // stage (whose writes land at 2i + v: the pattern the swizzle balances);
   // other tiles the padded one (which balances a first stage's 16i + v).
   static constexpr bool SWIZZLE = C * sizeof(V) == 64 && P::R0 == 2;
-  static constexpr int RAW_EX = SWIZZLE ? L * C : PassConfig<T, LOGL>::ROW_ELEMS * C;
+  // The shuffle variant exists for one warp of 32 lanes x 16 values per
+  // column and 64-byte tile rows: fp32, L = 512, C = 8.
+  static constexpr bool SHFL_OK = std::is_same<T, float>::value && LOGL == 9 && C == 8;
+  static_assert(!SHFL || SHFL_OK, "warp-shuffle pass: fp32, 512 points, 8 columns");
+  static constexpr int RAW_EX =
+      SHFL || SWIZZLE ? L * C : PassConfig<T, LOGL>::ROW_ELEMS * C;
   static constexpr int RAW_ELEMS = RAW_EX > C * RS ? RAW_EX : C * RS;
   static constexpr int MIN_BLOCKS = THREADS >= 1024 ? 1 : (THREADS >= 512 ? 2 : (THREADS >= 256 ? 3 : 4));
+  // Buffers start on 128-byte boundaries (TMA), 1024-byte ones for the
+  // swizzled tiles of the shuffle variant (whose pattern follows address
+  // bits 4..8 within each 512-byte span).
+  static constexpr int ALIGN = SHFL ? 1024 : 128;
   static constexpr int BUF_ELEMS =
-      ((RAW_ELEMS * (int)sizeof(V) + 127) / 128) * 128 / (int)sizeof(V);
-  // Stage-twiddle table shared by the block's columns (rounded to 128 B).
+      ((RAW_ELEMS * (int)sizeof(V) + ALIGN - 1) / ALIGN) * ALIGN / (int)sizeof(V);
+  // Stage-twiddle table shared by the block's columns (rounded to 128 B);
+  // the shuffle variant forms its twiddles in registers.
   static constexpr int TW_ELEMS =
-      ((P::TW_ELEMS * (int)sizeof(V) + 127) / 128) * 128 / (int)sizeof(V);
+      SHFL ? 0 : ((P::TW_ELEMS * (int)sizeof(V) + 127) / 128) * 128 / (int)sizeof(V);
+  // Barriers and twiddle table before the buffers, rounded to ALIGN.
+  static constexpr int HEAD =
+      ((128 + TW_ELEMS * (int)sizeof(V) + ALIGN - 1) / ALIGN) * ALIGN;
   // Buffers per block: the loads run NBUF - 1 tiles ahead of the
   // computation.  Three (two tiles in flight) when that leaves room for two
   // blocks per SM, else two when three blocks still fit, else one (the
@@ -138,9 +156,13 @@ template <typename T, int LOGL> struct TmaConfig {
   static constexpr int NBUF = 3 * BUF_ELEMS * sizeof(V) <= 110 * 1024
                                   ? 3
                                   : (2 * BUF_ELEMS * sizeof(V) <= 76 * 1024 ? 2 : 1);
-  static constexpr size_t SMEM =
-      256 + (size_t)TW_ELEMS * sizeof(V) + NBUF * (size_t)BUF_ELEMS * sizeof(V);
+  static constexpr size_t SMEM = ALIGN + HEAD + NBUF * (size_t)BUF_ELEMS * sizeof(V);
 };
+
+// Byte offset within a tile of 64-byte rows as the TMA's 64-byte swizzle
+// places it: the 16-byte chunk index (bits 4..5) is XORed with bits 7..8
+// (the row index halved, mod 4), for a tile starting on a 512-byte boundary.
+__device__ __forceinline__ int swz64(int o) { return o ^ (((o >> 7) & 3) << 4); }
 
 struct TmaGeom {
   int log_n;
@@ -163,23 +185,33 @@ inline int log2_pow2(long long v) {
   return l;
 }
 
-template <typename T, int LOGL, int DIR>
-__global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL>::MIN_BLOCKS)
+// SHFL (fp32, L = 512, 8 columns; FFT_OPT_PASS_SHFL): warp w transforms
+// column w of the tile by fft512_warp -- lane l holds rows l + 32 r --
+// exchanging by __shfl_xor_sync instead of through shared memory.  The tile
+// arrives and leaves with the TMA's 64-byte swizzle, which keeps a warp's
+// accesses to one column within 4 shared-memory wavefronts (16 without it);
+// each warp reads and writes only its own column's slots, so two block
+// barriers per tile remain (after the loads, before the store) instead of
+// six.
+template <typename T, int LOGL, int DIR, bool SHFL = false>
+__global__ void __launch_bounds__(TmaConfig<T, LOGL, SHFL>::THREADS,
+                                  TmaConfig<T, LOGL, SHFL>::MIN_BLOCKS)
     fft_pass_tma_kernel(const __grid_constant__ CUtensorMap tin,
                         const __grid_constant__ CUtensorMap tout, vec2_t<T> *out_linear,
                         TmaGeom g, int *status) {
-  using Cfg = TmaConfig<T, LOGL>;
+  using Cfg = TmaConfig<T, LOGL, SHFL>;
   using P = StagePlan<LOGL>;
   using V = vec2_t<T>;
   constexpr int C = Cfg::C;
   constexpr int L = Cfg::L;
+  constexpr unsigned A = Cfg::ALIGN;
   extern __shared__ __align__(128) unsigned char smem_tma[];
-  // TMA destinations must be 128-byte aligned: round the base up (the
-  // allocation carries 128 spare bytes for this).
-  unsigned char *base = smem_tma + ((128u - (smem_addr(smem_tma) & 127u)) & 127u);
+  // TMA destinations must be 128-byte aligned (1024 for the swizzled
+  // tiles): round the base up (the allocation carries ALIGN spare bytes).
+  unsigned char *base = smem_tma + ((A - (smem_addr(smem_tma) & (A - 1))) & (A - 1));
   uint64_t *bar = reinterpret_cast<uint64_t *>(base);
   V *const twt = reinterpret_cast<V *>(base + 128);
-  V *const buf0 = twt + Cfg::TW_ELEMS;
+  V *const buf0 = reinterpret_cast<V *>(base + Cfg::HEAD);
 
   const int tid = threadIdx.x;
   const int c = tid % C;
@@ -204,7 +236,7 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
     for (int j = 0; j < NB; ++j) mbar_init(&bar[j], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  fill_twiddle_table<LOGL, DIR>(twt, tid, Cfg::THREADS);
+  if constexpr (!SHFL) fill_twiddle_table<LOGL, DIR>(twt, tid, Cfg::THREADS);
   __syncthreads();
   // When launched with programmatic dependent launch (after another pass)
   // the set-up above overlaps the previous kernel's tail; every global
@@ -247,6 +279,68 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL>::THREADS, TmaConfig<T, LOGL
       }
     }
     const bool ok = mbar_wait(&bar[s], (uint32_t)(k / NB) & 1u);
+
+    if constexpr (SHFL) {
+      const int lane = tid & 31, col = tid >> 5;
+      unsigned char *const cb = reinterpret_cast<unsigned char *>(cur);
+      V x[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r)
+        x[r] = *reinterpret_cast<const V *>(cb + swz64(((lane + 32 * r) << 6) + (col << 3)));
+      if (__syncthreads_or(!ok)) {
+        if (tid == 0) {
+          atomicExch(status, kDeviceErrorTimeout);
+#pragma unroll
+          for (int j = 1; j < NB; ++j)
+            if (tile + (long long)j * gridDim.x < g.total_tiles)
+              mbar_wait(&bar[(k + j) % NB], (uint32_t)((k + j) / NB) & 1u);
+        }
+        break;
+      }
+      const long long b = tile >> g.log_tpb;
+      const long long i0 = (tile & (g.tiles_per_batch - 1)) * C;  // the tile's first column
+      if (g.twiddle && g.log_m > 0) {
+        const long long p = (i0 + col) & ((1LL << g.log_m) - 1);
+        const int log_lm = g.log_m + LOGL;
+        apply_geometric<16>(x, twiddle<DIR>(p * lane, log_lm, T()),
+                            twiddle<DIR>(p * 32, log_lm, T()));
+      }
+      fft512_warp<DIR>(x, lane);  // x[c] = output row (lane >> 1) + 16 c + 256 (lane & 1)
+      if constexpr (DIR > 0) {
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) x[c2] = c_scale(x[c2], (T)(1.0 / L));
+      }
+      const int v0 = (lane >> 1) + 256 * (lane & 1);
+      if (g.log_m == 0) {
+        // Column col staged contiguously at col * RS, one bulk copy each.
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) cur[col * Cfg::RS + v0 + 16 * c2] = x[c2];
+        fence_async_smem();
+        __syncthreads();
+        if (tid < C) {
+          V *dst = out_linear + b * (1LL << g.log_n) + (i0 + tid) * L;
+          bulk_store(dst, cur + tid * Cfg::RS, (uint32_t)(L * sizeof(V)));
+          bulk_commit();
+        }
+      } else {
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2)
+          *reinterpret_cast<V *>(cb + swz64(((v0 + 16 * c2) << 6) + (col << 3))) = x[c2];
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+          const long long m = 1LL << g.log_m;
+          const long long q = i0 >> g.log_m;
+          const long long p0 = i0 & (m - 1);
+#pragma unroll
+          for (int kb = 0; kb < Cfg::BOXES; ++kb)
+            tma_store_4d(&tout, cur + kb * Cfg::ROWS_PER_BOX * C, (int)(2 * p0),
+                         kb * Cfg::ROWS_PER_BOX, (int)q, (int)b);
+          bulk_commit();
+        }
+      }
+      continue;
+    }
 
     const long long b = tile >> g.log_tpb;
     const long long i = (tile & (g.tiles_per_batch - 1)) * C + c;
@@ -364,10 +458,15 @@ inline int sm_count() {
 // launched) when the shape does not suit it: tiles narrower than 2 columns
 // (16-byte TMA rows), fewer columns than one tile, output blocks shorter than
 // a tile, FFT_OPT_NO_TMA set, or no driver entry point.
-template <typename T, int LOGL, int DIR>
+template <typename T, int LOGL, int DIR, bool SHFL>
 cudaError_t launch_pass_tma_t(const void *in, void *out, int log_n, int log_m, int twiddle,
                               long long batch, cudaStream_t st, int overlap) {
-  using Cfg = TmaConfig<T, LOGL>;
+  using Cfg = TmaConfig<T, LOGL, SHFL>;
+  if constexpr (!SHFL && TmaConfig<T, LOGL>::SHFL_OK) {
+    if (option(FFT_OPT_PASS_SHFL) == 1)
+      return launch_pass_tma_t<T, LOGL, DIR, true>(in, out, log_n, log_m, twiddle, batch, st,
+                                                   overlap);
+  }
   if constexpr (Cfg::C < 2 || LOGL < 4) {
     return cudaErrorNotSupported;
   } else {
@@ -386,11 +485,13 @@ cudaError_t launch_pass_tma_t(const void *in, void *out, int log_n, int log_m, i
     // Input: [batch][L rows][cols] complex, as scalars (re, im) on the
     // innermost axis.
     CUtensorMap tin, tout;
+    // The shuffle variant's tiles (64-byte rows) use the 64-byte swizzle.
+    const CUtensorMapSwizzle swz = SHFL ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE;
     const cuuint64_t din[3] = {2ull * (cuuint64_t)cols, (cuuint64_t)Cfg::L, (cuuint64_t)batch};
     const cuuint64_t sin_[2] = {(cuuint64_t)cols * es, n * es};
     const cuuint32_t box3[3] = {2u * Cfg::C, (cuuint32_t)Cfg::ROWS_PER_BOX, 1u};
     if (enc(&tin, dt, 3, const_cast<void *>(in), din, sin_, box3, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     if (log_m > 0) {
@@ -401,13 +502,13 @@ cudaError_t launch_pass_tma_t(const void *in, void *out, int log_n, int log_m, i
       const cuuint64_t sout[3] = {m * es, (cuuint64_t)Cfg::L * m * es, n * es};
       const cuuint32_t box4[4] = {2u * Cfg::C, (cuuint32_t)Cfg::ROWS_PER_BOX, 1u, 1u};
       if (enc(&tout, dt, 4, out, dout, sout, box4, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     } else {
       tout = tin;  // unused: the first pass stores linearly
     }
-    auto kern = fft_pass_tma_kernel<T, LOGL, DIR>;
+    auto kern = fft_pass_tma_kernel<T, LOGL, DIR, SHFL>;
     static DeviceOnce attr_set;
     const cudaError_t attr = smem_limit_once((const void *)kern, Cfg::SMEM, attr_set);
     if (attr != cudaSuccess) return attr;

@@ -88,7 +88,7 @@ int cuda_fail(cudaError_t e) {
 // Process-wide test / tuning options (fft_debug_set_option); -1 = the
 // library's own choice.
 static std::atomic<long long> g_options[kNumOptions] = {
-    {-1}, {-1}, {-1}, {-1}, {-1}, {-1}, {-1}, {-1}, {-1}};
+    {-1}, {-1}, {-1}, {-1}, {-1}, {-1}, {-1}, {-1}, {-1}, {-1}};
 
 long long option(int which) {
   return which > 0 && which < kNumOptions ? g_options[which].load(std::memory_order_relaxed) : -1;

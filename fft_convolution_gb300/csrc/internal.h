@@ -35,7 +35,7 @@ struct DeviceOnce {
 // Process-wide test / tuning options of fft_debug_set_option (FFT_OPT_*
 // in the public header; fft_plan.cu): the current value, -1 for the
 // library's own choice.
-constexpr int kNumOptions = 9;
+constexpr int kNumOptions = 10;
 long long option(int which);
 bool set_option(int which, long long value);
 

@@ -430,6 +430,10 @@ int fft_debug_cluster_timeout(void *data, int64_t polls, void *stream);
 #define FFT_OPT_ROWS_SHFL 8       /* launch: 1 = 512-point on-chip transforms exchange data
                                      between stages by warp shuffles (one warp per transform)
                                      instead of shared memory; own choice 0 */
+#define FFT_OPT_PASS_SHFL 9       /* launch: 1 = fp32 HBM passes of 512-point columns give each
+                                     column to one warp and exchange by warp shuffles (tiles
+                                     loaded and stored with the TMA's 64-byte swizzle);
+                                     0 = shared-memory exchanges */
 int fft_debug_set_option(int option, int64_t value);
 
 /* Last status recorded on this host thread by a call that returns a

@@ -154,6 +154,53 @@ def test_rows_warp_shuffle_512(fg, opt, dtype, batch):
     assert rel_rows(z, oracle.ifft(y.astype(np.complex128))).max() <= tol(dtype, n)
 
 
+# 512-point fp32 HBM passes with the warp-shuffle exchange (FFT_OPT_PASS_SHFL):
+# one warp per column, tiles moved with the TMA's 64-byte swizzle.  Splits put
+# the 512-point pass first (m = 1, linear bulk stores), in the middle and last
+# (twiddled, TMA stores), with blocks of m down to one tile (m = 8); the 2D
+# shapes run it as the column pass (folded and not), in and out of place.
+@pytest.mark.parametrize("logn,split,batch", [
+    (18, "9,9", 2), (21, "3,9,9", 1), (13, "4,9", 3), (12, "3,9", 2), (17, "9,8", 1),
+    (22, "9,9,4", 1)])
+def test_pass_warp_shuffle(fg, opt, logn, split, batch):
+    opt("PASS_SPLIT", split)
+    opt("PASS_SHFL", 1)
+    n = 1 << logn
+    x = workloads.normal_complex((batch, n), 6400 + logn, np.complex64)
+    ref = oracle.fft(x.astype(np.complex128))
+    y = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, F32)
+    assert rel_rows(y, ref).max() <= tol(F32, n)
+    y2 = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, F32, inplace=True)
+    assert rel_rows(y2, ref).max() <= tol(F32, n)
+    z = run_plan(fg, y, n, batch, 1, fg.FFT_INVERSE, F32)
+    assert rel_rows(z, oracle.ifft(y.astype(np.complex128))).max() <= tol(F32, n)
+    assert fg.fft_device_status(stream()) == 0
+
+
+@pytest.mark.parametrize("shape,batch", [((2048, 2048), 2), ((512, 512), 3), ((512, 256), 2),
+                                         ((1024, 64), 2)])
+def test_pass_warp_shuffle_2d(fg, opt, shape, batch):
+    opt("PASS_SHFL", 1)
+    x = workloads.normal_complex((batch,) + shape, 6500 + sum(shape), np.complex64)
+    npts = int(np.prod(shape))
+    p = fg.Plan(0, batch, direction=fg.FFT_FORWARD, dtype=F32, shape=shape)
+    pi = fg.Plan(0, batch, direction=fg.FFT_INVERSE, dtype=F32, shape=shape)
+    xd = torch.from_numpy(x).cuda()
+    yd, zd = torch.empty_like(xd), torch.empty_like(xd)
+    p.exec(xd, yd)
+    pi.exec(yd, zd)
+    torch.cuda.synchronize()
+    ref = oracle.fftn(x.astype(np.complex128), 2)
+    assert rel_rows(yd.cpu().numpy(), ref).max() <= tol(F32, npts)
+    assert rel_rows(zd.cpu().numpy(), x).max() <= 2 * tol(F32, npts)
+    p.exec(xd, xd)
+    torch.cuda.synchronize()
+    assert rel_rows(xd.cpu().numpy(), ref).max() <= tol(F32, npts)
+    assert fg.fft_device_status(stream()) == 0
+    p.close()
+    pi.close()
+
+
 # --- passes whose on-chip length (2^11 .. 2^13) is split over a cluster --------
 
 @pytest.mark.parametrize("dtype,logn,split,batch", [
