@@ -111,8 +111,8 @@ def workload_info(name: str, pass_log: int = 9, passes=None):
         info.update(passes=passes, bytes_per_step=directions * (passes or 1) * 2 * arr,
                     ideal_bytes_per_step=directions * 2 * arr)
         if n & (n - 1) == 0 and log2i(n) > 14:
-            # the survey's minimum for a transform beyond one block: a 2-pass
-            # four-step (every element read and written twice)
+            # the least HBM traffic for a transform beyond one block: a
+            # 2-pass four-step (every element read and written twice)
             info.update(min_passes=2, min_bytes_per_step=directions * 2 * 2 * arr)
         return info
     if c["kind"] == "real":
@@ -791,7 +791,7 @@ def measure(name, args, fg, torch, dev, world, barrier, with_cpu):
                 "launch_ms": round(dom_ms, 4),
                 "inverse_launch_ms": round(statistics.mean(inv_ms), 4) if inv_ms else None}
     if info.get("min_bytes_per_step"):
-        # Against the survey's 2-pass minimum for this length, next to the
+        # Against the 2-pass four-step minimum for this length, next to the
         # chosen plan's own pass count.
         mb = info["min_bytes_per_step"] / info["directions"]
         roofline.update(min_passes=info["min_passes"], min_bytes_per_launch=mb,

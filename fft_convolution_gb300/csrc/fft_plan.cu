@@ -200,10 +200,10 @@ static fft_plan *plan_real(int64_t n, int64_t batch, int direction, int cdtype) 
 }
 
 // The stages of a mixed-radix plan of length n: the odd factors first (a 3
-// and a 5 together as radix 15 while both remain, then 3s, 5s, 7s: short
-// blocks m while the stride N/R is odd), then the power of two as one 2, 4
-// or 8 and radix-16 stages.  False if n has a prime factor above 7 or needs
-// more than 16 stages.
+// and a 5 together as radix 15 while both remain, then 3s, 5s, 7s, 11s, 13s:
+// short blocks m while the stride N/R is odd), then the power of two as one
+// 2, 4 or 8 and radix-16 stages.  False if n has a prime factor above 13 or
+// needs more than 16 stages.
 static bool mixed_stages(int64_t n, int elem, MixedStages *ms) {
   int radix[64], k = 0, a = 0;
   int64_t r = n;
@@ -217,7 +217,7 @@ static bool mixed_stages(int64_t n, int elem, MixedStages *ms) {
     r /= 15;
     radix[k++] = 15;
   }
-  const int odd[3] = {3, 5, 7};
+  const int odd[5] = {3, 5, 7, 11, 13};
   for (int f : odd)
     while (r % f == 0 && k < 64) {
       r /= f;
@@ -278,9 +278,11 @@ static void mixed_twiddles(const MixedStages &ms, bool f64, void *host) {
   }
 }
 
-static bool is_smooth_2357(int64_t n) {
-  const int f[4] = {2, 3, 5, 7};
-  for (int k = 0; k < 4; ++k)
+// True when every prime factor of n is at most 13 (the mixed-radix kernel's
+// radices).
+static bool is_smooth_13(int64_t n) {
+  const int f[6] = {2, 3, 5, 7, 11, 13};
+  for (int k = 0; k < 6; ++k)
     while (n % f[k] == 0) n /= f[k];
   return n == 1;
 }
@@ -355,7 +357,7 @@ static fft_plan *plan_four_step(int64_t n, int64_t n1, int64_t batch, int direct
 
 // Plans a 1D length that is not a power of two (the caller validated the
 // other arguments): the direct DFT for n <= kDirectDftMax; mixed radix on
-// chip for longer lengths whose prime factors are 2, 3, 5, 7 (up to
+// chip for longer lengths whose prime factors are 2, 3, 5, 7, 11, 13 (up to
 // kMixedMaxF32 / kMixedMaxF64); Bluestein for the rest, whose chirp and
 // filter spectrum are computed here (on the legacy default stream, waited
 // for before returning).
@@ -404,7 +406,7 @@ static fft_plan *plan_any_length(int64_t n, int64_t batch, int direction, int dt
     return p;
   }
   const int64_t mixed_max = dtype == FFT_C2C_F32 ? kMixedMaxF32 : kMixedMaxF64;
-  if (n > mixed_max && is_smooth_2357(n)) {
+  if (n > mixed_max && is_smooth_13(n)) {
     // Smooth but longer than one block: the four-step split N = N1 N2 with
     // both factors on chip, N1 the divisor closest to sqrt(N).
     int64_t n1 = 0;

@@ -171,7 +171,7 @@ cudaError_t dft_small_f64(const void *in, void *out, int N, long long batch, int
                           cudaStream_t st);
 
 // Mixed-radix on-chip transforms (mixed_*.cu): stage k has radix radix[k]
-// (2, 3, 4, 5, 7, 8 or 16) and block length m[k] (the product of the
+// (2, 3, 4, 5, 7, 8, 11, 13, 15 or 16) and block length m[k] (the product of the
 // radices before it); its forward twiddles W_{R m}^{p u} sit at
 // tw_off[k] + (u - 1) m + p of the plan's table.  A block holds F transforms.
 struct MixedStages {

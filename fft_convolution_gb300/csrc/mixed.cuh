@@ -1,4 +1,5 @@
-// mixed.cuh -- on-chip mixed-radix transforms for lengths N = 2^a 3^b 5^c 7^d.
+// mixed.cuh -- on-chip mixed-radix transforms for lengths
+// N = 2^a 3^b 5^c 7^d 11^e 13^f.
 //
 // "FFT on GPU" (section Algorithm per signal Length) names the mixed-radix
 // FFT for lengths such as 12 = 3 * 4 beside the power-of-two one.  The
@@ -14,8 +15,8 @@
 // applying the stage twiddles (read from a per-plan table of the forward
 // roots, conjugated for the inverse), running the radix-R DFT in registers
 // and storing the R outputs.  Radices 2, 4, 8, 16 use the power-of-two
-// register DFTs, 15 the prime-factor split into 3 and 5 (dft15); 3, 5, 7
-// pair x_u with x_{R-u}:
+// register DFTs, 15 the prime-factor split into 3 and 5 (dft15); 3, 5, 7,
+// 11 and 13 pair x_u with x_{R-u}:
 //   X_v = x_0 + sum_{u<=(R-1)/2} [(x_u + x_{R-u}) cos(2 pi uv/R)
 //                                 + DIR i (x_u - x_{R-u}) sin(2 pi uv/R)],
 // and X_{R-v} the same with the sine term negated.
@@ -29,25 +30,54 @@ namespace {
 
 constexpr int kMixedThreads = 256;
 
-// cos(2 pi k / R), sin(2 pi k / R) for R = 3, 5, 7, k <= (R-1)/2.
+// cos(2 pi k / R), sin(2 pi k / R) for R = 3, 5, 7, 11, 13, 1 <= k <= (R-1)/2
+// (36 significant digits, rounded to the element type at compile time).
 __host__ __device__ constexpr double odd_cos(int R, int k) {
-  return R == 3   ? -0.5
-         : R == 5 ? (k == 1 ? 0.309016994374947424102293417182819059
-                            : -0.809016994374947424102293417182819059)
-                  : (k == 1   ? 0.623489801858733530525004884004239811
-                     : k == 2 ? -0.222520933956314404288902564496794759
-                              : -0.900968867902419126236102319507445051);
+  switch (R * 16 + k) {
+    case 3 * 16 + 1: return -0.5;
+    case 5 * 16 + 1: return 0.309016994374947424102293417182819059;
+    case 5 * 16 + 2: return -0.809016994374947424102293417182819059;
+    case 7 * 16 + 1: return 0.623489801858733530525004884004239811;
+    case 7 * 16 + 2: return -0.222520933956314404288902564496794759;
+    case 7 * 16 + 3: return -0.900968867902419126236102319507445051;
+    case 11 * 16 + 1: return 0.841253532831181168861811648919367718;
+    case 11 * 16 + 2: return 0.415415013001886425529274149229623204;
+    case 11 * 16 + 3: return -0.142314838273285140443792668616369669;
+    case 11 * 16 + 4: return -0.654860733945285064056925072466293553;
+    case 11 * 16 + 5: return -0.959492973614497389890368057066327699;
+    case 13 * 16 + 1: return 0.885456025653209895900375522015098879;
+    case 13 * 16 + 2: return 0.568064746731155802511807559127516624;
+    case 13 * 16 + 3: return 0.120536680255323053349067687452543582;
+    case 13 * 16 + 4: return -0.354604887042535625969637892600018474;
+    case 13 * 16 + 5: return -0.748510748171101098634630599701351384;
+    case 13 * 16 + 6: return -0.970941817426052027156982276293789227;
+    default: return 0.0;
+  }
 }
 __host__ __device__ constexpr double odd_sin(int R, int k) {
-  return R == 3   ? 0.866025403784438646763723170752936183
-         : R == 5 ? (k == 1 ? 0.951056516295153572116439333379382143
-                            : 0.587785252292473129168705954639072769)
-                  : (k == 1   ? 0.781831482468029808708444526674057750
-                     : k == 2 ? 0.974927912181823607018131682993931217
-                              : 0.433883739117558120475768332848358755);
+  switch (R * 16 + k) {
+    case 3 * 16 + 1: return 0.866025403784438646763723170752936183;
+    case 5 * 16 + 1: return 0.951056516295153572116439333379382143;
+    case 5 * 16 + 2: return 0.587785252292473129168705954639072769;
+    case 7 * 16 + 1: return 0.781831482468029808708444526674057750;
+    case 7 * 16 + 2: return 0.974927912181823607018131682993931217;
+    case 7 * 16 + 3: return 0.433883739117558120475768332848358755;
+    case 11 * 16 + 1: return 0.540640817455597582107635954318691695;
+    case 11 * 16 + 2: return 0.909631995354518371411715383079028460;
+    case 11 * 16 + 3: return 0.989821441880932732376092037776718787;
+    case 11 * 16 + 4: return 0.755749574354258283774035843972344420;
+    case 11 * 16 + 5: return 0.281732556841429697711417915346616899;
+    case 13 * 16 + 1: return 0.464723172043768545656015335133104778;
+    case 13 * 16 + 2: return 0.822983865893656394579617423439381991;
+    case 13 * 16 + 3: return 0.992708874098053992800751649492520179;
+    case 13 * 16 + 4: return 0.935016242685414823439784599837830729;
+    case 13 * 16 + 5: return 0.663122658240795202376785492666766280;
+    case 13 * 16 + 6: return 0.239315664287557767148753726260211895;
+    default: return 0.0;
+  }
 }
 
-// In-register DFT of odd prime length R (3, 5, 7), natural order.
+// In-register DFT of odd prime length R (3, 5, 7, 11, 13), natural order.
 template <int R, int DIR, typename V> __device__ __forceinline__ void dft_odd(V *x) {
   using T = decltype(V::x);
   constexpr int H = (R - 1) / 2;
@@ -110,7 +140,7 @@ template <int DIR, typename V> __device__ __forceinline__ void dft15(V *x) {
 }
 
 template <int R, int DIR, typename V> __device__ __forceinline__ void dft_any(V *x) {
-  if constexpr (R == 3 || R == 5 || R == 7) dft_odd<R, DIR>(x);
+  if constexpr (R == 3 || R == 5 || R == 7 || R == 11 || R == 13) dft_odd<R, DIR>(x);
   else if constexpr (R == 15) dft15<DIR>(x);
   else dft_reg<R, DIR>(x);
 }
@@ -182,6 +212,8 @@ __device__ __forceinline__ void mixed_stage_any(const V *src, V *dst, const Mixe
     case 4: mixed_stage<4, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
     case 5: mixed_stage<5, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
     case 7: mixed_stage<7, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
+    case 11: mixed_stage<11, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
+    case 13: mixed_stage<13, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
     case 8: mixed_stage<8, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
     case 15: mixed_stage<15, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
     default: mixed_stage<16, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
@@ -235,6 +267,8 @@ __device__ __forceinline__ void mixed_first_stage_any(const V *g, V *dst, const 
     case 4: mixed_first_stage<4, DIR>(g, dst, ms, rows); break;
     case 5: mixed_first_stage<5, DIR>(g, dst, ms, rows); break;
     case 7: mixed_first_stage<7, DIR>(g, dst, ms, rows); break;
+    case 11: mixed_first_stage<11, DIR>(g, dst, ms, rows); break;
+    case 13: mixed_first_stage<13, DIR>(g, dst, ms, rows); break;
     case 8: mixed_first_stage<8, DIR>(g, dst, ms, rows); break;
     case 15: mixed_first_stage<15, DIR>(g, dst, ms, rows); break;
     default: mixed_first_stage<16, DIR>(g, dst, ms, rows); break;

@@ -29,9 +29,9 @@ enum Kind {
   KIND_REAL_ROWS = 5,  // real, N = 2H with H a power of two on chip: one kernel
   KIND_REAL_EVEN = 6,  // real, other even N: complex plan of length N/2 + pre/post kernel
   KIND_REAL_ODD = 7,   // real, odd N: complex plan of length N + widen/narrow kernels
-  KIND_MIXED = 8,      // N = 2^a 3^b 5^c 7^d (not a power of two) on chip
+  KIND_MIXED = 8,      // N = 2^a 3^b 5^c 7^d 11^e 13^f (not a power of two) on chip
   KIND_ND_ANY = 9,     // 2D / 3D with a side that is not a power of two (or beyond KIND_ND's limits)
-  KIND_FOUR_STEP = 10  // N = N1 N2 (2, 3, 5, 7 only) beyond one block: two mixed-radix plans
+  KIND_FOUR_STEP = 10  // N = N1 N2 (factors 2 .. 13 only) beyond one block: two mixed-radix plans
 };
 
 // Lengths that are not powers of two: the direct DFT up to this length,

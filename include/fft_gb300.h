@@ -5,7 +5,8 @@
  *   - batched 1D complex-to-complex transforms of any length, forward
  *     (unscaled) and inverse (scaled by 1/N), fp32 or fp64: powers of two on
  *     chip or in 2-4 HBM passes; other lengths by the direct DFT (N <= 64),
- *     mixed radix (prime factors 2, 3, 5, 7; four-step beyond one block) or
+ *     mixed radix (prime factors 2, 3, 5, 7, 11, 13; four-step beyond one
+ *     block) or
  *     Bluestein;
  *   - transforms of real sequences (half spectrum out / in, any length);
  *   - separable 2D and 3D transforms of any sides (rows, then columns, ...);

@@ -61,7 +61,7 @@ C2C = [  # (n, batch, dtype)
     (64, 37, 0), (4096, 3, 0), (8192, 2, 1), (1 << 16, 3, 0), (1 << 15, 2, 1),   # pow2 rows / passes
     (12, 37, 0), (63, 5, 1),                                                    # direct DFT
     (100, 37, 0), (3000, 3, 0), (6144, 2, 1),                                   # mixed radix
-    (1009, 3, 0), (10007, 2, 0), (4095, 2, 1),                                  # Bluestein
+    (1009, 3, 0), (10007, 2, 0), (4091, 2, 1),                                  # Bluestein
 ]
 
 

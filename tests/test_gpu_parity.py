@@ -447,12 +447,12 @@ def test_direct_dft_short_lengths(fg, dtype, n):
     assert rel_rows(z, x).max() <= 2 * tol(dtype, n)
 
 
-@pytest.mark.parametrize("dtype,n", [(F32, 65), (F32, 130), (F32, 1009), (F32, 3001), (F32, 8191),
-                                     (F64, 65), (F64, 1009), (F64, 4095),
+@pytest.mark.parametrize("dtype,n", [(F32, 67), (F32, 134), (F32, 1009), (F32, 3001), (F32, 8191),
+                                     (F64, 67), (F64, 1009), (F64, 4091),
                                      (F32, 10007), (F64, 5003), (F64, 9999)])
 def test_bluestein(fg, dtype, n):
-    # n <= 8191 fp32 / 4095 fp64 fuse the whole convolution on chip; the rest
-    # take the multi-pass path.
+    # Lengths with a prime factor above 13.  n <= 8191 fp32 / 4096 fp64 fuse
+    # the whole convolution on chip; the rest take the multi-pass path.
     batch = 3
     x = workloads.normal_complex((batch, n), 5300 + n, NP[dtype])
     y = run_plan(fg, x, n, batch, 1, fg.FFT_FORWARD, dtype)
@@ -463,12 +463,15 @@ def test_bluestein(fg, dtype, n):
     assert rel_rows(z, x).max() <= 2 * t
 
 
-# Lengths whose prime factors are 2, 3, 5, 7 (above the direct-DFT range):
-# mixed-radix stages on chip, one kernel.
+# Lengths whose prime factors are 2, 3, 5, 7, 11, 13 (above the direct-DFT
+# range): mixed-radix stages on chip, one kernel.
 @pytest.mark.parametrize("dtype,n", [(F32, 72), (F32, 96), (F32, 100), (F32, 120), (F32, 210),
                                      (F32, 243), (F32, 343), (F32, 625), (F32, 1000), (F32, 3000),
                                      (F32, 5040), (F32, 11025), (F32, 12288),
-                                     (F64, 72), (F64, 210), (F64, 1000), (F64, 3000), (F64, 6144)])
+                                     (F32, 65), (F32, 121), (F32, 143), (F32, 169), (F32, 1001),
+                                     (F32, 1331), (F32, 2197), (F32, 6656), (F32, 11264),
+                                     (F64, 72), (F64, 210), (F64, 1000), (F64, 3000), (F64, 6144),
+                                     (F64, 143), (F64, 4004), (F64, 2197)])
 def test_mixed_radix(fg, dtype, n):
     batch = 3 if n > 2048 else 37   # ragged against the transforms per block
     x = workloads.normal_complex((batch, n), 5400 + n, NP[dtype])
@@ -490,7 +493,8 @@ def test_mixed_radix(fg, dtype, n):
 # transforms, transpose); 16 sampled bins of two rows against the direct sum,
 # Parseval, the inverse round trip, and the in-place form.
 @pytest.mark.parametrize("dtype,n", [(F32, 12800), (F32, 100000), (F32, 59049), (F32, 78125),
-                                     (F32, 53760), (F64, 24576), (F64, 10000)])
+                                     (F32, 53760), (F32, 15488), (F32, 28561), (F64, 24576),
+                                     (F64, 10000), (F64, 8788)])
 def test_four_step_smooth(fg, dtype, n):
     batch = 3
     x = workloads.normal_complex((batch, n), 5500 + n % 997, NP[dtype])
