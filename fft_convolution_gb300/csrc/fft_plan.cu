@@ -201,11 +201,15 @@ static fft_plan *plan_real(int64_t n, int64_t batch, int direction, int cdtype) 
 
 // The stages of a mixed-radix plan of length n: the odd factors first (a 3
 // and a 5 together as radix 15 while both remain, then 3s, 5s, 7s, 11s, 13s:
-// short blocks m while the stride N/R is odd), then the power of two as one
-// 2, 4 or 8 and radix-16 stages.  False if n has a prime factor above 13 or
-// needs more than 16 stages.
+// short blocks m while the stride N/R is odd), then the power of two as
+// radix-16 stages.  The power of two left over (2, 4 or 8 = 4 * 2) joins
+// remaining odd primes as prime-factor radices -- 4 with a 5 or a 3 (20,
+// 12), 2 with a 5, a 3 or a 7 (10, 6, 14) -- placed after the odd stages,
+// one stage fewer per pairing; what finds no partner stays one 2, 4 or 8
+// stage.  False if n has a prime factor above 13 or needs more than 16
+// stages.
 static bool mixed_stages(int64_t n, int elem, MixedStages *ms) {
-  int radix[64], k = 0, a = 0;
+  int odd[64], no = 0, a = 0;
   int64_t r = n;
   while (r % 2 == 0) {
     r /= 2;
@@ -213,19 +217,50 @@ static bool mixed_stages(int64_t n, int elem, MixedStages *ms) {
   }
   // A 3 and a 5 merge into one radix-15 stage (an in-register prime-factor
   // DFT: one shared-memory round trip fewer), first.
-  while (r % 15 == 0 && k < 64) {
+  while (r % 15 == 0 && no < 64) {
     r /= 15;
-    radix[k++] = 15;
+    odd[no++] = 15;
   }
-  const int odd[5] = {3, 5, 7, 11, 13};
-  for (int f : odd)
-    while (r % f == 0 && k < 64) {
+  const int primes[5] = {3, 5, 7, 11, 13};
+  for (int f : primes)
+    while (r % f == 0 && no < 64) {
       r /= f;
-      radix[k++] = f;
+      odd[no++] = f;
     }
   if (r != 1) return false;
-  if (a % 4) radix[k++] = 1 << (a % 4);
-  for (int j = 0; j < a / 4; ++j) radix[k++] = 16;
+  int rest2[2], nr = 0;
+  if (a % 4 == 3) {
+    rest2[nr++] = 4;
+    rest2[nr++] = 2;
+  } else if (a % 4) {
+    rest2[nr++] = 1 << (a % 4);
+  }
+  int pfa[2], np = 0, single2 = 1;
+  for (int i = 0; i < nr; ++i) {
+    const int q = rest2[i];
+    const int partners[3] = {5, 3, 7};
+    int at = -1;
+    for (int w = 0; w < 3 && at < 0; ++w) {
+      if (partners[w] == 7 && q != 2) continue;  // 28 values: too many registers
+      for (int j = 0; j < no; ++j)
+        if (odd[j] == partners[w]) {
+          at = j;
+          break;
+        }
+    }
+    if (at >= 0) {
+      pfa[np++] = q * odd[at];
+      odd[at] = 0;
+    } else {
+      single2 *= q;
+    }
+  }
+  int radix[64], k = 0;
+  for (int j = 0; j < no && k < 64; ++j)
+    if (odd[j]) radix[k++] = odd[j];
+  for (int j = 0; j < np && k < 64; ++j) radix[k++] = pfa[j];
+  if (single2 > 1 && k < 64) radix[k++] = single2;
+  for (int j = 0; j < a / 4 && k < 64; ++j) radix[k++] = 16;
   if (k > 16) return false;
   memset(ms, 0, sizeof(*ms));
   ms->N = (int)n;

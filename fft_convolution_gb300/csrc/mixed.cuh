@@ -15,8 +15,8 @@
 // applying the stage twiddles (read from a per-plan table of the forward
 // roots, conjugated for the inverse), running the radix-R DFT in registers
 // and storing the R outputs.  Radices 2, 4, 8, 16 use the power-of-two
-// register DFTs, 15 the prime-factor split into 3 and 5 (dft15); 3, 5, 7,
-// 11 and 13 pair x_u with x_{R-u}:
+// register DFTs; 6, 10, 12, 14, 15 and 20 the prime-factor split into two
+// coprime factors (dft_pfa); 3, 5, 7, 11 and 13 pair x_u with x_{R-u}:
 //   X_v = x_0 + sum_{u<=(R-1)/2} [(x_u + x_{R-u}) cos(2 pi uv/R)
 //                                 + DIR i (x_u - x_{R-u}) sin(2 pi uv/R)],
 // and X_{R-v} the same with the sine term negated.
@@ -112,36 +112,59 @@ template <int R, int DIR, typename V> __device__ __forceinline__ void dft_odd(V 
   }
 }
 
-// In-register DFT of length 15 = 3 * 5 by the prime-factor mapping (the
-// factors are coprime, so no twiddles sit between the two sub-transforms):
-// with u = (5 n1 + 3 n2) mod 15 and v = (10 k1 + 6 k2) mod 15,
-//   u v = 5 n1 k1 + 3 n2 k2 (mod 15)   (10 = 5 * (5^-1 mod 3), 6 = 3 * (3^-1 mod 5)),
-// so X_v = sum_{n2} W_5^{n2 k2} sum_{n1} W_3^{n1 k1} x_u: five 3-point DFTs,
-// then three 5-point DFTs, the index maps being register renaming only.
-template <int DIR, typename V> __device__ __forceinline__ void dft15(V *x) {
-  V a[5][3];
-#pragma unroll
-  for (int n2 = 0; n2 < 5; ++n2)
-#pragma unroll
-    for (int n1 = 0; n1 < 3; ++n1) a[n2][n1] = x[(5 * n1 + 3 * n2) % 15];
-#pragma unroll
-  for (int n2 = 0; n2 < 5; ++n2) dft_odd<3, DIR>(a[n2]);
-  V b[3][5];
-#pragma unroll
-  for (int k1 = 0; k1 < 3; ++k1)
-#pragma unroll
-    for (int n2 = 0; n2 < 5; ++n2) b[k1][n2] = a[n2][k1];
-#pragma unroll
-  for (int k1 = 0; k1 < 3; ++k1) dft_odd<5, DIR>(b[k1]);
-#pragma unroll
-  for (int k1 = 0; k1 < 3; ++k1)
-#pragma unroll
-    for (int k2 = 0; k2 < 5; ++k2) x[(10 * k1 + 6 * k2) % 15] = b[k1][k2];
+// (a^-1 mod m) for coprime a, m (compile time).
+__host__ __device__ constexpr int inv_mod(int a, int m) {
+  for (int x = 1; x < m; ++x)
+    if ((a * x) % m == 1) return x;
+  return 1;
 }
 
+template <int R, int DIR, typename V> __device__ __forceinline__ void dft_any(V *x);
+
+// In-register DFT of length R = R1 * R2, R1 and R2 coprime, by the
+// prime-factor (Good-Thomas) mapping: with input index
+// u = (R2 n1 + R1 n2) mod R and output index v = (e1 k1 + e2 k2) mod R,
+// e1 = R2 (R2^-1 mod R1), e2 = R1 (R1^-1 mod R2), the exponent is
+//   u v = R2 e1 n1 k1 + R1 e2 n2 k2 (mod R),
+// and W_R^{R2 e1 n1 k1} = W_{R1}^{n1 k1}, W_R^{R1 e2 n2 k2} = W_{R2}^{n2 k2},
+// so X_v = sum_{n2} W_{R2}^{n2 k2} sum_{n1} W_{R1}^{n1 k1} x_u: R2 DFTs of
+// length R1, then R1 of length R2, with no twiddle between them; the index
+// maps are register renaming only (15 = 3 * 5: u = (5 n1 + 3 n2) mod 15,
+// v = (10 k1 + 6 k2) mod 15).
+template <int R1, int R2, int DIR, typename V> __device__ __forceinline__ void dft_pfa(V *x) {
+  constexpr int R = R1 * R2;
+  constexpr int E1 = R2 * inv_mod(R2 % R1, R1);
+  constexpr int E2 = R1 * inv_mod(R1 % R2, R2);
+  V a[R2][R1];
+#pragma unroll
+  for (int n2 = 0; n2 < R2; ++n2)
+#pragma unroll
+    for (int n1 = 0; n1 < R1; ++n1) a[n2][n1] = x[(R2 * n1 + R1 * n2) % R];
+#pragma unroll
+  for (int n2 = 0; n2 < R2; ++n2) dft_any<R1, DIR>(a[n2]);
+  V b[R1][R2];
+#pragma unroll
+  for (int k1 = 0; k1 < R1; ++k1)
+#pragma unroll
+    for (int n2 = 0; n2 < R2; ++n2) b[k1][n2] = a[n2][k1];
+#pragma unroll
+  for (int k1 = 0; k1 < R1; ++k1) dft_any<R2, DIR>(b[k1]);
+#pragma unroll
+  for (int k1 = 0; k1 < R1; ++k1)
+#pragma unroll
+    for (int k2 = 0; k2 < R2; ++k2) x[(E1 * k1 + E2 * k2) % R] = b[k1][k2];
+}
+
+// The stage radices: powers of two up to 16 (dft_reg), odd primes up to
+// 13 (dft_odd) and the coprime products 6, 10, 12, 14, 15, 20 (dft_pfa).
 template <int R, int DIR, typename V> __device__ __forceinline__ void dft_any(V *x) {
   if constexpr (R == 3 || R == 5 || R == 7 || R == 11 || R == 13) dft_odd<R, DIR>(x);
-  else if constexpr (R == 15) dft15<DIR>(x);
+  else if constexpr (R == 6) dft_pfa<2, 3, DIR>(x);
+  else if constexpr (R == 10) dft_pfa<2, 5, DIR>(x);
+  else if constexpr (R == 12) dft_pfa<4, 3, DIR>(x);
+  else if constexpr (R == 14) dft_pfa<2, 7, DIR>(x);
+  else if constexpr (R == 15) dft_pfa<3, 5, DIR>(x);
+  else if constexpr (R == 20) dft_pfa<4, 5, DIR>(x);
   else dft_reg<R, DIR>(x);
 }
 
@@ -215,7 +238,12 @@ __device__ __forceinline__ void mixed_stage_any(const V *src, V *dst, const Mixe
     case 11: mixed_stage<11, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
     case 13: mixed_stage<13, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
     case 8: mixed_stage<8, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
+    case 6: mixed_stage<6, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
+    case 10: mixed_stage<10, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
+    case 12: mixed_stage<12, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
+    case 14: mixed_stage<14, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
     case 15: mixed_stage<15, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
+    case 20: mixed_stage<20, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
     default: mixed_stage<16, DIR, LAST>(src, dst, ms, k, t, rows, scale); break;
   }
 }
@@ -270,7 +298,12 @@ __device__ __forceinline__ void mixed_first_stage_any(const V *g, V *dst, const 
     case 11: mixed_first_stage<11, DIR>(g, dst, ms, rows); break;
     case 13: mixed_first_stage<13, DIR>(g, dst, ms, rows); break;
     case 8: mixed_first_stage<8, DIR>(g, dst, ms, rows); break;
+    case 6: mixed_first_stage<6, DIR>(g, dst, ms, rows); break;
+    case 10: mixed_first_stage<10, DIR>(g, dst, ms, rows); break;
+    case 12: mixed_first_stage<12, DIR>(g, dst, ms, rows); break;
+    case 14: mixed_first_stage<14, DIR>(g, dst, ms, rows); break;
     case 15: mixed_first_stage<15, DIR>(g, dst, ms, rows); break;
+    case 20: mixed_first_stage<20, DIR>(g, dst, ms, rows); break;
     default: mixed_first_stage<16, DIR>(g, dst, ms, rows); break;
   }
 }
