@@ -36,9 +36,9 @@ def draw_length(g, cap_other=3000, cap_pow2=1 << 16):
     kind = g.integers(0, 4)
     if kind == 0:
         return int(1 << g.integers(0, cap_pow2.bit_length()))
-    if kind == 1:   # smooth: 2^a 3^b 5^c 7^d
+    if kind == 1:   # smooth: 2^a 3^b 5^c 7^d 11^e 13^f
         n = 1
-        for f, e in ((2, 6), (3, 4), (5, 3), (7, 2)):
+        for f, e in ((2, 6), (3, 4), (5, 3), (7, 2), (11, 1), (13, 1)):
             n *= f ** int(g.integers(0, e + 1))
         return int(min(n, cap_other)) if n <= cap_other else 3 * 5 * 7
     return int(g.integers(1, cap_other + 1))
