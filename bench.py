@@ -269,6 +269,10 @@ def kernel_source_hash(config: str) -> str:
 
 
 def committed_traffic(config: str):
+    # The counters belong to the workload as captured: none for a resized
+    # workload (--n / --batch) or one run with forced library choices.
+    if SIZE_OVERRIDE or OPTIONS:
+        return None
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:

@@ -49,3 +49,20 @@ def test_roofline_byte_accounting():
     L = 1 << 21
     assert c5["flops_per_step"] == 3 * 5.0 * L * 21 * 64
     assert c5["fp64_flops_per_step"] == (5.0 * L * 21 + 5.0 * (L // 2) * 20) * 64
+
+
+def test_traffic_only_for_the_captured_workload():
+    # The committed DRAM counters describe each workload at its own size
+    # with the library's own choices; a resized run or one with forced
+    # options reports none.
+    ent = bench.committed_traffic("c2")
+    assert ent is not None and ent["traffic_bytes_per_launch"] > 0
+    bench.SIZE_OVERRIDE.update(n=1024, batch=4)
+    assert bench.committed_traffic("c2") is None
+    bench.SIZE_OVERRIDE.clear()
+    bench.OPTIONS.append("PASS_SHFL=1")
+    try:
+        assert bench.committed_traffic("c2") is None
+    finally:
+        bench.OPTIONS.remove("PASS_SHFL=1")
+    assert bench.committed_traffic("c2") is not None
