@@ -26,6 +26,7 @@ from __future__ import annotations
 import argparse
 import concurrent.futures as cf
 import hashlib
+import itertools
 import json
 import math
 import os
@@ -399,24 +400,29 @@ def _oracle_units(name: str):
         "fp64 FFT products of 2^16-coefficient pairs, scaled by L log2 L to 2^20"
 
 
-def cpu_oracle_sample(name: str, budget_s: float = 6.0, threads: int = 1):
+def cpu_oracle_sample(name: str, budget_s: float = 6.0, threads: int = 1,
+                      max_fraction: float = None):
     """Times the fp64 oracle as it stands on a bounded sample of the
-    workload (about `budget_s` seconds) on `threads` host threads -- units of
-    work run concurrently, each a plain call into the oracle's C code, which
-    releases the interpreter lock -- and scales to the metric's unit."""
+    workload (about `budget_s` seconds, and at most `max_fraction` of one
+    step's work when given) on `threads` host threads -- units of work run
+    concurrently, each a plain call into the oracle's C code, which releases
+    the interpreter lock -- and scales to the metric's unit."""
     info = workload_info(name)
     unit, frac, what = _oracle_units(name)
     unit(0)  # first-call set-up (library load) outside the timed sample
+    limit = None if max_fraction is None else max(1, int(round(max_fraction / frac)))
     done = [0] * threads
+    next_unit = itertools.count()  # shared by the workers (atomic under the GIL)
     t0 = time.perf_counter()
     deadline = t0 + budget_s
 
     def worker(w):
-        k = w
         while True:
+            k = next(next_unit)
+            if limit is not None and k >= limit:
+                return
             unit(k)
             done[w] += 1
-            k += threads
             if time.perf_counter() >= deadline:
                 return
     if threads == 1:
@@ -1006,10 +1012,11 @@ def workload_label(name: str) -> str:
 # ---------------------------------------------------------------------------
 
 def run_reference(args):
-    """The fp64 CPU oracle as it stands, on every host core: each step is a
-    bounded sample (about --ref-step-seconds) of the workload's work, and
-    the line reports the rate over the sampled work, the sampled fraction of
-    a full step, and the wall time actually spent."""
+    """The fp64 CPU oracle as it stands, on every host core: each step runs
+    the workload's work, or a bounded sample of it (about --ref-step-seconds)
+    when the whole step would take longer; the line reports the rate over
+    the work done, the fraction of a full step each timed step covered, and
+    the wall time actually spent."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
@@ -1020,7 +1027,8 @@ def run_reference(args):
     cores = host_cores()
 
     def one_step():
-        return cpu_oracle_sample(name, budget_s=args.ref_step_seconds, threads=cores)
+        return cpu_oracle_sample(name, budget_s=args.ref_step_seconds, threads=cores,
+                                 max_fraction=1.0)
     t_all = time.perf_counter()
     for _ in range(args.warmup):
         one_step()
@@ -1041,12 +1049,13 @@ def run_reference(args):
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        # Wall time of one timed (sampled) step; the sampled work is
-        # `sample_fraction` of a full step.
+        # Wall time of one timed step; its work is `sample_fraction` of a
+        # full step (1 when the whole step ran), the full-step time
+        # extrapolated only when it is less.
         "ms_per_step": round(ms_step, 2),
         "sample_fraction": float(f"{done / args.steps:.4g}"),
-        "extrapolated": {"ms_per_full_step": round(ms_step * args.steps / done, 2)
-                         if done > 0 else None},
+        "extrapolated": ({"ms_per_full_step": round(ms_step * args.steps / done, 2)}
+                         if 0 < done < args.steps * 0.9999 else None),
         "wall_s": {"timed": round(wall, 2), "total": round(time.perf_counter() - t_all, 2)},
         "higher_is_better": True,
         "scaling": "weak",
