@@ -713,21 +713,27 @@ fft_plan *fft_plan_create_nd(int rank, const int64_t *shape, int64_t batch, int 
   p->batch = batch;
   p->direction = direction;
   p->dtype = dtype;
-  // Columns of 1024 or 2048 points: fold the first radix-R stage (R = 2, 4)
-  // of the column transform into the row pass so that the column pass
-  // transforms 512-point columns of R times wider rows (out-of-place
-  // execution only), where the row pass keeps blocks of at most 512
-  // threads.  Measured on GB300 (fp32, forward + inverse, ms): 1024^2 x 32
-  // 0.404 unfolded, 0.366 R = 2, 0.382 R = 4; 2048^2 x 8 0.427 unfolded,
-  // 0.441 R = 2, 0.420 R = 4, 0.503 R = 8 (and 0.444 with R = 4 split over
-  // a cluster of two 256-thread blocks); 4096^2 x 2 keeps its cluster column
-  // pass (0.530 unfolded, 0.531 R = 8).
+  // Columns of 1024 to 8192 points: fold the first radix-R stage of the
+  // column transform into the row pass so that the column pass transforms
+  // columns R times shorter of R times wider rows (out-of-place execution
+  // only).  1024 and 2048 points take R = 2 and 4 (512-point column
+  // passes) where the row pass keeps blocks of at most 512 threads; 4096
+  // and 8192 points take R = 4 (1024- and 2048-point column passes instead
+  // of cluster passes) where that holds, else R = 2.  Measured on GB300
+  // (fp32, forward + inverse, ms): 1024^2 x 32 0.404 unfolded, 0.366 R = 2,
+  // 0.382 R = 4; 2048^2 x 8 0.427 unfolded, 0.441 R = 2, 0.420 R = 4, 0.503
+  // R = 8 (and 0.444 with R = 4 split over a cluster of two 256-thread
+  // blocks); 4096 x 256 x 16 0.264 unfolded, 0.214 R = 2, 0.208 R = 4;
+  // 4096 x 1024 x 4 0.270, 0.224, 0.215; 4096^2 x 2 0.527, 0.458, 0.486;
+  // 8192 x 1024 x 2 0.295, 0.271, 0.226; 8192 x 2048 0.292, 0.271, 0.231;
+  // fp64 8192 x 512 x 2 3.15, 3.11, 2.89.
   if (!p->nd_rows_t) {
     const int logh = logs[rank - 2], logw = logs[rank - 1];
     const long long forced = option(FFT_OPT_COL_RADIX_LOG);
     int logr = 0;
     if (forced >= 0) logr = (int)forced;
     else if ((logh == 10 || logh == 11) && logw >= 4 && (logh - 9) + logw - 4 <= 9) logr = logh - 9;
+    else if (logh == 12 || logh == 13) logr = 2 + logw - 4 <= 9 ? 2 : 1;
     if (logr >= 1 && logr < logh && rows_col_supported(dtype == FFT_C2C_F64, logw, logr))
       p->col_radix_log = logr;
   }

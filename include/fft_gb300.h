@@ -427,7 +427,8 @@ int fft_debug_cluster_timeout(void *data, int64_t polls, void *stream);
 #define FFT_OPT_COL_RADIX_LOG 7   /* planning: 2D / 3D, out of place: log2 of the radix of the
                                      column transform's first stage folded into the row pass
                                      (0 = none, 1 .. 3); own choice log2(H / 512) for columns
-                                     of 1024 and 2048 points (blocks of at most 512 threads) */
+                                     of 1024 and 2048 points (blocks of at most 512 threads),
+                                     2 (1 for rows of 4096 points) for 4096 and 8192 */
 #define FFT_OPT_ROWS_SHFL 8       /* launch: 1 = 512-point on-chip transforms exchange data
                                      between stages by warp shuffles (one warp per transform)
                                      instead of shared memory; own choice 0 */

@@ -308,13 +308,16 @@ def test_nd_forward_inverse(fg, dtype, shape):
 
 
 # Columns of 1024 points or more, out of place: the row pass also takes the
-# first radix-R stage of the column transform (R = H / 512) and the column
-# pass transforms 512-point columns R W apart.  In place the plan keeps rows
-# plus a full column pass; both schedules are checked against the oracle.
+# first radix-R stage of the column transform (R = H / 512 up to 2048
+# points, R = 4 or 2 for 4096 and 8192) and the column pass transforms
+# columns H / R long, R W apart.  In place the plan keeps rows plus a full
+# column pass; both schedules are checked against the oracle.
 @pytest.mark.parametrize("dtype,shape,batch", [
     (F32, (1024, 256), 3), (F32, (2048, 256), 2), (F64, (2048, 256), 2), (F32, (4096, 256), 1),
     (F64, (4096, 256), 1), (F32, (2048, 2048), 2), (F32, (4096, 1024), 1), (F32, (1024, 4096), 1),
-    (F64, (1024, 2048), 1), (F32, (2, 1024, 256), 2), (F64, (4, 2048, 512), 1)])
+    (F64, (1024, 2048), 1), (F32, (2, 1024, 256), 2), (F64, (4, 2048, 512), 1),
+    (F32, (4096, 4096), 1), (F32, (8192, 1024), 1), (F32, (8192, 256), 2), (F64, (8192, 512), 1),
+    (F32, (2, 4096, 256), 1)])
 def test_nd_folded_column_radix(fg, dtype, shape, batch):
     x = workloads.normal_complex((batch,) + shape, 3600 + sum(shape), NP[dtype])
     npts = int(np.prod(shape))
