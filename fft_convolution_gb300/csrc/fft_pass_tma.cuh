@@ -7,10 +7,10 @@
 //   * persistent blocks (as many as fit per SM), each walking the tiles
 //     blockIdx.x, blockIdx.x + gridDim.x, ...;
 //   * the input tile (L rows x C columns, rows 8*cols bytes apart) arrives
-//     by cp.async.bulk.tensor into one of two shared-memory buffers, tracked
-//     by an mbarrier, while the block computes the previous tile from the
-//     other buffer -- HBM reads overlap the arithmetic inside one block and
-//     the load/store units carry only the shared-memory exchanges;
+//     by cp.async.bulk.tensor into one of up to three shared-memory buffers,
+//     tracked by an mbarrier, up to two tiles ahead of the one the block
+//     computes -- HBM reads overlap the arithmetic inside one block and the
+//     load/store units carry only the shared-memory exchanges;
 //   * outputs of passes with m > 1 (rows m elements apart) leave by a TMA
 //     tensor store from the same buffer; the first pass (m = 1), whose tile
 //     output is one contiguous block, stages it column by column and
@@ -216,7 +216,6 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL, SHFL>::THREADS,
   const int tid = threadIdx.x;
   const int c = tid % C;
   const int t = tid / C;
-  const long long cols = 1LL << (g.log_n - LOGL);
 
   auto issue_load = [&](long long tile, int s) {
     const long long b = tile >> g.log_tpb;
@@ -414,7 +413,6 @@ __global__ void __launch_bounds__(TmaConfig<T, LOGL, SHFL>::THREADS,
     }
   }
   if (tid < C) bulk_wait_all();
-  (void)cols;
 }
 
 // ---------------------------------------------------------------------------
