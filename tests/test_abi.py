@@ -106,7 +106,10 @@ def test_debug_set_option_checks(fg):
     assert fg.fft_debug_set_option(fg.FFT_OPT_CLUSTER_LOG_MIN, 10) == fg.FFT_ERR_INVALID_ARG
     assert fg.fft_debug_set_option(fg.FFT_OPT_COL_RADIX_LOG, 4) == fg.FFT_ERR_INVALID_ARG
     assert fg.fft_debug_set_option(fg.FFT_OPT_NO_TMA, 2) == fg.FFT_ERR_INVALID_ARG
-    for code in range(1, 9):
+    assert fg.fft_debug_set_option(fg.FFT_OPT_ROWS_SHFL, 2) == fg.FFT_ERR_INVALID_ARG
+    assert fg.fft_debug_set_option(fg.FFT_OPT_PASS_SHFL, 2) == fg.FFT_ERR_INVALID_ARG
+    assert fg.fft_debug_set_option(fg.FFT_OPT_PASS_SHFL + 1, 0) == fg.FFT_ERR_INVALID_ARG
+    for code in range(1, fg.FFT_OPT_PASS_SHFL + 1):
         assert fg.fft_debug_set_option(code, -1) == fg.FFT_OK
     assert fg.pass_split_value([9, 9, 8]) == 9 | 9 << 4 | 8 << 8
 
