@@ -262,6 +262,23 @@ static bool mixed_stages(int64_t n, int elem, MixedStages *ms) {
   if (single2 > 1 && k < 64) radix[k++] = single2;
   for (int j = 0; j < a / 4 && k < 64; ++j) radix[k++] = 16;
   if (k > 16) return false;
+  // The last stage writes global memory in runs of m = N / R consecutive
+  // values.  When a prime-factor last stage writes runs shorter than 16
+  // values and moving the largest radix to the front lengthens them to 16
+  // or more, do so.  Measured (fp32, forward + inverse of 131072
+  // transforms, ms): 100 = 5 * 20 0.121, as 20 * 5 0.095; 96 = 6 * 16
+  // 0.107, as 16 * 6 0.144 (so a power-of-two last stage stays).
+  if (k >= 2 && n / radix[k - 1] < 16 && (radix[k - 1] & (radix[k - 1] - 1)) != 0) {
+    int big = 0;
+    for (int j = 1; j < k; ++j)
+      if (radix[j] > radix[big]) big = j;
+    const int last = big == k - 1 ? radix[k - 2] : radix[k - 1];
+    if (big != 0 && n / last >= 16) {
+      const int rb = radix[big];
+      for (int j = big; j > 0; --j) radix[j] = radix[j - 1];
+      radix[0] = rb;
+    }
+  }
   memset(ms, 0, sizeof(*ms));
   ms->N = (int)n;
   ms->nstages = k;
