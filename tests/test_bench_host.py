@@ -66,3 +66,14 @@ def test_traffic_only_for_the_captured_workload():
     finally:
         bench.OPTIONS.remove("PASS_SHFL=1")
     assert bench.committed_traffic("c2") is not None
+
+
+def test_reference_step_is_capped_at_one_full_step():
+    # The reference arm runs a whole step when it fits the time budget and
+    # never more: c1 is one 1024-point transform, so one unit is the step.
+    r = bench.cpu_oracle_sample("c1", budget_s=5.0, threads=2, max_fraction=1.0)
+    assert r["step_fraction"] == 1.0
+    assert r["sample"].startswith("1 ")
+    # Without the cap the same budget runs many steps' worth of units.
+    r = bench.cpu_oracle_sample("c1", budget_s=0.2, threads=1)
+    assert r["step_fraction"] > 1.0
